@@ -1,0 +1,468 @@
+"""Benchmark of the 4-bit weight-only decode GEMV on one GB300 (or N replicas).
+
+Default workload: NVFP4 weight-only GEMV at batch 1, K=2048 -> N=16384 (seeded
+synthetic weights: E2M1 codes uniform over 16 values, e4m3 group-16 scales from
+U[0.25, 4], global scale 1e-2; x ~ N(0,1) in bf16).  One step is one call of the
+whole path (E2M1/e4m3 decode, dot products, split-K fixup, bf16 store).
+
+Timing: the calls rotate over enough copies of the weights to cover 4x the L2
+cache, so every call streams its weights from HBM.  W warm-up steps, then K timed
+steps, replayed from CUDA graphs and bracketed by CUDA events on the launching
+stream with a barrier + synchronize on both sides; the max over ranks is taken.
+`value` is the effective weight bandwidth (algorithmic bytes / time per call).
+The `e2e` key repeats the measurement through the same public call with the
+activations copied in from pinned host memory and the result copied back every
+step.  `--impl reference` times the CPU oracle on the host cores instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "4-bit decode GEMV µs/call & effective weight GB/s (% of GB300 HBM peak)"
+
+# DRAM traffic of one launch of the streaming kernel on the default workload, from
+# the ncu capture summarised in profiles/ (dram__bytes_read.sum +
+# dram__bytes_write.sum), valid only for the kernel source it was taken on.
+TRAFFIC = {
+    # workload key: (bytes per launch, sha256 of csrc/gemv.cu when captured)
+}
+
+WORKLOADS = ("nvfp4_gemv", "int4_gemv", "decode_step", "batched", "prefill")
+
+
+# ---------------------------------------------------------------- helpers
+def _dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def max_over_ranks(value: float, world: int) -> float:
+    """Max of a per-rank float over all ranks (identity for one process)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int) -> None:
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def _src_sha(rel: str) -> str:
+    with open(os.path.join(ROOT, rel), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during a region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.lines: list[str] = []
+        self.t = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", self.gpu_id],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+            time.sleep(0.3)
+        except (OSError, ValueError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            if self.t is not None:
+                self.t.join(timeout=2)
+
+    def summary(self) -> dict:
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------ workloads
+class Workload:
+    """Seeded inputs on the device, a ring of weight copies and one call per step."""
+
+    def __init__(self, name: str, device):
+        import torch
+        from bit_weight_only_q4_gb300 import layout, q4, synth
+        from tests import parity as P
+        self.name = name
+        self.torch = torch
+        self.q4 = q4
+        self.device = device
+        l2 = torch.cuda.get_device_properties(device).L2_cache_size
+        self.kernel_launches_per_step = 1
+        if name == "nvfp4_gemv":
+            c = synth.NVFP4_GEMV_16384
+            x, w = synth.nvfp4_gemv_16384()
+            self.M, self.N, self.K = c["M"], c["N"], c["K"]
+            self.layout = "nvfp4"
+            self.desc = c["name"]
+            base = P.nvfp4_dev(w)
+        elif name == "int4_gemv":
+            c = synth.INT4_GEMV_2048
+            x, w = synth.int4_gemv_2048()
+            self.M, self.N, self.K = c["M"], c["N"], c["K"]
+            self.layout = "int4"
+            self.desc = c["name"]
+            base = P.int4_dev(w)
+        else:
+            raise ValueError(f"workload {name} is not a bench line of this build")
+        self.x_host_bits = x
+        self.x = P.bf16_dev(x).to(device)
+        self.bytes_per_call = layout.linear_bytes(self.layout, self.M, self.N, self.K)
+        wbytes = layout.weight_bytes(self.layout, self.N, self.K)
+        self.copies = max(2, math.ceil(4 * l2 / wbytes))
+        self.ring = [tuple(t.to(device).clone() for t in base) for _ in range(self.copies)]
+        self.y = torch.empty((self.M, self.N), dtype=torch.bfloat16, device=device)
+        lay = q4.LAYOUT_NVFP4 if self.layout == "nvfp4" else q4.LAYOUT_INT4G128
+        self.ws = q4.alloc_workspace(lay, self.M, self.N, self.K, device)
+        self.ring_bytes = self.copies * wbytes
+        self.l2 = l2
+
+    def call(self, i: int, x=None, y=None):
+        w = self.ring[i % self.copies]
+        x = self.x if x is None else x
+        y = self.y if y is None else y
+        if self.layout == "nvfp4":
+            self.q4.q4_linear_nvfp4(x, *w, y=y, workspace=self.ws)
+        else:
+            self.q4.q4_linear_int4g128(x, *w, y=y, workspace=self.ws)
+
+
+def _capture(torch, fn, n: int, stream):
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(n):
+                fn(i)
+    return g
+
+
+def _time_graphs(torch, stream, graphs, world):
+    """Replay graphs [(graph, times)] between two events; returns elapsed ms."""
+    barrier(world)
+    torch.cuda.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    with torch.cuda.stream(stream):
+        for g, times in graphs:
+            for _ in range(times):
+                g.replay()
+    end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    return start.elapsed_time(end)
+
+
+def run_profile(args, local):
+    """Plain launches for an ncu capture: W warm-up calls, then K calls, no graphs
+    and no timing (a number printed under a profiler is never a bench value)."""
+    import torch
+    from bit_weight_only_q4_gb300 import build as libbuild
+    from bit_weight_only_q4_gb300 import q4
+    torch.cuda.set_device(local)
+    libbuild.build()
+    q4.load()
+    q4.set_launch_flags(0)
+    wl = Workload(args.workload, torch.device("cuda", local))
+    for i in range(args.warmup + args.steps):
+        wl.call(i)
+    torch.cuda.synchronize()
+    print(json.dumps({"profile_run": wl.desc, "calls": args.warmup + args.steps}))
+
+
+def run_gpu(args, world, rank, local):
+    import torch
+    from bit_weight_only_q4_gb300 import build as libbuild
+    from bit_weight_only_q4_gb300 import q4
+
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if rank == 0:
+        libbuild.build()
+    barrier(world)
+    libbuild.build()
+    q4.load()
+    q4.set_launch_flags(q4.FLAG_PDL if not args.no_pdl else 0)
+    wl = Workload(args.workload, device)
+    stream = torch.cuda.Stream(device)
+    R = wl.copies
+    K, W = args.steps, args.warmup
+
+    # warm-up (also the first, uncaptured calls: plans and attributes cached)
+    with torch.cuda.stream(stream):
+        for i in range(max(W, 1)):
+            wl.call(i)
+    torch.cuda.synchronize()
+    g_ring = _capture(torch, wl.call, R, stream)
+    g_tail = _capture(torch, wl.call, K % R, stream) if K % R else None
+    g_warm = _capture(torch, wl.call, W % R, stream) if W % R else None
+    warm = [(g_ring, W // R)] + ([(g_warm, 1)] if g_warm else [])
+    timed = [(g_ring, K // R)] + ([(g_tail, 1)] if g_tail else [])
+    _time_graphs(torch, stream, warm, world)
+
+    props = torch.cuda.get_device_properties(device)
+    gpu_id = str(getattr(props, "uuid", local))
+    if gpu_id and not gpu_id.startswith("GPU-") and "-" in gpu_id:
+        gpu_id = "GPU-" + gpu_id
+    with ClockSampler(gpu_id) as clk:
+        ms = _time_graphs(torch, stream, timed, world)
+    ms = max_over_ranks(ms, world)
+    clocks = clk.summary()
+
+    # end to end through the public call: pinned host x in, y back, every step
+    xh = torch.empty_like(wl.x, device="cpu").pin_memory()
+    xh.copy_(wl.x.cpu())
+    yh = torch.empty((wl.M, wl.N), dtype=torch.bfloat16).pin_memory()
+    xd = torch.empty_like(wl.x)
+
+    def e2e_step(i):
+        xd.copy_(xh, non_blocking=True)
+        wl.call(i, x=xd)
+        yh.copy_(wl.y, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            e2e_step(i)
+    torch.cuda.synchronize()
+    Ke = max(R, min(K, 20000))
+    ge = _capture(torch, e2e_step, R, stream)
+    ge_tail = _capture(torch, e2e_step, Ke % R, stream) if Ke % R else None
+    e2e_ms = _time_graphs(torch, stream, [(ge, Ke // R)] + ([(ge_tail, 1)] if ge_tail else []),
+                          world)
+    e2e_ms = max_over_ranks(e2e_ms, world)
+
+    us_per_call = ms * 1e3 / K
+    gbs = wl.bytes_per_call / (us_per_call * 1e-6) / 1e9
+    e2e_us = e2e_ms * 1e3 / Ke
+    e2e_gbs = wl.bytes_per_call / (e2e_us * 1e-6) / 1e9
+    peak, peak_src = _peaks()
+    traffic = None
+    t = TRAFFIC.get(args.workload)
+    if t and t[1] == _src_sha("bit_weight_only_q4_gb300/csrc/gemv.cu"):
+        traffic = t[0]
+
+    cpu_baseline = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu_baseline = time_oracle(wl.name, budget_s=args.cpu_seconds)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC,
+            "value": round(gbs * world, 2),
+            "unit": "GB/s",
+            "us_per_call": round(us_per_call, 4),
+            "hbm_frac": round(gbs / peak, 4),
+            "n_gpus": world,
+            "steps": K,
+            "warmup": W,
+            "ms_per_step": round(ms / K, 6),
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "f32",
+            "data": "synthetic (seeded PCG64; shapes and distributions of the workload)",
+            "config": {
+                "workload": wl.desc,
+                "layout": wl.layout, "M": wl.M, "N": wl.N, "K": wl.K,
+                "algorithmic_bytes_per_call": wl.bytes_per_call,
+                "l2": f"weights rotate over {wl.copies} copies "
+                      f"({wl.ring_bytes / 1e6:.0f} MB, >= 4x the {wl.l2 / 1e6:.0f} MB L2)",
+                "graph": "CUDA graph replay, one call per step",
+                "pdl": not args.no_pdl,
+                "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
+            },
+            "roofline": {
+                "bound": "hbm",
+                "achieved": round(gbs, 2),
+                "peak": peak,
+                "unit": "GB/s",
+                "frac": round(gbs / peak, 4),
+                "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
+                else "fallback 6.8 TB/s",
+                "traffic": traffic,
+            },
+            "e2e": {
+                "value": round(e2e_gbs * world, 2),
+                "unit": "GB/s",
+                "us_per_call": round(e2e_us, 4),
+                "h2d_bytes_per_step": int(wl.x.numel() * 2),
+                "d2h_bytes_per_step": int(wl.M * wl.N * 2),
+                "steps": Ke,
+            },
+            "gpu_launches": K * wl.kernel_launches_per_step,
+            "clocks": clocks,
+            "cpu_baseline": cpu_baseline,
+        }
+        print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------- CPU oracle
+def time_oracle(workload: str, budget_s: float = 12.0, steps: int | None = None) -> dict:
+    """Time the CPU oracle (as it stands) on a bounded sample of the workload."""
+    import numpy as np
+    import oracle
+    from bit_weight_only_q4_gb300 import layout, synth
+    if workload == "nvfp4_gemv":
+        x, w = synth.nvfp4_gemv_16384()
+        N, K, lay = w.N, w.K, "nvfp4"
+
+        def run(rows):
+            oracle.linear_nvfp4(x, w.codes[:rows], w.scale[:rows], w.global_scale)
+    else:
+        x, w = synth.int4_gemv_2048()
+        N, K, lay = w.N, w.K, "int4"
+
+        def run(rows):
+            oracle.linear_int4g128(x, w.qweight[:rows], w.scale[:rows], w.minv[:rows])
+    oracle.build()
+    run(min(N, 256))
+    t0 = time.perf_counter()
+    run(N)
+    t_full = time.perf_counter() - t0
+    if steps is None:
+        calls = max(1, int(budget_s / max(t_full, 1e-6)))
+        rows = N
+    else:
+        # each step a bounded sample of rows: the whole run stays within budget_s
+        per_step = budget_s / max(steps, 1)
+        rows = int(max(64, min(N, N * per_step / max(t_full, 1e-9))))
+        calls = steps
+    t0 = time.perf_counter()
+    for _ in range(calls):
+        run(rows)
+    dt = time.perf_counter() - t0
+    us_per_call = dt / calls * (N / rows) * 1e6
+    gbs = layout.linear_bytes(lay, 1, N, K) / (us_per_call * 1e-6) / 1e9
+    return {"value": round(gbs, 4), "unit": "GB/s", "us_per_call": round(us_per_call, 2),
+            "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{calls} oracle calls on {rows} of {N} rows (K={K}), "
+                      f"time scaled to all rows; {dt:.1f} s"}
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    wl_desc = {"nvfp4_gemv": "nvfp4 GEMV M=1 N=16384 K=2048",
+               "int4_gemv": "int4-g128 GEMV M=1 N=2048 K=2048"}[args.workload]
+    budget = min(150.0, max(10.0, 2.0 * (args.steps + args.warmup)))
+    cb = time_oracle(args.workload, budget_s=budget, steps=args.steps)
+    line = {
+        "metric": METRIC, "impl": "reference", "value": cb["value"], "unit": "GB/s",
+        "us_per_call": cb["us_per_call"], "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": cb["us_per_call"] / 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded PCG64)",
+        "config": {"workload": wl_desc},
+        "cpu_baseline": cb,
+        "e2e": {"value": cb["value"], "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200000)
+    ap.add_argument("--warmup", type=int, default=2000)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", choices=("nvfp4_gemv", "int4_gemv"), default="nvfp4_gemv")
+    ap.add_argument("--no-pdl", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--profile", action="store_true",
+                    help="plain launches for an ncu capture (no timing output)")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world, rank, local = _dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if args.impl == "ours" else "gloo"
+        if backend == "nccl":
+            import torch
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    try:
+        if args.impl == "reference":
+            run_reference(args, world, rank)
+        elif args.profile:
+            run_profile(args, local)
+        else:
+            run_gpu(args, world, rank, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,160 @@
+/*
+ * q4.h -- C ABI of the GB300 (sm_103a) 4-bit weight-only linear library.
+ *
+ * Every entry point takes plain pointers and sizes.  Unless a comment says
+ * otherwise, pointers are DEVICE pointers, tensors are row-major and contiguous,
+ * the caller owns (allocates and frees) every buffer, and the library allocates
+ * nothing.  Calls are asynchronous on the given stream (`stream` is a
+ * cudaStream_t passed as void*; NULL means the legacy default stream) and issue
+ * no host synchronisation, so they can be recorded into a CUDA graph.
+ *
+ * Error behaviour: arguments are validated on the host before anything is
+ * launched.  A failed check returns a non-zero q4_status and launches nothing.
+ * A failed launch returns Q4_ERR_CUDA.  q4_last_error_string() gives the detail
+ * of the last failure on the calling host thread.
+ *
+ * Weight layouts (the two the source pages fix exactly):
+ *   int4-g128-minmax -- "rumik-oss-1-int4", section "Format
+ *     (rumik-int4-g128-minmax-v1)": qweight uint8 [N, K/2], two 4-bit codes per
+ *     byte, the low nibble holds the even column; scale and min fp16
+ *     [N, K/128]; w[n,k] = code[n,k] * scale[n,k/128] + min[n,k/128].
+ *     Codes are unsigned 0..15.
+ *   NVFP4 weight-only -- "VoxCPM2 NVFP4 (GPTQ)", section "NVFP4 settings":
+ *     E2M1 codes uint8 [N, K/2] (same nibble order as int4), float8_e4m3fn group
+ *     scales uint8 [N, K/16] (one per 16 columns), one fp32 global scale per
+ *     matrix which multiplies: w[n,k] = E2M1(code) * e4m3(scale[n,k/16]) * g.
+ *     Activations stay BF16 (there is no activation scale).
+ * Activations x and outputs y are bf16; accumulation is fp32 and the output is
+ * rounded to bf16 (round to nearest even).
+ */
+#ifndef Q4_GB300_H
+#define Q4_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define Q4_ABI_VERSION 1
+
+typedef enum {
+    Q4_OK = 0,
+    Q4_ERR_NULL = 1,       /* a required pointer is NULL                          */
+    Q4_ERR_SHAPE = 2,      /* a size is out of range or not a multiple it must be */
+    Q4_ERR_ALIGN = 3,      /* a pointer is not 16-byte aligned                    */
+    Q4_ERR_WORKSPACE = 4,  /* workspace too small (see q4_workspace_bytes)        */
+    Q4_ERR_ARG = 5,        /* any other invalid argument (row index, flag, ...)   */
+    Q4_ERR_CUDA = 6,       /* a CUDA runtime call or kernel launch failed         */
+    Q4_ERR_DEVICE = 7      /* the current device is not a compute-capability 10.3 GPU */
+} q4_status;
+
+/* Layout identifiers for q4_workspace_bytes. */
+#define Q4_LAYOUT_INT4G128 0
+#define Q4_LAYOUT_NVFP4 1
+
+/* Process-wide launch flags (q4_set_launch_flags).  Default: 0.
+ *   Q4_FLAG_PDL: launch with programmatic dependent launch.  A kernel may then
+ *     start reading its weights, scales and global scale before the previous
+ *     kernel on the stream has finished, so those buffers must not be written
+ *     by the immediately preceding kernel.  Activations, outputs and workspace
+ *     are touched only after the previous kernel has completed.
+ *   Q4_FLAG_FORCE_CUDA_CORE / Q4_FLAG_FORCE_TENSOR_CORE: override the choice of
+ *     kernel by M (testing and benchmarking only). */
+#define Q4_FLAG_PDL 0x1u
+#define Q4_FLAG_FORCE_CUDA_CORE 0x2u
+#define Q4_FLAG_FORCE_TENSOR_CORE 0x4u
+
+int q4_abi_version(void);
+const char *q4_status_string(q4_status s);
+/* Detail of the last non-OK status returned on this host thread ("" if none). */
+const char *q4_last_error_string(void);
+q4_status q4_set_launch_flags(unsigned flags);
+unsigned q4_get_launch_flags(void);
+
+/*
+ * Bytes of device workspace that q4_linear_int4g128 (layout 0) or
+ * q4_linear_nvfp4 (layout 1) needs for an [M,N,K] call on the current device
+ * (split-K partial sums, arrival counters, dequantised tiles for large M).
+ * The workspace must be zero-filled once after allocation; every call leaves
+ * its counters at zero again.  Calls that run concurrently must not share a
+ * workspace.  Returns 0 for invalid sizes.
+ */
+size_t q4_workspace_bytes(int layout, int M, int N, int K);
+
+/*
+ * y[M,N] = x[M,K] * W^T for the int4-g128-minmax layout.
+ *   x        bf16 [M, K]
+ *   qweight  uint8 [N, K/2]     low nibble = even column
+ *   scale    fp16 [N, K/128]
+ *   minv     fp16 [N, K/128]
+ *   y        bf16 [M, N]        written
+ * Requirements: M >= 1, N >= 1, K >= 128, K % 128 == 0; x, qweight, y and the
+ * workspace 16-byte aligned, scale/minv 2-byte aligned; workspace of at least
+ * q4_workspace_bytes(0, M, N, K) bytes (may be NULL when that is 0).
+ * M selects the kernel: a CUDA-core GEMV for small M, the tcgen05 tensor-core
+ * GEMM for larger M.
+ */
+q4_status q4_linear_int4g128(const void *x, const uint8_t *qweight, const void *scale,
+                             const void *minv, void *y, int M, int N, int K,
+                             void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * y[M,N] = x[M,K] * W^T for the NVFP4 weight-only layout.
+ *   x             bf16 [M, K]
+ *   codes         uint8 [N, K/2]   low nibble = even column, E2M1 (bit 3 = sign)
+ *   scale_e4m3    uint8 [N, K/16]  float8_e4m3fn bit patterns
+ *   global_scale  fp32 [1]         DEVICE pointer, multiplies every weight
+ *   y             bf16 [M, N]      written
+ * Requirements: M >= 1, N >= 1, K >= 16, K % 16 == 0; x, codes, y and the
+ * workspace 16-byte aligned; workspace as for q4_linear_int4g128 (layout 1).
+ */
+q4_status q4_linear_nvfp4(const void *x, const uint8_t *codes, const uint8_t *scale_e4m3,
+                          const float *global_scale, void *y, int M, int N, int K,
+                          void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Restricted output head -- "Rumik TTS Fast Inference", section "What Made It
+ * Faster" and Figure 3: project the hidden state only onto the rows of the
+ * current codebook (2,048 codes) plus the end token, 2,049 rows instead of the
+ * full vocabulary.
+ *   h          bf16 [M, H]
+ *   head       bf16 [R_total, H]   the (audio) head matrix, row-major
+ *   logits     bf16 [M, n_rows + (extra_row >= 0)]   written
+ * Column j < n_rows of logits is row (row_begin + j) of head; when
+ * extra_row >= 0 the last column is row extra_row (the end token).
+ * Requirements: M >= 1, H >= 8, H % 8 == 0, 0 <= row_begin,
+ * row_begin + n_rows <= R_total, -1 <= extra_row < R_total, at least one output
+ * column; h and head 16-byte aligned.  Uses no workspace.
+ */
+q4_status audio_head_logits_restricted(const void *h, const void *head, int R_total,
+                                       int row_begin, int n_rows, int extra_row,
+                                       void *logits, int M, int H, void *stream);
+
+/*
+ * Device-side error word of the current device.  Bit 0 (Q4_DEVERR_TIMEOUT) is set
+ * when a bounded wait inside a kernel gave up (a copy or a peer warp never
+ * arrived); the kernel then returned early and its output is not valid.  This
+ * call synchronises with the device (it is a diagnostic, not for the hot path);
+ * with clear != 0 the word is reset to zero afterwards.
+ */
+#define Q4_DEVERR_TIMEOUT 0x1u
+q4_status q4_device_error_flags(unsigned *flags, int clear);
+
+/*
+ * Test helpers: decode whole weight matrices to fp32 [N, K] with the same
+ * in-register decoders the linear kernels use.  Each weight is the exact value
+ * of the layout's formula rounded once to fp32.
+ */
+q4_status q4_dequant_int4g128_f32(const uint8_t *qweight, const void *scale,
+                                  const void *minv, float *w, int N, int K, void *stream);
+q4_status q4_dequant_nvfp4_f32(const uint8_t *codes, const uint8_t *scale_e4m3,
+                               const float *global_scale, float *w, int N, int K,
+                               void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* Q4_GB300_H */
