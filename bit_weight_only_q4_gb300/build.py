@@ -38,16 +38,25 @@ def _newest_header() -> float:
     return max((os.path.getmtime(h) for h in hdrs), default=0.0)
 
 
-def build(verbose: bool = False, jobs: int | None = None) -> str:
+def build(verbose: bool = False, jobs: int | None = None, defines: tuple[str, ...] = (),
+          out_dir: str | None = None, src_dir: str | None = None) -> str:
+    """Compile and link the library; ``defines`` (e.g. ``Q4_BULK_RW=2``),
+    ``out_dir`` and ``src_dir`` build a variant elsewhere without touching the
+    default build."""
     nvcc = _nvcc()
-    os.makedirs(OUT, exist_ok=True)
-    srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
-    hdr_time = _newest_header()
+    csrc = src_dir or CSRC
+    out = out_dir or OUT
+    lib = os.path.join(out, os.path.basename(LIB))
+    os.makedirs(out, exist_ok=True)
+    srcs = sorted(glob.glob(os.path.join(csrc, "*.cu")))
+    hdr_time = max(_newest_header(), max((os.path.getmtime(h) for h in
+                                          glob.glob(os.path.join(csrc, "*.cuh"))), default=0.0))
     flags = ARCH + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
                     "-Xptxas", "-v" if verbose else "-O3", "-I", os.path.join(ROOT, "include")]
+    flags += [f"-D{d}" for d in defines]
 
     def compile_one(src: str) -> str:
-        obj = os.path.join(OUT, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(out, os.path.basename(src)[:-3] + ".o")
         if (os.path.exists(obj) and os.path.getmtime(obj) >= os.path.getmtime(src)
                 and os.path.getmtime(obj) >= hdr_time):
             return obj
@@ -63,15 +72,15 @@ def build(verbose: bool = False, jobs: int | None = None) -> str:
 
     with ThreadPoolExecutor(max_workers=jobs or min(8, os.cpu_count() or 4)) as ex:
         objs = list(ex.map(compile_one, srcs))
-    if not os.path.exists(LIB) or any(os.path.getmtime(o) > os.path.getmtime(LIB) for o in objs):
-        tmp = LIB + f".tmp{os.getpid()}"
+    if not os.path.exists(lib) or any(os.path.getmtime(o) > os.path.getmtime(lib) for o in objs):
+        tmp = lib + f".tmp{os.getpid()}"
         cmd = [nvcc, *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *objs,
                "-Xlinker", "-rpath=" + _cuda_lib_dir(nvcc)]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

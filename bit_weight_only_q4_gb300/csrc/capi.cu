@@ -118,6 +118,13 @@ static q4_status run_stream(int kind, GemvParams p, int M, int N, int K, void *w
     unsigned char *wsb = static_cast<unsigned char *>(ws);
     p.N = N;
     p.K = K;
+#ifndef Q4_PREFER_BULK
+    if (rows_eligible(kind, K)) {
+        RowsPlan plan;
+        if ((s = rows_plan(dev, kind, M, N, K, plan)) == Q4_OK)
+            return rows_launch(plan, p, M, st, pdl);
+    }
+#endif
     if (bulk_ok && bulk_eligible(kind, K)) {
         BulkPlan plan;
         if ((s = bulk_plan(dev, kind, M, N, K, plan)) != Q4_OK)

@@ -176,7 +176,7 @@ __global__ void __launch_bounds__(GEMV_THREADS) q4_stream_kernel(GemvParams p)
     const int64_t u1 = unit_start(p, gw + 1);
     const int Kpad = p.S * Kind<WK>::KSTEP;
     uint16_t *xs = reinterpret_cast<uint16_t *>(smem);
-    float *cf = reinterpret_cast<float *>(smem + (size_t)MT * Kpad * 2);
+    float *cf = reinterpret_cast<float *>(smem + (size_t)MT * Kpad * 2);  // 16-byte aligned
 
     UnitRegs<RW> A, B;
     if (u0 < u1)
@@ -261,12 +261,12 @@ static const void *select_kernel(int kind, int mt, int rw)
 }
 
 static int kstep_of(int kind) { return kind == W_BF16 ? 256 : 1024; }
-static int cols_of(int kind) { return kind == W_BF16 ? 8 : 32; }
 
 static size_t smem_bytes(int kind, int mt, int S)
 {
     const size_t Kpad = (size_t)S * kstep_of(kind);
-    return (size_t)mt * Kpad * 2 + (size_t)mt * (Kpad / cols_of(kind)) * 4;
+    const size_t ch = kind == W_INT4 ? 4 : (kind == W_BF16 ? 0 : 1);
+    return (size_t)mt * Kpad * 2 + (size_t)mt * (Kpad / 32) * ch * 4;
 }
 
 q4_status gemv_plan(const DeviceInfo &dev, int kind, int M, int N, int K, GemvPlan &plan)

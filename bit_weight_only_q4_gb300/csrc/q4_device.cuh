@@ -112,6 +112,33 @@ __device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte_lo8)
     return r;
 }
 
+// The four bytes of w (eight E2M1 codes, low nibble = even column) -> four f16x2
+// pairs: h[b] = (E2M1(code 2b), E2M1(code 2b + 1)).  The byte operands come from a
+// vector unpack, which the converter reads in place (no shifts).
+__device__ __forceinline__ void e2m1x8_to_f16x2x4(uint32_t w, uint32_t (&h)[4])
+{
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+        "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+        : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+        : "r"(w));
+}
+
+// Two 4-bit codes at bit positions 0..3 and 16..19 (mask 0x000F000F) or 4..7 and
+// 20..23 (mask 0x00F000F0) of v become the f16 pair (1024 + c) or (1024 + 16 c):
+// OR the masked bits into the mantissa of 1024.0 (0x6400), whose last mantissa
+// bit weighs 1.  Exact for c in 0..15.
+template <uint32_t MASK>
+__device__ __forceinline__ uint32_t int4_pair_f16_biased(uint32_t v)
+{
+    uint32_t r;
+    asm("lop3.b32 %0, %1, %2, 0x64006400, 0xEA;" : "=r"(r) : "r"(v), "n"(MASK));
+    return r;  // (v & MASK) | 0x64006400
+}
+
 // Two float8_e4m3fn bytes (low 16 bits) -> f16x2 (exact: e4m3 fits in fp16).
 __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_bytes)
 {
@@ -170,23 +197,28 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar)
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
+// Suspend-time hint of one poll (ns): the waiting thread sleeps in hardware until
+// the phase completes or this much time has passed, instead of spinning and
+// taking issue slots from the warps that compute.
+constexpr uint32_t kMbarSuspendNs = 20000;
+
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
 {
     uint32_t ok;
     asm volatile("{\n\t.reg .pred p;\n\t"
-                 "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                 "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
                  "selp.u32 %0, 1, 0, p;\n\t}"
                  : "=r"(ok)
-                 : "r"(bar), "r"(parity)
+                 : "r"(bar), "r"(parity), "n"(kMbarSuspendNs)
                  : "memory");
     return ok != 0;
 }
 
 // Bounded wait for the phase of the given parity to complete.  Every wait in this
-// library ends: after kMbarSpinLimit polls (seconds; each poll may suspend the
-// thread for a while in hardware) the wait sets kErrBarrierTimeout in *err and returns
-// false so the kernel can finish instead of hanging.
-constexpr uint32_t kMbarSpinLimit = 1u << 24;
+// library ends: after kMbarSpinLimit polls (at most kMbarSpinLimit x 20 us, a few
+// seconds) the wait sets kErrBarrierTimeout in *err and returns false so the
+// kernel can finish instead of hanging.
+constexpr uint32_t kMbarSpinLimit = 1u << 18;
 constexpr unsigned kErrBarrierTimeout = 1u;
 
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned *err)

@@ -37,6 +37,7 @@ struct GemvParams {
     int64_t T;                // stages = row blocks * S
     int grid;                 // CTAs
     int nst;                  // shared-memory ring depth
+    int consumers;            // consumer warps per CTA
     unsigned *err;            // device error flags (bounded waits that timed out)
 };
 
@@ -74,7 +75,7 @@ q4_status gemv_launch(const GemvPlan &plan, GemvParams p, int M, cudaStream_t st
 
 // ---- bulk-copy (TMA engine) weight-streaming kernel (gemv_bulk.cu)
 struct BulkPlan {
-    int kind = 0, mt = 1, rw = 4, nst = 4;
+    int kind = 0, mt = 1, rpw = 1, nst = 4, consumers = 16;
     int64_t gran = 1;
     int grid = 0;
     size_t smem = 0;
@@ -86,6 +87,15 @@ struct BulkPlan {
 bool bulk_eligible(int kind, int K);
 q4_status bulk_plan(const DeviceInfo &dev, int kind, int M, int N, int K, BulkPlan &plan);
 q4_status bulk_launch(const BulkPlan &plan, GemvParams p, int M, cudaStream_t stream, bool pdl);
+// ---- register-prefetch weight-streaming kernel (gemv_rows.cu)
+struct RowsPlan {
+    int kind = 0, mt = 1, rb = 4, S = 1, grid = 0;
+    size_t smem = 0;
+};
+bool rows_eligible(int kind, int K);
+q4_status rows_plan(const DeviceInfo &dev, int kind, int M, int N, int K, RowsPlan &plan);
+q4_status rows_launch(const RowsPlan &plan, GemvParams p, int M, cudaStream_t stream, bool pdl);
+
 // Device address of the library's error-flag word on the current device.
 unsigned *device_error_flags();
 

@@ -1,6 +1,21 @@
 // Pieces shared by the two CUDA-core weight-streaming kernels (register path in
 // gemv.cu, bulk-copy path in gemv_bulk.cu): the unit geometry, the staging of x
 // in shared memory and the in-register decode + dot product of one unit.
+//
+// Arithmetic (both 4-bit layouts): x is staged as fp16 values x' = x * 2^p with
+// one power-of-two p per 32-column chunk, chosen so the chunk's largest |x'| lies
+// in [2^14, 2^15): every bf16 value converts without overflow, and exactly down
+// to 2^-22 of the chunk maximum.  Codes are decoded to exact fp16 operands and
+// every product is accumulated in fp32 by one mixed-precision FMA
+// (fma.rn.f32.f16); the chunk's partial sums are scaled back by 2^-p, the group
+// scale (and min) in fp32.
+//   NVFP4: E2M1 pairs -> f16x2 by cvt.rn.f16x2.e2m1x2 on bytes unpacked from the
+//     packed word (no shifts); per group of 16 columns: sum_k e2m1(c) x'.
+//   int4: nibble pairs -> f16x2 (1024 + c) or (1024 + 16 c) by one LOP3 each
+//     ("magic number" decode); per chunk the two partial sums
+//       A1 = sum_{even k} (1024 + c) x'   and   A2 = sum_{odd k} (1024 + 16 c) x'
+//     give  sum_k (c s + m) x' = s A1 + (s/16) A2 + (m - 1024 s) X1 + (m - 64 s) X2
+//     with X1, X2 the sums of x' over the chunk's even and odd columns.
 #pragma once
 
 #include "q4_device.cuh"
@@ -13,6 +28,9 @@ struct Kind {
     // columns held by one lane's 16 weight bytes
     static constexpr int COLS = (WK == W_BF16) ? 8 : 32;
     static constexpr int KSTEP = 32 * COLS;
+    // floats of per-chunk data in shared memory: int4 (2^-p, X1, X2, 0),
+    // NVFP4 (2^-p), bf16 none
+    static constexpr int CH = (WK == W_INT4) ? 4 : ((WK == W_BF16) ? 0 : 1);
 };
 
 template <int RW>
@@ -22,23 +40,29 @@ struct UnitRegs {
 };
 
 // Shared-memory image of x for one launch: MT rows of Kpad operand values
-// (bf16 bits for int4 and bf16 weights, f16 bits for NVFP4), then MT x Kpad/COLS
-// floats of per-chunk data (int4: chunk sum of x; NVFP4: 2^-p of the chunk's
-// power-of-two prescale).  For the 4-bit kinds every k-step of 1024 columns is
-// stored lane-interleaved: the i-th 16-byte vector of lane l (columns
-// 32 l + 8 i .. + 7) sits at vector index i * 32 + l, so the four vector loads a
-// lane issues per k-step are each conflict-free across the warp.
+// (f16 bits of x' for the 4-bit kinds, bf16 bits for bf16 weights), then
+// MT x (Kpad/32) x CH floats of per-chunk data.  For the 4-bit kinds every k-step
+// of 1024 columns is stored lane-interleaved: the i-th 16-byte vector of lane l
+// (columns 32 l + 8 i .. + 7) sits at vector index i * 32 + l, so the four
+// vector loads a lane issues per k-step are each conflict-free across the warp.
+// For int4 each vector holds the pairs (x'[8j+t], x'[8j+t+4]), t = 0..3 -- the
+// order the nibble decoder produces codes in.
 __device__ __forceinline__ int xs_vec_index(int k0)
 {
     const int ks = k0 >> 10, kk = k0 & 1023;
     return ks * 128 + ((kk & 31) >> 3) * 32 + (kk >> 5);
 }
 
+__device__ __forceinline__ float pow2f(int e)  // 2^e for -126 <= e <= 127
+{
+    return __uint_as_float((uint32_t)(e + 127) << 23);
+}
+
 template <int WK, int MT>
 __device__ void stage_x(const GemvParams &p, int Kpad, uint16_t *xs, float *cf, int tid,
                         int nthreads)
 {
-    constexpr int COLS = Kind<WK>::COLS;
+    constexpr int CH = Kind<WK>::CH;
     const int blocks_per_row = Kpad / 8;
     const int total = MT * blocks_per_row;
     // total is a multiple of 4 and every 4 consecutive blocks form one 32-column
@@ -51,27 +75,11 @@ __device__ void stage_x(const GemvParams &p, int Kpad, uint16_t *xs, float *cf, 
         uint4 v = make_uint4(0u, 0u, 0u, 0u);
         if (active && m < p.mcount && k0 < p.K)
             v = *reinterpret_cast<const uint4 *>(p.x + (int64_t)(p.m0 + m) * p.K + k0);
-        uint32_t e[4] = {v.x, v.y, v.z, v.w};
-        if constexpr (WK == W_INT4) {
-            // pair (x[8j+t], x[8j+t+4]) -- the order int4_pair_bf16_biased(w >> 4t)
-            // produces codes in
-            uint4 o;
-            o.x = __byte_perm(e[0], e[2], 0x5410);
-            o.y = __byte_perm(e[0], e[2], 0x7632);
-            o.z = __byte_perm(e[1], e[3], 0x5410);
-            o.w = __byte_perm(e[1], e[3], 0x7632);
-            float s = 0.f;
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-                s += bf16_bits_to_f32(e[i] & 0xffffu) + bf16_bits_to_f32(e[i] >> 16);
-            s += __shfl_xor_sync(0xffffffffu, s, 1);
-            s += __shfl_xor_sync(0xffffffffu, s, 2);
-            if (active) {
-                reinterpret_cast<uint4 *>(xs + (size_t)m * Kpad)[xs_vec_index(k0)] = o;
-                if ((k0 % 32) == 0)
-                    cf[(size_t)m * (Kpad / COLS) + k0 / 32] = s;
-            }
-        } else if constexpr (WK == W_NVFP4_A16 || WK == W_NVFP4_A8) {
+        if constexpr (WK == W_BF16) {
+            if (active)
+                *reinterpret_cast<uint4 *>(xs + (size_t)m * Kpad + k0) = v;
+        } else {
+            const uint32_t e[4] = {v.x, v.y, v.z, v.w};
             float f[8];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
@@ -84,29 +92,119 @@ __device__ void stage_x(const GemvParams &p, int Kpad, uint16_t *xs, float *cf, 
                 amax = fmaxf(amax, fabsf(f[i]));
             amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
             amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-            // power-of-two prescale putting the chunk's largest |x| in [2^14, 2^15)
-            // so every bf16 value of the chunk converts to fp16 without overflow
-            // and, down to 2^-16 of the maximum, without rounding
+            // exponent ex with amax = f * 2^ex, f in [0.5, 1)
             int ex = 0;
-            if (amax > 0.f && !isinf(amax))
-                frexpf(amax, &ex);
+            if (amax > 0.f && !isinf(amax)) {
+                const int be = (int)((__float_as_uint(amax) >> 23) & 0xff);
+                if (be > 0)
+                    ex = be - 126;
+                else
+                    frexpf(amax, &ex);
+            }
             int pw = 15 - ex;
             pw = pw > 100 ? 100 : (pw < -100 ? -100 : pw);
+            const float up = pow2f(pw);
+            float xq[8];
             uint32_t h[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                __half2 hh = __floats2half2_rn(ldexpf(f[2 * i], pw), ldexpf(f[2 * i + 1], pw));
+                __half2 hh;
+                if constexpr (WK == W_INT4)   // pairs (x'[t], x'[t+4])
+                    hh = __floats2half2_rn(f[i] * up, f[i + 4] * up);
+                else                          // natural order
+                    hh = __floats2half2_rn(f[2 * i] * up, f[2 * i + 1] * up);
                 h[i] = *reinterpret_cast<uint32_t *>(&hh);
+                xq[2 * i] = __low2float(hh);
+                xq[2 * i + 1] = __high2float(hh);
             }
-            if (active) {
+            if (active)
                 reinterpret_cast<uint4 *>(xs + (size_t)m * Kpad)[xs_vec_index(k0)] =
                     make_uint4(h[0], h[1], h[2], h[3]);
-                if ((k0 % 32) == 0)
-                    cf[(size_t)m * (Kpad / COLS) + k0 / 32] = ldexpf(1.f, -pw);
+            if constexpr (WK == W_INT4) {
+                // h[i] holds columns (i, i+4): even columns are i = 0, 2
+                float s_even = (xq[0] + xq[1]) + (xq[4] + xq[5]);
+                float s_odd = (xq[2] + xq[3]) + (xq[6] + xq[7]);
+                s_even += __shfl_xor_sync(0xffffffffu, s_even, 1);
+                s_even += __shfl_xor_sync(0xffffffffu, s_even, 2);
+                s_odd += __shfl_xor_sync(0xffffffffu, s_odd, 1);
+                s_odd += __shfl_xor_sync(0xffffffffu, s_odd, 2);
+                if (active && (k0 % 32) == 0)
+                    reinterpret_cast<float4 *>(cf)[(size_t)m * (Kpad / 32) + k0 / 32] =
+                        make_float4(pow2f(-pw), s_even, s_odd, 0.f);
+            } else {
+                if (active && (k0 % 32) == 0)
+                    cf[(size_t)m * (Kpad / 32) + k0 / 32] = pow2f(-pw);
             }
+            (void)CH;
+        }
+    }
+}
+
+// One lane's slice of x for the bulk kernel, loaded straight from global memory:
+// columns [col0, col0 + COLS) of every token, converted to the decoder's operand
+// format (the same values stage_x writes to shared memory), and its chunk data
+// (int4: 2^-p, X1, X2; NVFP4: 2^-p * g).  A 32-column chunk is exactly one lane's
+// slice, so the prescale needs no communication between lanes.
+template <int WK, int MT, int XV>
+__device__ __forceinline__ void load_x_slice(const GemvParams &p, int col0, float gsc,
+                                             uint32_t (&xr)[MT][XV], float4 (&cd)[MT])
+{
+#pragma unroll
+    for (int m = 0; m < MT; ++m) {
+        const bool ok = m < p.mcount && col0 < p.K;
+        const uint16_t *src = p.x + (int64_t)(p.m0 + m) * p.K + col0;
+        cd[m] = make_float4(1.f, 0.f, 0.f, 0.f);
+        if constexpr (WK == W_BF16) {
+            const uint4 v = ok ? *reinterpret_cast<const uint4 *>(src) : make_uint4(0u, 0u, 0u, 0u);
+            xr[m][0] = v.x; xr[m][1] = v.y; xr[m][2] = v.z; xr[m][3] = v.w;
         } else {
-            if (active)
-                *reinterpret_cast<uint4 *>(xs + (size_t)m * Kpad + k0) = v;
+            uint32_t e[16];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const uint4 v = ok ? reinterpret_cast<const uint4 *>(src)[i]
+                                   : make_uint4(0u, 0u, 0u, 0u);
+                e[4 * i] = v.x; e[4 * i + 1] = v.y; e[4 * i + 2] = v.z; e[4 * i + 3] = v.w;
+            }
+            float f[32];
+            float amax = 0.f;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                f[2 * i] = bf16_bits_to_f32(e[i] & 0xffffu);
+                f[2 * i + 1] = bf16_bits_to_f32(e[i] >> 16);
+                amax = fmaxf(amax, fmaxf(fabsf(f[2 * i]), fabsf(f[2 * i + 1])));
+            }
+            int ex = 0;
+            if (amax > 0.f && !isinf(amax)) {
+                const int be = (int)((__float_as_uint(amax) >> 23) & 0xff);
+                if (be > 0)
+                    ex = be - 126;
+                else
+                    frexpf(amax, &ex);
+            }
+            int pw = 15 - ex;
+            pw = pw > 100 ? 100 : (pw < -100 ? -100 : pw);
+            const float up = pow2f(pw);
+            float s_even = 0.f, s_odd = 0.f;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {        // 8-column block i
+#pragma unroll
+                for (int t = 0; t < 4; ++t) {
+                    __half2 hh;
+                    if constexpr (WK == W_INT4)  // pair (col t, col t + 4)
+                        hh = __floats2half2_rn(f[8 * i + t] * up, f[8 * i + t + 4] * up);
+                    else                         // pair (col 2t, col 2t + 1)
+                        hh = __floats2half2_rn(f[8 * i + 2 * t] * up, f[8 * i + 2 * t + 1] * up);
+                    xr[m][4 * i + t] = *reinterpret_cast<uint32_t *>(&hh);
+                    if constexpr (WK == W_INT4) {
+                        const float pr = __low2float(hh) + __high2float(hh);
+                        if (t % 2 == 0)
+                            s_even += pr;
+                        else
+                            s_odd += pr;
+                    }
+                }
+            }
+            cd[m] = make_float4(pow2f(-pw) * (WK == W_INT4 ? 1.f : gsc), s_even, s_odd, 0.f);
         }
     }
 }
@@ -138,7 +236,6 @@ __device__ __forceinline__ void compute_unit(const GemvParams &p, const UnitRegs
         }
     } else {
         uint32_t xr[MT][16];
-        float cc[MT];
 #pragma unroll
         for (int m = 0; m < MT; ++m) {
             const uint4 *src = reinterpret_cast<const uint4 *>(xs + (size_t)m * Kpad) + ks * 128;
@@ -148,35 +245,59 @@ __device__ __forceinline__ void compute_unit(const GemvParams &p, const UnitRegs
                 xr[m][4 * i + 0] = t.x; xr[m][4 * i + 1] = t.y;
                 xr[m][4 * i + 2] = t.z; xr[m][4 * i + 3] = t.w;
             }
-            cc[m] = cf[(size_t)m * (Kpad / COLS) + col0 / 32];
         }
+        const int chunk = col0 / 32;
+        if constexpr (WK == W_INT4) {
+            float4 cd[MT];
 #pragma unroll
-        for (int r = 0; r < RW; ++r) {
-            const uint32_t q[4] = {R.q[r].x, R.q[r].y, R.q[r].z, R.q[r].w};
-            if constexpr (WK == W_INT4) {
-                float T[MT];
+            for (int m = 0; m < MT; ++m)
+                cd[m] = reinterpret_cast<const float4 *>(cf)[(size_t)m * (Kpad / 32) + chunk];
 #pragma unroll
-                for (int m = 0; m < MT; ++m)
-                    T[m] = 0.f;
+            for (int r = 0; r < RW; ++r) {
+                const uint32_t q[4] = {R.q[r].x, R.q[r].y, R.q[r].z, R.q[r].w};
+                float A1[MT], A2[MT];
+#pragma unroll
+                for (int m = 0; m < MT; ++m) {
+                    A1[m] = 0.f;
+                    A2[m] = 0.f;
+                }
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
+                    const uint32_t w8 = q[j] >> 8;
+                    const uint32_t pa = int4_pair_f16_biased<0x000F000Fu>(q[j]);   // cols 0, 4
+                    const uint32_t pb = int4_pair_f16_biased<0x00F000F0u>(q[j]);   // cols 1, 5
+                    const uint32_t pc = int4_pair_f16_biased<0x000F000Fu>(w8);     // cols 2, 6
+                    const uint32_t pd = int4_pair_f16_biased<0x00F000F0u>(w8);     // cols 3, 7
 #pragma unroll
-                    for (int t = 0; t < 4; ++t) {
-                        const uint32_t pr = int4_pair_bf16_biased(q[j] >> (4 * t));
-#pragma unroll
-                        for (int m = 0; m < MT; ++m)
-                            T[m] = fma2_bf16(T[m], pr, xr[m][4 * j + t]);
+                    for (int m = 0; m < MT; ++m) {
+                        A1[m] = fma2_f16(A1[m], pa, xr[m][4 * j + 0]);
+                        A2[m] = fma2_f16(A2[m], pb, xr[m][4 * j + 1]);
+                        A1[m] = fma2_f16(A1[m], pc, xr[m][4 * j + 2]);
+                        A2[m] = fma2_f16(A2[m], pd, xr[m][4 * j + 3]);
                     }
                 }
-                // sum_k (128 + c) x = 128 X + sum_k c x, so
-                // s * sum c x + min * X = s * T + (min - 128 s) * X
                 const float s = f16lo_to_f32(R.s[r]);
                 const float mn = f16hi_to_f32(R.s[r]);
-                const float mb = fmaf(-128.f, s, mn);
+                const float c1 = fmaf(-1024.f, s, mn);
+                const float c2 = fmaf(-64.f, s, mn);
+                const float s16 = s * 0.0625f;
 #pragma unroll
-                for (int m = 0; m < MT; ++m)
-                    acc[r][m] = fmaf(mb, cc[m], fmaf(s, T[m], acc[r][m]));
-            } else {
+                for (int m = 0; m < MT; ++m) {
+                    float t = s * A1[m];
+                    t = fmaf(s16, A2[m], t);
+                    t = fmaf(c1, cd[m].y, t);
+                    t = fmaf(c2, cd[m].z, t);
+                    acc[r][m] = fmaf(t, cd[m].x, acc[r][m]);
+                }
+            }
+        } else {
+            float cc[MT];
+#pragma unroll
+            for (int m = 0; m < MT; ++m)
+                cc[m] = cf[(size_t)m * (Kpad / 32) + chunk] * gsc;
+#pragma unroll
+            for (int r = 0; r < RW; ++r) {
+                const uint32_t q[4] = {R.q[r].x, R.q[r].y, R.q[r].z, R.q[r].w};
                 float Ta[MT], Tb[MT];
 #pragma unroll
                 for (int m = 0; m < MT; ++m) {
@@ -185,21 +306,22 @@ __device__ __forceinline__ void compute_unit(const GemvParams &p, const UnitRegs
                 }
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
+                    uint32_t h[4];
+                    e2m1x8_to_f16x2x4(q[j], h);
 #pragma unroll
                     for (int b = 0; b < 4; ++b) {
-                        const uint32_t h = e2m1x2_to_f16x2(q[j] >> (8 * b));
 #pragma unroll
                         for (int m = 0; m < MT; ++m) {
                             if (j < 2)
-                                Ta[m] = fma2_f16(Ta[m], h, xr[m][4 * j + b]);
+                                Ta[m] = fma2_f16(Ta[m], h[b], xr[m][4 * j + b]);
                             else
-                                Tb[m] = fma2_f16(Tb[m], h, xr[m][4 * j + b]);
+                                Tb[m] = fma2_f16(Tb[m], h[b], xr[m][4 * j + b]);
                         }
                     }
                 }
                 const uint32_t sc = e4m3x2_to_f16x2(R.s[r]);
-                const float sa = f16lo_to_f32(sc) * gsc;
-                const float sb = f16hi_to_f32(sc) * gsc;
+                const float sa = f16lo_to_f32(sc);
+                const float sb = f16hi_to_f32(sc);
 #pragma unroll
                 for (int m = 0; m < MT; ++m)
                     acc[r][m] = fmaf(fmaf(Ta[m], sa, Tb[m] * sb), cc[m], acc[r][m]);
