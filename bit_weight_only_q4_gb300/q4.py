@@ -64,6 +64,7 @@ def load() -> ctypes.CDLL:
             "q4_workspace_bytes": ([i, i, i, i], sz),
             "q4_linear_int4g128": ([p, p, p, p, p, i, i, i, p, sz, p], st),
             "q4_linear_nvfp4": ([p, p, p, p, p, i, i, i, p, sz, p], st),
+            "q4_linear_int4g128_noalloc": ([p, p, p, p, p, i, i, i, p], st),
             "audio_head_logits_restricted": ([p, p, i, i, i, i, p, i, i, p], st),
             "q4_device_error_flags": ([ctypes.POINTER(ctypes.c_uint), i], st),
             "q4_dequant_int4g128_f32": ([p, p, p, p, i, i, p], st),
@@ -82,7 +83,7 @@ def symbols() -> list[str]:
     return ["q4_abi_version", "q4_status_string", "q4_last_error_string",
             "q4_set_launch_flags", "q4_get_launch_flags", "q4_workspace_bytes",
             "q4_linear_int4g128", "q4_linear_nvfp4", "audio_head_logits_restricted",
-            "q4_device_error_flags", "q4_dequant_int4g128_f32", "q4_dequant_nvfp4_f32"]
+            "q4_linear_int4g128_noalloc", "q4_device_error_flags", "q4_dequant_int4g128_f32", "q4_dequant_nvfp4_f32"]
 
 
 def _check(status: int) -> None:
@@ -163,6 +164,21 @@ def q4_linear_int4g128(x, qweight, scale, minv, y=None, workspace=None, stream=N
     wp, wn = _ws_args(workspace)
     _check(load().q4_linear_int4g128(_ptr(x), _ptr(qweight), _ptr(scale), _ptr(minv), _ptr(y),
                                      M, N, K, wp, wn, _stream(stream)))
+    return y
+
+
+def q4_linear_int4g128_noalloc(x, qweight, scale, minv, y, stream=None):
+    """As q4_linear_int4g128, for callers that cannot allocate device memory: the
+    library's own static scratch replaces the workspace and ``y`` must be given."""
+    _cuda(x, "x", torch.bfloat16)
+    _cuda(qweight, "qweight", torch.uint8)
+    _cuda(scale, "scale")
+    _cuda(minv, "min")
+    _cuda(y, "y", torch.bfloat16)
+    M, K = x.shape
+    N = qweight.shape[0]
+    _check(load().q4_linear_int4g128_noalloc(_ptr(x), _ptr(qweight), _ptr(scale), _ptr(minv),
+                                             _ptr(y), M, N, K, _stream(stream)))
     return y
 
 

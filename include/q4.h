@@ -115,6 +115,32 @@ q4_status q4_linear_nvfp4(const void *x, const uint8_t *codes, const uint8_t *sc
                           void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * q4_linear_int4g128 for callers that cannot allocate device memory: code that
+ * runs where the CUDA allocator must not be called (inside an audio or other
+ * real-time callback that may not block, in a plugin whose host application owns
+ * every device buffer, after a memory pool has been frozen) and so cannot hand
+ * this library a workspace.  The source pages have no counterpart to this entry
+ * point; it exists for such deployments.
+ *
+ * Same arguments, layout and result as q4_linear_int4g128 minus the workspace.
+ * It runs the split-K CUDA-core kernel with its scratch (arrival counters and
+ * partial sums) in a static device array of 4 MiB that is part of the library:
+ * every GPU that loads the library keeps those 4 MiB until the process exits.
+ * Shapes whose scratch would exceed 4 MiB are rejected with Q4_ERR_SHAPE (for
+ * M <= 4 this covers N * ceil(K / 1024) up to about 250,000 per token block).
+ * The call allocates and frees nothing.  The first call on a device looks up the
+ * array's device address (with that device current); make that first call
+ * before starting any stream capture.  Every call clears the counters it needs
+ * with an asynchronous memset on `stream`, then launches the kernel.  All calls
+ * share the one array, which keeps the last call's contents: calls whose work
+ * overlaps on the GPU (other streams or host threads) race on it and must be
+ * serialised by the caller.
+ */
+q4_status q4_linear_int4g128_noalloc(const void *x, const uint8_t *qweight, const void *scale,
+                                     const void *minv, void *y, int M, int N, int K,
+                                     void *stream);
+
+/*
  * Restricted output head -- "Rumik TTS Fast Inference", section "What Made It
  * Faster" and Figure 3: project the hidden state only onto the rows of the
  * current codebook (2,048 codes) plus the end token, 2,049 rows instead of the
