@@ -12,6 +12,9 @@
 namespace q4 {
 
 static thread_local char g_last_error[512] = "";
+// Smallest M served by the tcgen05 kernel (below it the CUDA-core streaming
+// kernels run, one launch per block of up to four tokens).
+static constexpr int kTensorCoreMinM = 5;
 static std::atomic<unsigned> g_flags{0u};
 
 q4_status fail(q4_status s, const char *fmt, ...)
@@ -191,17 +194,26 @@ size_t q4_workspace_bytes(int layout, int M, int N, int K)
 {
     if (M < 1 || N < 1 || K < 1)
         return 0;
+    int sms = 0, dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+        (void)cudaGetLastError();
+        sms = 160;   // no device: size for a GB300-class part
+    }
+    size_t a = 0;
     if (layout == Q4_LAYOUT_INT4G128) {
         if (K % 128)
             return 0;
-        return stream_ws_layout(W_INT4, M, N, K).total;
-    }
-    if (layout == Q4_LAYOUT_NVFP4) {
+        a = stream_ws_layout(W_INT4, M, N, K).total;
+    } else if (layout == Q4_LAYOUT_NVFP4) {
         if (K % 16)
             return 0;
-        return stream_ws_layout(W_NVFP4_A16, M, N, K).total;
+        a = stream_ws_layout(W_NVFP4_A16, M, N, K).total;
+    } else {
+        return 0;
     }
-    return 0;
+    const size_t b = tc_workspace_bytes(M, N, K, sms);
+    return a > b ? a : b;
 }
 
 q4_status q4_linear_int4g128(const void *x, const uint8_t *qweight, const void *scale,
@@ -218,8 +230,15 @@ q4_status q4_linear_int4g128(const void *x, const uint8_t *qweight, const void *
         return s;
     if (!aligned(scale, 2) || !aligned(minv, 2))
         return fail(Q4_ERR_ALIGN, "scale and min must be 2-byte aligned");
-    if (g_flags.load() & Q4_FLAG_FORCE_TENSOR_CORE)
-        return fail(Q4_ERR_ARG, "tensor-core path not available for this build");
+    const unsigned flags = g_flags.load();
+    const bool tc_ok = tc_eligible(W_INT4, M, N, K);
+    if ((flags & Q4_FLAG_FORCE_TENSOR_CORE) && !tc_ok)
+        return fail(Q4_ERR_ARG, "the tensor-core path needs K %% 64 == 0");
+    if (tc_ok && !(flags & Q4_FLAG_FORCE_CUDA_CORE) &&
+        ((flags & Q4_FLAG_FORCE_TENSOR_CORE) || M >= kTensorCoreMinM))
+        return tc_launch(W_INT4, x, qweight, scale, minv, nullptr, y, M, N, K, workspace,
+                         workspace_bytes, static_cast<cudaStream_t>(stream),
+                         (flags & Q4_FLAG_PDL) != 0);
     GemvParams p = {};
     p.x = static_cast<const uint16_t *>(x);
     p.w = qweight;
@@ -251,8 +270,15 @@ q4_status q4_linear_nvfp4(const void *x, const uint8_t *codes, const uint8_t *sc
         return fail(Q4_ERR_ALIGN, "global_scale must be 4-byte aligned");
     if (K % 32 == 0 && !aligned(scale_e4m3, 2))
         return fail(Q4_ERR_ALIGN, "scale_e4m3 must be 2-byte aligned");
-    if (g_flags.load() & Q4_FLAG_FORCE_TENSOR_CORE)
-        return fail(Q4_ERR_ARG, "tensor-core path not available for this build");
+    const unsigned flags = g_flags.load();
+    const bool tc_ok = tc_eligible(W_NVFP4_A16, M, N, K) && aligned(scale_e4m3, 2);
+    if ((flags & Q4_FLAG_FORCE_TENSOR_CORE) && !tc_ok)
+        return fail(Q4_ERR_ARG, "the tensor-core path needs K %% 64 == 0");
+    if (tc_ok && !(flags & Q4_FLAG_FORCE_CUDA_CORE) &&
+        ((flags & Q4_FLAG_FORCE_TENSOR_CORE) || M >= kTensorCoreMinM))
+        return tc_launch(W_NVFP4_A16, x, codes, scale_e4m3, nullptr, global_scale, y, M, N, K,
+                         workspace, workspace_bytes, static_cast<cudaStream_t>(stream),
+                         (flags & Q4_FLAG_PDL) != 0);
     GemvParams p = {};
     p.x = static_cast<const uint16_t *>(x);
     p.w = codes;

@@ -96,6 +96,13 @@ bool rows_eligible(int kind, int K);
 q4_status rows_plan(const DeviceInfo &dev, int kind, int M, int N, int K, RowsPlan &plan);
 q4_status rows_launch(const RowsPlan &plan, GemvParams p, int M, cudaStream_t stream, bool pdl);
 
+// ---- tcgen05 tensor-core GEMM (tc_gemm.cu)
+bool tc_eligible(int kind, int M, int N, int K);
+size_t tc_workspace_bytes(int M, int N, int K, int sms);
+q4_status tc_launch(int kind, const void *x, const uint8_t *codes, const void *scale,
+                    const void *minv, const float *gscale, void *y, int M, int N, int K,
+                    void *ws, size_t ws_bytes, cudaStream_t stream, bool pdl);
+
 // Device address of the library's error-flag word on the current device.
 unsigned *device_error_flags();
 

@@ -75,8 +75,9 @@ unsigned q4_get_launch_flags(void);
 
 /*
  * Bytes of device workspace that q4_linear_int4g128 (layout 0) or
- * q4_linear_nvfp4 (layout 1) needs for an [M,N,K] call on the current device
- * (split-K partial sums, arrival counters, dequantised tiles for large M).
+ * q4_linear_nvfp4 (layout 1) needs for an [M,N,K] call on the current device:
+ * split-K partial sums and arrival counters of whichever kernel the call may use
+ * (also when a Q4_FLAG_FORCE_* flag selects it).
  * The workspace must be zero-filled once after allocation; every call leaves
  * its counters at zero again.  Calls that run concurrently must not share a
  * workspace.  Returns 0 for invalid sizes.
@@ -93,8 +94,8 @@ size_t q4_workspace_bytes(int layout, int M, int N, int K);
  * Requirements: M >= 1, N >= 1, K >= 128, K % 128 == 0; x, qweight, y and the
  * workspace 16-byte aligned, scale/minv 2-byte aligned; workspace of at least
  * q4_workspace_bytes(0, M, N, K) bytes (may be NULL when that is 0).
- * M selects the kernel: a CUDA-core GEMV for small M, the tcgen05 tensor-core
- * GEMM for larger M.
+ * M selects the kernel: a CUDA-core GEMV for M <= 4 (one launch per block of up
+ * to four tokens), the tcgen05 tensor-core GEMM for M >= 5 when K % 64 == 0.
  */
 q4_status q4_linear_int4g128(const void *x, const uint8_t *qweight, const void *scale,
                              const void *minv, void *y, int M, int N, int K,
@@ -166,6 +167,11 @@ q4_status audio_head_logits_restricted(const void *h, const void *head, int R_to
  * with clear != 0 the word is reset to zero afterwards.
  */
 #define Q4_DEVERR_TIMEOUT 0x1u
+/* Bit 1: the tensor-core path (M >= 5, K % 64 == 0) met an activation whose
+ * magnitude exceeds the fp16 range (65504); it converts x to fp16 internally, so
+ * that output is not valid.  Activations inside the range are converted exactly
+ * (down to 2^-17; smaller values are rounded to fp16 subnormals). */
+#define Q4_DEVERR_FP16_RANGE 0x2u
 q4_status q4_device_error_flags(unsigned *flags, int clear);
 
 /*

@@ -58,8 +58,8 @@ def test_launch_flags_roundtrip(lib):
 
 
 def test_workspace_bytes(lib):
-    # single k-step: no split-K, no workspace
-    assert q4.workspace_bytes(0, 1, 2048, 1024) == 0
+    # one 128-column k-range: no kernel splits K, no workspace
+    assert q4.workspace_bytes(0, 1, 2048, 128) == 0
     # split-K needs counters and partial slots, growing with N and K
     a = q4.workspace_bytes(0, 1, 2048, 2048)
     b = q4.workspace_bytes(0, 1, 2048, 8192)
@@ -75,11 +75,11 @@ def test_workspace_bytes(lib):
 FAKE = 1 << 20          # a 16-byte aligned address that is never dereferenced
 
 
-def _int4(lib, x=FAKE, w=FAKE, s=FAKE, m=FAKE, y=FAKE, M=1, N=64, K=1024, ws=None, wsb=0):
+def _int4(lib, x=FAKE, w=FAKE, s=FAKE, m=FAKE, y=FAKE, M=1, N=64, K=128, ws=None, wsb=0):
     return lib.q4_linear_int4g128(x, w, s, m, y, M, N, K, ws, wsb, None)
 
 
-def _nv(lib, x=FAKE, w=FAKE, s=FAKE, g=FAKE, y=FAKE, M=1, N=64, K=1024, ws=None, wsb=0):
+def _nv(lib, x=FAKE, w=FAKE, s=FAKE, g=FAKE, y=FAKE, M=1, N=64, K=128, ws=None, wsb=0):
     return lib.q4_linear_nvfp4(x, w, s, g, y, M, N, K, ws, wsb, None)
 
 

@@ -1,0 +1,125 @@
+"""GPU parity of the tcgen05 tensor-core path (batched decode and prefill) against
+the CPU oracle: forced tensor-core launches over ragged shapes, the batched-decode
+M sweep, and the prefill GEMM at full size on sampled output rows."""
+import numpy as np
+import pytest
+import torch
+
+from bit_weight_only_q4_gb300 import synth
+from tests import parity as P
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def q4():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from bit_weight_only_q4_gb300 import build, q4 as lib
+    build.build()
+    lib.load()
+    lib.set_launch_flags(0)
+    return lib
+
+
+def _run(q4, layout, x, w, flags):
+    q4.set_launch_flags(flags)
+    try:
+        if layout == "int4":
+            y = q4.q4_linear_int4g128(P.bf16_dev(x), *P.int4_dev(w))
+        else:
+            y = q4.q4_linear_nvfp4(P.bf16_dev(x), *P.nvfp4_dev(w))
+    finally:
+        q4.set_launch_flags(0)
+    torch.cuda.synchronize()
+    assert q4.device_error_flags() == 0
+    return y
+
+
+def _oracle(oracle_mod, layout, x, w, rows=None):
+    if layout == "int4":
+        q, s, m = (w.qweight, w.scale, w.minv) if rows is None else \
+            (w.qweight[rows], w.scale[rows], w.minv[rows])
+        return oracle_mod.linear_int4g128(x, q, s, m, with_abs=True)
+    c, s = (w.codes, w.scale) if rows is None else (w.codes[rows], w.scale[rows])
+    return oracle_mod.linear_nvfp4(x, c, s, w.global_scale, with_abs=True)
+
+
+def _mat(layout, rng, N, K):
+    return synth.int4_matrix(rng, N, K) if layout == "int4" else synth.nvfp4_matrix(rng, N, K)
+
+
+@pytest.mark.parametrize("layout", ["int4", "nvfp4"])
+@pytest.mark.parametrize("M,N,K", [(16, 128, 128), (1, 128, 128), (5, 200, 256), (48, 1000, 640),
+                                   (64, 384, 1024), (200, 130, 2048), (300, 256, 384),
+                                   (17, 8192, 128), (48, 96, 8192)])
+def test_forced_tensor_core_shapes(q4, oracle_mod, layout, M, N, K):
+    if layout == "int4" and K % 128:
+        pytest.skip("int4 needs K % 128")
+    rng = synth.rng_for(300, M, N, K)
+    w = _mat(layout, rng, N, K)
+    x = synth.activations(rng, M, K)
+    y = _run(q4, layout, x, w, q4.FLAG_FORCE_TENSOR_CORE)
+    yo, ao = _oracle(oracle_mod, layout, x, w)
+    P.check(y, yo, ao, f"tc {layout} M={M} N={N} K={K}")
+
+
+@pytest.mark.parametrize("layout", ["int4", "nvfp4"])
+def test_tensor_core_matches_cuda_core(q4, layout):
+    """The two kernel families agree with each other as well as with the oracle."""
+    rng = synth.rng_for(301)
+    w = _mat(layout, rng, 512, 2048)
+    x = synth.activations(rng, 8, 2048)
+    a = _run(q4, layout, x, w, q4.FLAG_FORCE_TENSOR_CORE).float()
+    b = _run(q4, layout, x, w, q4.FLAG_FORCE_CUDA_CORE).float()
+    rel = float((a - b).norm() / b.norm())
+    assert rel < 3e-3
+
+
+@pytest.mark.parametrize("layout", ["int4", "nvfp4"])
+@pytest.mark.parametrize("shape_index", [0, 1])
+def test_prefill_2048_tokens_sampled_rows(q4, oracle_mod, layout, shape_index):
+    x, w = synth.prefill(layout, shape_index)
+    y = _run(q4, layout, x, w, 0)
+    N = w.N
+    rows = np.unique(np.concatenate([np.arange(0, 5), np.arange(N - 5, N),
+                                     synth.rng_for(302, shape_index).integers(0, N, 22)]))
+    yo, ao = _oracle(oracle_mod, layout, x, w, rows)
+    P.check(y[:, torch.as_tensor(rows, device=y.device)], yo, ao,
+            f"prefill {layout} shape {shape_index}")
+
+
+def test_tensor_core_is_deterministic(q4):
+    rng = synth.rng_for(303)
+    w = synth.nvfp4_matrix(rng, 2048, 8192)
+    x = synth.activations(rng, 48, 8192)
+    y1 = _run(q4, "nvfp4", x, w, 0)
+    y2 = _run(q4, "nvfp4", x, w, 0)
+    assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))
+
+
+def test_fp16_range_flag(q4):
+    """An activation beyond the fp16 range on the tensor-core path is reported in
+    the device error word (the CUDA-core path has no such limit)."""
+    rng = synth.rng_for(304)
+    w = synth.int4_matrix(rng, 128, 128)
+    xf = np.zeros((16, 128), np.float32)
+    xf[3, 7] = 1.0e6
+    x = torch.from_numpy(xf).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    q4.device_error_flags()            # clear
+    q4.set_launch_flags(q4.FLAG_FORCE_TENSOR_CORE)
+    try:
+        q4.q4_linear_int4g128(P.bf16_dev(x), *P.int4_dev(w))
+    finally:
+        q4.set_launch_flags(0)
+    torch.cuda.synchronize()
+    assert q4.device_error_flags() & 0x2
+    y = q4.q4_linear_int4g128(P.bf16_dev(x), *P.int4_dev(w), ) if False else None
+    q4.set_launch_flags(q4.FLAG_FORCE_CUDA_CORE)
+    try:
+        y = q4.q4_linear_int4g128(P.bf16_dev(x), *P.int4_dev(w))
+    finally:
+        q4.set_launch_flags(0)
+    torch.cuda.synchronize()
+    assert torch.isfinite(y.float()).all()
+    assert q4.device_error_flags() == 0
