@@ -40,7 +40,6 @@ TRAFFIC = {
     # workload key: (bytes per launch, sha256 of csrc/gemv.cu when captured)
 }
 
-WORKLOADS = ("nvfp4_gemv", "int4_gemv", "decode_step", "batched", "prefill")
 
 
 # ---------------------------------------------------------------- helpers
@@ -219,6 +218,152 @@ def _time_graphs(torch, stream, graphs, world):
     torch.cuda.synchronize()
     barrier(world)
     return start.elapsed_time(end)
+
+
+# ------------------------------------------------------- further workloads
+def _graph_time(torch, stream, fn, n_calls, reps, warm=3):
+    """Capture fn(0..n_calls-1) once; return ms per replay over `reps` replays."""
+    with torch.cuda.stream(stream):
+        for i in range(n_calls):
+            fn(i)
+    torch.cuda.synchronize()
+    g = _capture(torch, fn, n_calls, stream)
+    _time_graphs(torch, stream, [(g, warm)], 1)
+    return _time_graphs(torch, stream, [(g, reps)], 1) / reps
+
+
+def run_decode_step(args, device):
+    """One decode step of the synthetic 28-layer int4 stack (hidden 2048, FFN
+    8192): per layer q, k, v, gate, up read x; o reads v; down reads up; the
+    next layer's x is down's output; then the restricted head (2049 rows).
+    196 + 1 calls per step, replayed from one CUDA graph; 1.007 GB of weights."""
+    import torch
+    from bit_weight_only_q4_gb300 import layout, q4, synth
+    from tests import parity as P
+    c = synth.DECODE_STACK_28
+    mats = []
+    for layer in range(c["layers"]):
+        mats.append({k: P.int4_dev(v) for k, v in synth.decode_stack_layer(layer).items()})
+    head = P.bf16_dev(synth.decode_stack_head())
+    x0 = P.bf16_dev(synth.decode_stack_input())
+    H, F = c["hidden"], c["ffn"]
+    buf = {n: torch.empty((1, F if n in ("gate", "up") else H), dtype=torch.bfloat16,
+                          device=device) for n in ("q", "k", "v", "o", "gate", "up", "down")}
+    logits = torch.empty((1, c["head_rows"]), dtype=torch.bfloat16, device=device)
+    ws = q4.alloc_workspace(q4.LAYOUT_INT4G128, 1, F, F, device)
+    src = {"q": "x", "k": "x", "v": "x", "o": "v", "gate": "x", "up": "x", "down": "up"}
+    wbytes = sum(layout.weight_bytes("int4", N, K) for _, N, K in synth.DECODE_LAYER_PROJS) \
+        * c["layers"] + 2 * c["head_rows"] * H
+
+    def step(_):
+        x = x0
+        for layer in range(c["layers"]):
+            for name, N, K in synth.DECODE_LAYER_PROJS:
+                inp = x if src[name] == "x" else buf[src[name]]
+                q4.q4_linear_int4g128(inp, *mats[layer][name], y=buf[name], workspace=ws)
+            x = buf["down"]
+        q4.audio_head_logits_restricted(x, head, 0, c["head_rows"], -1, logits=logits)
+
+    stream = torch.cuda.Stream(device)
+    ms = _graph_time(torch, stream, step, 1, args.steps)
+    peak, _ = _peaks()
+    gbs = wbytes / (ms * 1e-3) / 1e9
+    return {"workload": c["name"], "ms_per_step": round(ms, 4), "weight_bytes": wbytes,
+            "value": round(gbs, 1), "unit": "GB/s", "hbm_frac": round(gbs / peak, 4),
+            "steps_per_s": round(1e3 / ms, 1), "launches_per_step": 197,
+            "pdl": not args.no_pdl}
+
+
+def run_batched(args, device):
+    """NVFP4 batched decode at M tokens: K=2048 -> N=8192 then K=8192 -> N=2048
+    per step, weights rotating over >= 4x L2; swept over M."""
+    import torch
+    from bit_weight_only_q4_gb300 import layout, q4, synth
+    from tests import parity as P
+    c = synth.NVFP4_BATCHED_48
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    out = {"workload": c["name"], "sweep": []}
+    peak, _ = _peaks()
+    for M in c["m_sweep"]:
+        calls = []
+        for si, (N, K) in enumerate(c["shapes"]):
+            x, w = synth.nvfp4_batched(si, M)
+            base = P.nvfp4_dev(w)
+            copies = max(2, math.ceil(2 * l2 / layout.weight_bytes("nvfp4", N, K)))
+            ring = [tuple(t.clone() for t in base) for _ in range(copies)]
+            xd = P.bf16_dev(x)
+            y = torch.empty((M, N), dtype=torch.bfloat16, device=device)
+            wsb = q4.alloc_workspace(q4.LAYOUT_NVFP4, M, N, K, device)
+            calls.append((ring, xd, y, wsb))
+        R = len(calls[0][0])
+
+        def fn(i):
+            for ring, xd, y, wsb in calls:
+                q4.q4_linear_nvfp4(xd, *ring[i % len(ring)], y=y, workspace=wsb)
+
+        stream = torch.cuda.Stream(device)
+        ms = _graph_time(torch, stream, fn, R, max(3, args.steps // R)) / R
+        wb = sum(layout.weight_bytes("nvfp4", N, K) for N, K in c["shapes"])
+        flops = sum(2 * M * N * K for N, K in c["shapes"])
+        gbs = wb / (ms * 1e-3) / 1e9
+        out["sweep"].append({"M": M, "us_per_step": round(ms * 1e3, 3), "weight_GBps": round(gbs, 1),
+                             "hbm_frac": round(gbs / peak, 4),
+                             "tflops": round(flops / (ms * 1e-3) / 1e12, 2)})
+    return out
+
+
+def run_prefill(args, device):
+    """Prefill GEMM, M=2048 tokens: int4-g128 and NVFP4, K=2048 -> N=8192 and
+    K=8192 -> N=2048 (68.7 GFLOP each), tcgen05 path."""
+    import torch
+    from bit_weight_only_q4_gb300 import q4, synth
+    from tests import parity as P
+    c = synth.PREFILL_2048
+    res = {"workload": c["name"], "gemms": []}
+    bf16_peak = _bf16_peak()
+    for lay in ("int4", "nvfp4"):
+        for si, (N, K) in enumerate(c["shapes"]):
+            x, w = synth.prefill(lay, si)
+            xd = P.bf16_dev(x)
+            y = torch.empty((c["M"], N), dtype=torch.bfloat16, device=device)
+            if lay == "int4":
+                wd = P.int4_dev(w)
+                wsb = q4.alloc_workspace(q4.LAYOUT_INT4G128, c["M"], N, K, device)
+                fn = lambda i, xd=xd, wd=wd, y=y, wsb=wsb: q4.q4_linear_int4g128(xd, *wd, y=y, workspace=wsb)
+            else:
+                wd = P.nvfp4_dev(w)
+                wsb = q4.alloc_workspace(q4.LAYOUT_NVFP4, c["M"], N, K, device)
+                fn = lambda i, xd=xd, wd=wd, y=y, wsb=wsb: q4.q4_linear_nvfp4(xd, *wd, y=y, workspace=wsb)
+            stream = torch.cuda.Stream(device)
+            ms = _graph_time(torch, stream, fn, 10, max(3, args.steps // 10)) / 10
+            tf = 2 * c["M"] * N * K / (ms * 1e-3) / 1e12
+            res["gemms"].append({"layout": lay, "N": N, "K": K, "us": round(ms * 1e3, 2),
+                                 "tflops": round(tf, 1), "tensor_frac": round(tf / bf16_peak, 4)})
+    return res
+
+
+def _bf16_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            return float(json.load(f)["bf16_tflops"])
+    return 1900.0
+
+
+def run_extra(args, local):
+    import torch
+    from bit_weight_only_q4_gb300 import build as libbuild
+    from bit_weight_only_q4_gb300 import q4
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    libbuild.build()
+    q4.load()
+    q4.set_launch_flags(q4.FLAG_PDL if not args.no_pdl else 0)
+    fn = {"decode_step": run_decode_step, "batched": run_batched, "prefill": run_prefill}
+    r = fn[args.workload](args, device)
+    r["metric"] = METRIC
+    r["data"] = "synthetic (seeded PCG64)"
+    print(json.dumps(r), flush=True)
 
 
 def run_profile(args, local):
@@ -434,7 +579,10 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=200000)
     ap.add_argument("--warmup", type=int, default=2000)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--workload", choices=("nvfp4_gemv", "int4_gemv"), default="nvfp4_gemv")
+    ap.add_argument("--workload", choices=("nvfp4_gemv", "int4_gemv", "decode_step", "batched",
+                                           "prefill"), default="nvfp4_gemv",
+                    help="nvfp4_gemv is the bench line; the others print their own "
+                         "measurement lines")
     ap.add_argument("--no-pdl", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
@@ -456,6 +604,8 @@ def main(argv=None):
             run_reference(args, world, rank)
         elif args.profile:
             run_profile(args, local)
+        elif args.workload in ("decode_step", "batched", "prefill"):
+            run_extra(args, local)
         else:
             run_gpu(args, world, rank, local)
     finally:

@@ -271,7 +271,7 @@ q4_status q4_linear_nvfp4(const void *x, const uint8_t *codes, const uint8_t *sc
     if (K % 32 == 0 && !aligned(scale_e4m3, 2))
         return fail(Q4_ERR_ALIGN, "scale_e4m3 must be 2-byte aligned");
     const unsigned flags = g_flags.load();
-    const bool tc_ok = tc_eligible(W_NVFP4_A16, M, N, K) && aligned(scale_e4m3, 2);
+    const bool tc_ok = tc_eligible(W_NVFP4_A16, M, N, K) && aligned(scale_e4m3, 4);
     if ((flags & Q4_FLAG_FORCE_TENSOR_CORE) && !tc_ok)
         return fail(Q4_ERR_ARG, "the tensor-core path needs K %% 64 == 0");
     if (tc_ok && !(flags & Q4_FLAG_FORCE_CUDA_CORE) &&

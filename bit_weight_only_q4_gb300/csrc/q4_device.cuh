@@ -197,28 +197,26 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar)
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
-// Suspend-time hint of one poll (ns): the waiting thread sleeps in hardware until
-// the phase completes or this much time has passed, instead of spinning and
-// taking issue slots from the warps that compute.
-constexpr uint32_t kMbarSuspendNs = 20000;
-
+// One poll: returns once the phase of the given parity has completed or a short,
+// system-dependent time limit has passed.  (A long suspend-time hint made every
+// hand-off in the tensor-core pipeline wait far past the phase completion.)
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
 {
     uint32_t ok;
     asm volatile("{\n\t.reg .pred p;\n\t"
-                 "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+                 "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
                  "selp.u32 %0, 1, 0, p;\n\t}"
                  : "=r"(ok)
-                 : "r"(bar), "r"(parity), "n"(kMbarSuspendNs)
+                 : "r"(bar), "r"(parity)
                  : "memory");
     return ok != 0;
 }
 
 // Bounded wait for the phase of the given parity to complete.  Every wait in this
-// library ends: after kMbarSpinLimit polls (at most kMbarSpinLimit x 20 us, a few
-// seconds) the wait sets kErrBarrierTimeout in *err and returns false so the
-// kernel can finish instead of hanging.
-constexpr uint32_t kMbarSpinLimit = 1u << 18;
+// library ends: after kMbarSpinLimit polls (seconds) the wait sets
+// kErrBarrierTimeout in *err and returns false so the kernel can finish instead
+// of hanging.
+constexpr uint32_t kMbarSpinLimit = 1u << 26;
 constexpr unsigned kErrBarrierTimeout = 1u;
 
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned *err)

@@ -12,9 +12,12 @@
 //   * Warp 0 (one thread) streams, per chunk, the token tile of x (bf16, TMA
 //     tensor load with 128-byte swizzle) and the 128 rows x 32 bytes of packed
 //     codes (TMA tensor load) into a ring of shared-memory stages.
-//   * Eight worker warps dequantise the codes into the A operand tile (fp16,
-//     K-major, 128-byte swizzle) and convert the x tile in place from bf16 to
-//     fp16.  int4: w = fp16(c * s + m) (one fused multiply-add, single rounding);
+//   * Sixteen worker warps in four groups dequantise the codes into the A
+//     operand tile (fp16, K-major, 128-byte swizzle; one weight row per thread)
+//     and convert the x tile in place from bf16 to fp16 (for large M a small
+//     kernel converts x once per call instead).  Chunk i goes to group i % 4, so
+//     four chunks are in flight and the per-chunk latency chain (wait, convert,
+//     decode, proxy fence, arrive) overlaps.  int4: w = fp16(c * s + m) (one fused multiply-add, single rounding);
 //     NVFP4: w = E2M1 * e4m3 in fp16, exact (the global scale is applied in the
 //     epilogue).  An x value outside the fp16 range sets Q4_DEVERR_FP16_RANGE.
 //   * Warp 1 allocates the TMEM accumulator (128 lanes x TN fp32 columns) and one
@@ -36,9 +39,30 @@ namespace q4 {
 
 constexpr int TC_ROWS = 128;           // weight rows per tile (MMA M)
 constexpr int TC_KC = 64;              // K columns per chunk (128 bytes of fp16)
-constexpr int TC_WORKERS = 8;          // dequant / epilogue warps
+constexpr int TC_GROUPS = 4;           // worker groups: chunk i goes to group i % 4
+constexpr int TC_WORKERS = 4 * TC_GROUPS;   // dequant / epilogue warps
 constexpr int TC_THREADS = (2 + TC_WORKERS) * 32;
 constexpr unsigned kErrFp16Range = 2u;
+
+// Per-CTA timestamps (globaltimer ns) for builds with -DQ4_TRACE: slots 0..7
+// start, TMEM ready, final commit seen by the epilogue, end; 8+i producer issued
+// chunk i, 24+i workers (warp 2) finished chunk i, 40+i MMA issued chunk i.
+#ifdef Q4_TRACE
+__device__ unsigned long long g_q4_tc_trace[1024 * 64];
+__device__ __forceinline__ unsigned long long tc_now()
+{
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+    return t;
+}
+#define TC_TRACE(slot) do { if ((slot) < 64 && blockIdx.x < 1024) g_q4_tc_trace[blockIdx.x * 64 + (slot)] = tc_now(); } while (0)
+extern "C" int q4_tc_trace_copy(unsigned long long *host, int n)
+{
+    return (int)cudaMemcpyFromSymbol(host, g_q4_tc_trace, sizeof(unsigned long long) * n);
+}
+#else
+#define TC_TRACE(slot) ((void)0)
+#endif
 
 struct TcParams {
     const uint8_t *codes;      // [N, K/2]
@@ -54,9 +78,13 @@ struct TcParams {
     int tiles_m;               // ceil(M / TN)
     int KS;                    // split-K factor
     int chunks;                // K / 64
-    int ns;                    // ring stages
+    int ns;                    // ring stages (x and A tiles)
     int tmem_cols;             // power of two >= max(32, TN)
+    int x_f16;                 // x already converted to fp16 (large M)
 };
+
+constexpr int TC_CSTAGES = 2;          // code stages, 4 chunks (128 bytes per row) each
+constexpr int TC_SCALE_AHEAD = 8;      // chunks of group scales loaded ahead
 
 // ------------------------------------------------------------ PTX helpers
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int c0, int c1,
@@ -167,10 +195,11 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
     const uint32_t x_stride = (x_bytes + 1023) & ~1023u;
     unsigned char *xbuf = smem;
     unsigned char *abuf = xbuf + (size_t)NS * x_stride;                 // 16 KB per stage
-    unsigned char *cbuf = abuf + (size_t)NS * 16384;                   // 4 KB per stage
-    uint64_t *bars = reinterpret_cast<uint64_t *>(cbuf + (size_t)NS * 4096);
-    // bars: full[NS], afull[NS], empty[NS], done
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 3 * NS + 1);
+    unsigned char *cbuf = abuf + (size_t)NS * 16384;                   // 16 KB per code stage
+    uint64_t *bars = reinterpret_cast<uint64_t *>(cbuf + (size_t)TC_CSTAGES * 16384);
+    // bars: full[NS], afull[NS], empty[NS], done, cfull[C], cempty[C]
+    uint64_t *cbars = bars + 3 * NS + 1;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(cbars + 2 * TC_CSTAGES);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -186,12 +215,17 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
     const int nch = c1 - c0;
 
     if (threadIdx.x == 0) {
+        TC_TRACE(0);
         for (int i = 0; i < NS; ++i) {
             mbar_init(smem_u32(&bars[i]), 1);                  // TMA arrive + bytes
-            mbar_init(smem_u32(&bars[NS + i]), TC_WORKERS);    // worker warps
+            mbar_init(smem_u32(&bars[NS + i]), 4);             // the chunk's worker group
             mbar_init(smem_u32(&bars[2 * NS + i]), 1);         // MMA commit
         }
         mbar_init(smem_u32(&bars[3 * NS]), 1);                 // final commit
+        for (int i = 0; i < TC_CSTAGES; ++i) {
+            mbar_init(smem_u32(&cbars[i]), 1);                 // TMA arrive + bytes
+            mbar_init(smem_u32(&cbars[TC_CSTAGES + i]), TC_WORKERS);
+        }
         mbar_init_fence();
     }
     if (warp == 1) {
@@ -203,28 +237,42 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    if (threadIdx.x == 0) TC_TRACE(1);
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
         pdl_launch_dependents();
         if (lane == 0) {
-            int issued = 0;
+            int issued = 0, cissued = 0;
             for (int i = 0; i < nch; ++i) {
                 const int s = i % NS, use = i / NS;
                 if (use > 0 && !mbar_wait(smem_u32(&bars[2 * NS + s]), (use - 1) & 1, p.err))
                     break;
+                if (i % 4 == 0) {
+                    // codes of chunks i .. i+3: 128 rows x 128 bytes in one copy
+                    const int j = i / 4, cs = j % TC_CSTAGES, cuse = j / TC_CSTAGES;
+                    if (cuse > 0 &&
+                        !mbar_wait(smem_u32(&cbars[TC_CSTAGES + cs]), (cuse - 1) & 1, p.err))
+                        break;
+                    const uint32_t cfull = smem_u32(&cbars[cs]);
+                    mbar_arrive_expect_tx(cfull, 16384);
+                    tma_load_2d(smem_u32(cbuf + (size_t)cs * 16384), &wmap, (c0 + i) * (TC_KC / 2),
+                                n0, cfull);
+                    cissued = j + 1;
+                }
                 if (i == 0)
                     pdl_wait();                // x comes from the previous kernel
                 const uint32_t full = smem_u32(&bars[s]);
-                mbar_arrive_expect_tx(full, x_bytes + 4096);
-                const int kc = c0 + i;
-                tma_load_2d(smem_u32(xbuf + (size_t)s * x_stride), &xmap, kc * TC_KC, m0, full);
-                tma_load_2d(smem_u32(cbuf + (size_t)s * 4096), &wmap, kc * (TC_KC / 2), n0, full);
+                mbar_arrive_expect_tx(full, x_bytes);
+                tma_load_2d(smem_u32(xbuf + (size_t)s * x_stride), &xmap, (c0 + i) * TC_KC, m0, full);
+                TC_TRACE(8 + i);
                 issued = i + 1;
             }
             // drain: every issued copy has landed before the CTA can exit
             for (int i = issued - NS > 0 ? issued - NS : 0; i < issued; ++i)
                 mbar_wait(smem_u32(&bars[i % NS]), (i / NS) & 1, p.err);
+            for (int j = cissued - TC_CSTAGES > 0 ? cissued - TC_CSTAGES : 0; j < cissued; ++j)
+                mbar_wait(smem_u32(&cbars[j % TC_CSTAGES]), (j / TC_CSTAGES) & 1, p.err);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------- MMA issue
@@ -242,18 +290,19 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
                     mma_f16(tmem_base, smem_desc_sw128(a0 + kk * 32), smem_desc_sw128(b0 + kk * 32),
                             idesc, (i > 0 || kk > 0) ? 1u : 0u);
                 mma_commit(smem_u32(&bars[2 * NS + s]));
+                TC_TRACE(40 + i);
             }
             mma_commit(smem_u32(&bars[3 * NS]));
         }
     } else {
         // ------------------------------------------------------------- workers
-        const int w = warp - 2;                  // 0..7
+        const int w = warp - 2;                  // 0..15
+        const int grp = w >> 2;                  // worker group: chunks i % 4 == grp
         const int quad = warp & 3;               // TMEM lane quadrant of this warp
-        const int half = w >> 2;                 // which 32 codes of the row
         const int r = quad * 32 + lane;          // weight row within the tile
         const int n = n0 + r;
         const bool nok = n < p.N;
-        const int tid = w * 32 + lane;           // 0..255
+        const int gtid = (w & 3) * 32 + lane;    // 0..127 within the group
         auto load_scale = [&](int kc) -> uint32_t {
             if (!nok)
                 return 0u;
@@ -262,23 +311,36 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
                 return ld_nc_u16(static_cast<const uint16_t *>(p.scale) + gi) |
                        (ld_nc_u16(p.minv + gi) << 16);
             } else {
-                // the two e4m3 scales of this thread's 32 codes
-                return ld_nc_u16(static_cast<const uint8_t *>(p.scale) + (int64_t)n * (p.K / 16) +
-                                 kc * 4 + half * 2);
+                // the four e4m3 scales of the chunk's 64 codes
+                return *reinterpret_cast<const uint32_t *>(
+                    static_cast<const uint8_t *>(p.scale) + (int64_t)n * (p.K / 16) + kc * 4);
             }
         };
-        uint32_t sc_next = nch > 0 ? load_scale(c0) : 0u;
+        // group scales come from HBM: keep TC_SCALE_AHEAD of this group's chunks
+        // of them in flight
+        uint32_t scq[TC_SCALE_AHEAD];
+#pragma unroll
+        for (int j = 0; j < TC_SCALE_AHEAD; ++j) {
+            const int ii = grp + j * TC_GROUPS;
+            scq[j] = ii < nch ? load_scale(c0 + ii) : 0u;
+        }
         bool range_bad = false;
-        for (int i = 0; i < nch; ++i) {
+        for (int i = grp; i < nch; i += TC_GROUPS) {
             const int s = i % NS, use = i / NS;
-            const uint32_t sc = sc_next;
-            if (i + 1 < nch)
-                sc_next = load_scale(c0 + i + 1);
+            const uint32_t sc = scq[0];
+#pragma unroll
+            for (int j = 0; j + 1 < TC_SCALE_AHEAD; ++j)
+                scq[j] = scq[j + 1];
+            const int inext = i + TC_SCALE_AHEAD * TC_GROUPS;
+            scq[TC_SCALE_AHEAD - 1] = inext < nch ? load_scale(c0 + inext) : 0u;
+            const int cs = (i / 4) % TC_CSTAGES, cuse = (i / 4) / TC_CSTAGES;
+            if (!mbar_wait(smem_u32(&cbars[cs]), cuse & 1, p.err))
+                break;
             if (!mbar_wait(smem_u32(&bars[s]), use & 1, p.err))
                 break;
             // x tile: bf16 -> fp16 in place (element-wise, swizzle-agnostic)
             uint4 *xv = reinterpret_cast<uint4 *>(xbuf + (size_t)s * x_stride);
-            for (int v = tid; v < TN * 8; v += TC_WORKERS * 32) {
+            for (int v = p.x_f16 ? TN * 8 : gtid; v < TN * 8; v += 128) {
                 const uint4 t = xv[v];
                 const uint32_t e[4] = {t.x, t.y, t.z, t.w};
                 uint32_t o[4];
@@ -295,13 +357,23 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
                     range_bad = true;
                 xv[v] = make_uint4(o[0], o[1], o[2], o[3]);
             }
-            // A rows: this thread's 32 codes of row r -> four 16-byte fp16 chunks
-            const uint4 cw = reinterpret_cast<const uint4 *>(cbuf + (size_t)s * 4096 + r * 32)[half];
-            const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
+            // A row r: the chunk's 64 codes of row r -> eight 16-byte fp16 chunks
+            const uint4 *crow = reinterpret_cast<const uint4 *>(cbuf + (size_t)cs * 16384 + r * 128 +
+                                                                (i % 4) * 32);
+            const uint4 cw0 = crow[0], cw1 = crow[1];
+            const uint32_t words[8] = {cw0.x, cw0.y, cw0.z, cw0.w, cw1.x, cw1.y, cw1.z, cw1.w};
             unsigned char *arow = abuf + (size_t)s * 16384 + (size_t)r * 128;
+            uint32_t sgs[4] = {0u, 0u, 0u, 0u};
+            if constexpr (LAYOUT == 1) {
+                const uint32_t s01 = e4m3x2_to_f16x2(sc & 0xffffu);
+                const uint32_t s23 = e4m3x2_to_f16x2(sc >> 16);
+                sgs[0] = f16x2_splat(s01 & 0xffffu);
+                sgs[1] = f16x2_splat(s01 >> 16);
+                sgs[2] = f16x2_splat(s23 & 0xffffu);
+                sgs[3] = f16x2_splat(s23 >> 16);
+            }
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int chunk = half * 4 + j;          // 8 K columns per chunk
+            for (int j = 0; j < 8; ++j) {               // 8 K columns per 16-byte chunk
                 uint32_t o[4];
                 if constexpr (LAYOUT == 0) {
                     const uint32_t s2 = f16x2_splat(sc & 0xffffu);
@@ -318,19 +390,20 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
                 } else {
                     uint32_t h[4];
                     e2m1x8_to_f16x2x4(words[j], h);
-                    const uint32_t s16 = e4m3x2_to_f16x2(sc);       // two group scales
-                    const uint32_t sg = f16x2_splat(j < 2 ? (s16 & 0xffffu) : (s16 >> 16));
 #pragma unroll
                     for (int b = 0; b < 4; ++b)
-                        o[b] = hmul2(h[b], sg);                     // exact in fp16
+                        o[b] = hmul2(h[b], sgs[j >> 1]);           // exact in fp16
                 }
-                *reinterpret_cast<uint4 *>(arow + ((chunk ^ (r & 7)) << 4)) =
+                *reinterpret_cast<uint4 *>(arow + ((j ^ (r & 7)) << 4)) =
                     make_uint4(o[0], o[1], o[2], o[3]);
             }
             fence_proxy_async();
             __syncwarp();
-            if (lane == 0)
+            if (lane == 0) {
                 mbar_arrive(smem_u32(&bars[NS + s]));
+                mbar_arrive(smem_u32(&cbars[TC_CSTAGES + cs]));
+            }
+            if (warp == 2 && lane == 0) TC_TRACE(24 + i);
         }
         if (range_bad && p.err)
             atomicOr(p.err, kErrFp16Range);
@@ -338,11 +411,12 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
         // ------------------------------------------------------------ epilogue
         const bool ok = nch > 0 && mbar_wait(smem_u32(&bars[3 * NS]), 0, p.err);
         tc_fence_after();
+        if (warp == 2 && lane == 0) TC_TRACE(2);
         float gsc = 1.f;
         if constexpr (LAYOUT == 1)
             gsc = __ldg(p.gscale);
         const int tile = tile_n * p.tiles_m + tile_m;
-        for (int cb = half * 16; cb < TN; cb += 32) {
+        for (int cb = grp * 16; cb < TN; cb += 16 * TC_GROUPS) {
             uint32_t v[16];
             tmem_ld16(tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)cb, v);
             if (!ok)
@@ -367,12 +441,12 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
             __threadfence();
             asm volatile("bar.sync 2, %0;" ::"r"(TC_WORKERS * 32) : "memory");
             __shared__ unsigned last_flag;
-            if (tid == 0)
+            if (w == 0 && lane == 0)
                 last_flag = (ok && atomicAdd(&p.tickets[tile], 1u) == (unsigned)(p.KS - 1)) ? 1u : 0u;
             asm volatile("bar.sync 2, %0;" ::"r"(TC_WORKERS * 32) : "memory");
             if (last_flag) {
                 __threadfence();
-                for (int c = half; c < TN; c += 2) {
+                for (int c = grp; c < TN; c += TC_GROUPS) {
                     const int m = m0 + c;
                     float sum = 0.f;
                     for (int k2 = 0; k2 < p.KS; ++k2)
@@ -380,7 +454,7 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
                     if (nok && m < p.M)
                         p.y[(int64_t)m * p.N + n] = f32_to_bf16_bits(sum * gsc);
                 }
-                if (tid == 0)
+                if (w == 0 && lane == 0)
                     p.tickets[tile] = 0u;
             }
         }
@@ -388,12 +462,43 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
 
     tc_fence_before();
     __syncthreads();
+    if (threadIdx.x == 0) TC_TRACE(3);
     if (warp == 1) {
         __syncwarp();
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;"
                      ::"r"(tmem_base), "r"(p.tmem_cols) : "memory");
     }
+}
+
+// x (bf16) -> fp16 once per call for large M, so that the GEMM's CTAs do not each
+// convert the same token tiles.  Out-of-range values set Q4_DEVERR_FP16_RANGE.
+__global__ void __launch_bounds__(256) q4_x_to_f16_kernel(const uint4 *__restrict__ x,
+                                                          uint4 *__restrict__ out, int64_t n16,
+                                                          unsigned *err)
+{
+    pdl_launch_dependents();
+    pdl_wait();
+    bool bad = false;
+    for (int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; v < n16;
+         v += (int64_t)gridDim.x * blockDim.x) {
+        const uint4 t = x[v];
+        const uint32_t e[4] = {t.x, t.y, t.z, t.w};
+        uint32_t o[4];
+        float mx = 0.f;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float lo = bf16_bits_to_f32(e[j] & 0xffffu);
+            const float hi = bf16_bits_to_f32(e[j] >> 16);
+            mx = fmaxf(mx, fmaxf(fabsf(lo), fabsf(hi)));
+            __half2 h = __floats2half2_rn(lo, hi);
+            o[j] = *reinterpret_cast<uint32_t *>(&h);
+        }
+        bad |= (mx >= 65520.f && mx <= 3.4e38f);
+        out[v] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+    if (bad && err)
+        atomicOr(err, kErrFp16Range);
 }
 
 // ------------------------------------------------------------------ host side
@@ -450,10 +555,15 @@ static int tc_ks(const DeviceInfo &dev, int M, int N, int K)
     return ks < 1 ? 1 : ks;
 }
 
-size_t tc_workspace_bytes(int M, int N, int K, int sms)
+static bool tc_preconvert(int M) { return M > 64; }
+
+static size_t tc_xf16_bytes(int M, int K)
 {
-    if (K % TC_KC || M < 1 || N < 1)
-        return 0;
+    return tc_preconvert(M) ? ((size_t)M * K * 2 + 255) / 256 * 256 : 0;
+}
+
+static size_t tc_split_bytes(int M, int N, int K, int sms)
+{
     DeviceInfo d;
     d.sms = sms;
     const int ks = tc_ks(d, M, N, K);
@@ -462,6 +572,14 @@ size_t tc_workspace_bytes(int M, int N, int K, int sms)
     const int TN = tc_tn(M);
     const size_t tiles = (size_t)((N + TC_ROWS - 1) / TC_ROWS) * ((M + TN - 1) / TN);
     return (tiles * 4 + 255) / 256 * 256 + tiles * ks * TN * TC_ROWS * 4;
+}
+
+// Workspace layout: [fp16 copy of x (large M)][split-K counters][partials].
+size_t tc_workspace_bytes(int M, int N, int K, int sms)
+{
+    if (K % TC_KC || M < 1 || N < 1)
+        return 0;
+    return tc_xf16_bytes(M, K) + tc_split_bytes(M, N, K, sms);
 }
 
 q4_status tc_launch(int kind, const void *x, const uint8_t *codes, const void *scale,
@@ -497,21 +615,52 @@ q4_status tc_launch(int kind, const void *x, const uint8_t *codes, const void *s
     if (need > ws_bytes)
         return fail(Q4_ERR_WORKSPACE, "tensor-core path needs %zu bytes of workspace", need);
     const size_t tiles = (size_t)((N + TC_ROWS - 1) / TC_ROWS) * p.tiles_m;
+    unsigned char *wsb = static_cast<unsigned char *>(ws);
+    const size_t xf16 = tc_xf16_bytes(M, K);
     if (p.KS > 1) {
-        unsigned char *b = static_cast<unsigned char *>(ws);
+        unsigned char *b = wsb + xf16;
         p.tickets = reinterpret_cast<unsigned *>(b);
         p.ws = reinterpret_cast<float *>(b + (tiles * 4 + 255) / 256 * 256);
     }
+    const void *xsrc = x;
+    p.x_f16 = 0;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    if (xf16 > 0) {
+        const int64_t n16 = (int64_t)M * K / 8;
+        int64_t blocks = (n16 + 255) / 256;
+        if (blocks > (int64_t)dev.sms * 8)
+            blocks = (int64_t)dev.sms * 8;
+        cudaLaunchConfig_t pc = {};
+        pc.gridDim = dim3((unsigned)blocks);
+        pc.blockDim = dim3(256);
+        pc.stream = stream;
+        pc.attrs = pdl ? attr : nullptr;
+        pc.numAttrs = pdl ? 1 : 0;
+        const uint4 *xin = static_cast<const uint4 *>(x);
+        uint4 *xo = reinterpret_cast<uint4 *>(wsb);
+        void *pargs[] = {&xin, &xo, (void *)&n16, &p.err};
+        cudaError_t e0 = cudaLaunchKernelExC(&pc, reinterpret_cast<const void *>(&q4_x_to_f16_kernel),
+                                             pargs);
+        if (e0 != cudaSuccess)
+            return cuda_fail(e0, "launch of the x conversion kernel");
+        xsrc = wsb;
+        p.x_f16 = 1;
+    }
     // ring depth: as many stages as fit beside the barriers
     const size_t x_stride = ((size_t)p.TN * 128 + 1023) / 1024 * 1024;
-    const size_t stage = x_stride + 16384 + 4096;
-    int ns = (int)((dev.smem_optin - 2048) / stage);
+    const size_t stage = x_stride + 16384;
+    // budget: alignment slack (1 KB) + static shared memory (1 KB) + code stages
+    // + barriers, the rest for x / A stages
+    int ns = (int)((dev.smem_optin - 2048 - 512 - TC_CSTAGES * 16384) / stage);
     if (ns > 6)
         ns = 6;
     if (ns < 2)
         return fail(Q4_ERR_SHAPE, "tensor-core tile does not fit in shared memory");
     p.ns = ns;
-    const size_t smem = 1024 + (size_t)ns * stage + (3 * ns + 1) * 8 + 16;
+    const size_t smem = 1024 + (size_t)ns * stage + TC_CSTAGES * 16384 +
+                        (3 * ns + 1 + 2 * TC_CSTAGES) * 8 + 16;
 
     CUtensorMap xmap, wmap;
     {
@@ -519,7 +668,9 @@ q4_status tc_launch(int kind, const void *x, const uint8_t *codes, const void *s
         cuuint64_t strides[1] = {(cuuint64_t)K * 2};
         cuuint32_t box[2] = {TC_KC, (cuuint32_t)p.TN};
         cuuint32_t estr[2] = {1, 1};
-        CUresult r = enc(&xmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(x), dims,
+        CUresult r = enc(&xmap, p.x_f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                        : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                         2, const_cast<void *>(xsrc), dims,
                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -529,7 +680,7 @@ q4_status tc_launch(int kind, const void *x, const uint8_t *codes, const void *s
     {
         cuuint64_t dims[2] = {(cuuint64_t)K / 2, (cuuint64_t)N};
         cuuint64_t strides[1] = {(cuuint64_t)K / 2};
-        cuuint32_t box[2] = {TC_KC / 2, TC_ROWS};
+        cuuint32_t box[2] = {2 * TC_KC, TC_ROWS};        // 4 chunks of codes
         cuuint32_t estr[2] = {1, 1};
         CUresult r = enc(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(codes),
                          dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -543,9 +694,6 @@ q4_status tc_launch(int kind, const void *x, const uint8_t *codes, const void *s
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess)
         return cuda_fail(e, "cudaFuncSetAttribute(tensor-core kernel)");
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(tiles * p.KS));
     cfg.blockDim = dim3(TC_THREADS);
