@@ -33,11 +33,12 @@ if ROOT not in sys.path:
 
 METRIC = "4-bit decode GEMV µs/call & effective weight GB/s (% of GB300 HBM peak)"
 
-# DRAM traffic of one launch of the streaming kernel on the default workload, from
-# the ncu capture summarised in profiles/ (dram__bytes_read.sum +
-# dram__bytes_write.sum), valid only for the kernel source it was taken on.
+# DRAM traffic of one launch of the decode GEMV kernel on a workload, from the ncu
+# capture summarised in profiles/ (dram__bytes_read.sum + dram__bytes_write.sum),
+# valid only for the kernel sources it was taken on (see _kernel_sha).
 TRAFFIC = {
-    # workload key: (bytes per launch, sha256 of csrc/gemv.cu when captured)
+    # workload key: (bytes per launch, _kernel_sha() when captured)
+    "nvfp4_gemv": (18900736, "e14521010cf4e1eec52a90f75e29d717d0f3fd88cee57657afe983e23de352e4"),
 }
 
 
@@ -77,9 +78,19 @@ def _peaks():
     return 6800.0, "fallback"
 
 
-def _src_sha(rel: str) -> str:
-    with open(os.path.join(ROOT, rel), "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()
+KERNEL_SOURCES = ("bit_weight_only_q4_gb300/csrc/gemv_rows.cu",
+                  "bit_weight_only_q4_gb300/csrc/stream_common.cuh",
+                  "bit_weight_only_q4_gb300/csrc/q4_device.cuh")
+
+
+def _kernel_sha() -> str:
+    """Hash of the sources of the decode GEMV kernel (traffic figures are only
+    valid for the kernel they were captured on)."""
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
 
 
 class ClockSampler:
@@ -368,19 +379,39 @@ def run_extra(args, local):
 
 def run_profile(args, local):
     """Plain launches for an ncu capture: W warm-up calls, then K calls, no graphs
-    and no timing (a number printed under a profiler is never a bench value)."""
+    and no timing (a number printed under a profiler is never a bench value).
+    GEMV workloads rotate their weight ring; prefill runs the int4 K=2048 ->
+    N=8192 GEMM at M=2048; batched runs the NVFP4 K=8192 -> N=2048 GEMM at M=48."""
     import torch
     from bit_weight_only_q4_gb300 import build as libbuild
-    from bit_weight_only_q4_gb300 import q4
+    from bit_weight_only_q4_gb300 import q4, synth
+    from tests import parity as P
     torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
     libbuild.build()
     q4.load()
     q4.set_launch_flags(0)
-    wl = Workload(args.workload, torch.device("cuda", local))
+    if args.workload in ("nvfp4_gemv", "int4_gemv"):
+        wl = Workload(args.workload, device)
+        call, desc = wl.call, wl.desc
+    elif args.workload == "prefill":
+        x, w = synth.prefill("int4", 0)
+        xd, wd = P.bf16_dev(x), P.int4_dev(w)
+        ws = q4.alloc_workspace(q4.LAYOUT_INT4G128, x.shape[0], w.N, w.K, device)
+        call = lambda i: q4.q4_linear_int4g128(xd, *wd, workspace=ws)
+        desc = "prefill int4 M=2048 K=2048 N=8192"
+    elif args.workload == "batched":
+        x, w = synth.nvfp4_batched(1, 48)
+        xd, wd = P.bf16_dev(x), P.nvfp4_dev(w)
+        ws = q4.alloc_workspace(q4.LAYOUT_NVFP4, 48, w.N, w.K, device)
+        call = lambda i: q4.q4_linear_nvfp4(xd, *wd, workspace=ws)
+        desc = "nvfp4 M=48 K=8192 N=2048"
+    else:
+        raise SystemExit(f"--profile does not cover {args.workload}")
     for i in range(args.warmup + args.steps):
-        wl.call(i)
+        call(i)
     torch.cuda.synchronize()
-    print(json.dumps({"profile_run": wl.desc, "calls": args.warmup + args.steps}))
+    print(json.dumps({"profile_run": desc, "calls": args.warmup + args.steps}))
 
 
 def run_gpu(args, world, rank, local):
@@ -451,7 +482,7 @@ def run_gpu(args, world, rank, local):
     peak, peak_src = _peaks()
     traffic = None
     t = TRAFFIC.get(args.workload)
-    if t and t[1] == _src_sha("bit_weight_only_q4_gb300/csrc/gemv.cu"):
+    if t and t[1] == _kernel_sha():
         traffic = t[0]
 
     cpu_baseline = None
