@@ -38,7 +38,7 @@ METRIC = "4-bit decode GEMV µs/call & effective weight GB/s (% of GB300 HBM pea
 # valid only for the kernel sources it was taken on (see _kernel_sha).
 TRAFFIC = {
     # workload key: (bytes per launch, _kernel_sha() when captured)
-    "nvfp4_gemv": (18900736, "e14521010cf4e1eec52a90f75e29d717d0f3fd88cee57657afe983e23de352e4"),
+    "nvfp4_gemv": (18916352, "57230a01d6632c75587dbd2900a7711fb40f7787a56cdb41b3762b82ef2eb6fc"),
 }
 
 

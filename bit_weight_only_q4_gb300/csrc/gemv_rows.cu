@@ -1,26 +1,35 @@
-// Register-prefetch weight-streaming kernel for sm_103a: the decode GEMV of both
-// 4-bit layouts for one to four tokens, and the restricted BF16 head.
+// Weight-streaming kernels for sm_103a that own whole rows: the decode GEMV of
+// both 4-bit layouts for one to four tokens, and the restricted BF16 head.
 //
 // Same arithmetic as the other streaming kernels (stream_common.cuh: prescaled
 // fp16 x, shift-free E2M1 / fp16-magic int4 decode, fp32 accumulation by
 // mixed-precision FMAs).  Data movement is chosen for short, dependent calls:
 //
-//   * Small CTAs (8 warps) each own a contiguous range of output rows with their
-//     full K.  Warp w owns one k-step ks = w % S (1024 4-bit or 256 bf16
-//     columns) of the rows g, g + G, g + 2G, ... of its CTA (g = w / S, G = 8/S).
-//   * Before griddepcontrol.wait every lane issues the 128-bit loads of its
-//     first RB rows (codes and scales): weights do not depend on the previous
-//     kernel, so they stream while that kernel finishes.  With up to four CTAs
-//     per SM, a CTA of the next call starts loading as soon as any CTA of this
-//     call exits.  (A TMA bulk-copy ring was measured slower here: the per-SM
-//     copy engine sustained ~26 GB/s in this short-burst pattern, below the
-//     ~44 GB/s per SM that HBM delivers.)
-//   * After the wait the CTA stages x once in shared memory; every warp keeps
-//     its k-step's slice in registers, decodes and multiplies its rows, reduces
-//     each row across lanes (transposing butterfly) and parks the partial per
-//     k-step in shared memory; later row batches are loaded after the first.
-//   * A final pass sums each row's S partials in k order and stores bf16.  No
-//     row is split between CTAs: no workspace, deterministic results.
+//   * Each CTA owns a contiguous range of output rows with their full K.  Warp w
+//     owns one k-step ks = w % S (1024 4-bit or 256 bf16 columns) of the rows
+//     g, g + G, g + 2G, ... of its CTA (g = w / S, G = warps / S).  S is a
+//     template parameter, so the warp geometry costs no divisions.  No row is
+//     split between CTAs: no workspace, deterministic results.
+//   * Weights do not depend on the previous kernel, so they are requested
+//     before griddepcontrol.wait.  For one token a call runs one 16-warp CTA per
+//     SM on half of the SM's registers and shared memory, so the next call's CTA
+//     is resident beside it (programmatic dependent launch) and streams its
+//     weights while this call computes.
+//   * After the wait the CTA stages x once in shared memory (prescaled fp16);
+//     every warp keeps its k-step's slice in registers, decodes and multiplies
+//     its rows, reduces each row across lanes (transposing butterfly) and parks
+//     the partial per k-step in shared memory.  A final pass sums each row's S
+//     partials in k order and stores bf16.
+//
+// Bringing the weights in: for one token the first RB rows of every warp come
+// straight into registers with 128-bit loads; every later row comes through a
+// per-thread ring of NB * RB shared-memory slots filled with cp.async (each lane
+// copies its own 16-byte slice, so no barrier is needed; the group scales come
+// with plain loads into a matching register ring).  Both are issued before
+// griddepcontrol.wait.  (Measured on the NVFP4 16384 x 2048 GEMV chain: a TMA
+// bulk-copy stage ring was slower, 6.9 against 5.2 us per call, and a deeper
+// cp.async ring did not help: 16 warps of cp.async per SM are throttled near
+// 34 GB/s, so fewer requests in flight let the first rows land sooner.)
 //
 // Eligibility: S = ceil(K / kstep) in {1, 2, 4, 8}; 16-byte aligned rows (int4
 // always, NVFP4 K % 32 == 0, bf16 H % 8 == 0).  Other shapes use gemv.cu.
@@ -30,74 +39,26 @@
 
 namespace q4 {
 
-constexpr int RK_WARPS = 8;
-constexpr int RK_THREADS = RK_WARPS * 32;
-
-template <int WK, int MT, int RB>
-__global__ void __launch_bounds__(RK_THREADS, (MT == 1 ? 4 : 2)) q4_rows_kernel(GemvParams p)
+// Ring bytes of a CTA of NW warps holding NB batches of RB rows per thread.
+__host__ __device__ constexpr size_t rows_ring_bytes(int NW, int NB, int RB)
 {
-    extern __shared__ __align__(16) unsigned char smem[];
-    constexpr int KSTEP = Kind<WK>::KSTEP;
-    constexpr int COLS = Kind<WK>::COLS;
-    constexpr int CH = Kind<WK>::CH;
-    constexpr int XV = (WK == W_BF16) ? 4 : 16;      // x registers per token
-    const int S = p.S;
-    const int G = RK_WARPS / S;
-    const int warp = threadIdx.x >> 5;
-    const int lane = threadIdx.x & 31;
-    const int ks = warp % S;
-    const int g = warp / S;
-    const int col0 = ks * KSTEP + lane * COLS;
-    const bool colok = col0 < p.K;
-    const int Kpad = S * KSTEP;
-    uint16_t *xs = reinterpret_cast<uint16_t *>(smem);
-    float *cf = reinterpret_cast<float *>(smem + (size_t)MT * Kpad * 2);
-    float *red = cf + (size_t)MT * (Kpad / 32) * CH;        // [row][ks][m] partials
-    const int64_t n0 = (int64_t)blockIdx.x * p.N / p.grid;
-    const int64_t n1 = ((int64_t)blockIdx.x + 1) * p.N / p.grid;
-    const int rows_cta = (int)(n1 - n0);
-    const int my_rows = rows_cta > g ? (rows_cta - g + G - 1) / G : 0;   // rows g + G*j
+    return (size_t)NB * RB * NW * 32 * 16;
+}
 
-    uint4 q[RB];
-    uint32_t sw[RB];
-    auto load_batch = [&](int j0) {
-#pragma unroll
-        for (int r = 0; r < RB; ++r) {
-            q[r] = make_uint4(0u, 0u, 0u, 0u);
-            sw[r] = 0u;
-            const int j = j0 + r;
-            if (j < my_rows && colok) {
-                const int64_t n = n0 + g + (int64_t)G * j;
-                const int64_t prow = n < p.n_rows ? (int64_t)p.row_begin + n : (int64_t)p.extra_row;
-                if constexpr (WK == W_BF16) {
-                    q[r] = ld_stream_v4(p.w + prow * p.w_row_bytes + (int64_t)col0 * 2);
-                } else {
-                    q[r] = ld_stream_v4(p.w + prow * p.w_row_bytes + col0 / 2);
-                    if constexpr (WK == W_INT4) {
-                        const int64_t gi = prow * (p.K / 128) + col0 / 128;
-                        sw[r] = ld_nc_u16(static_cast<const uint16_t *>(p.scale) + gi) |
-                                (ld_nc_u16(p.minv + gi) << 16);
-                    } else {
-                        sw[r] = ld_nc_u16(static_cast<const uint8_t *>(p.scale) +
-                                          prow * (p.K / 16) + col0 / 16);
-                    }
-                }
-            }
-        }
-    };
+// One token (MT = 1): one 16-warp CTA per SM per call at 64 registers, so the
+// CTA of the next call fits beside it.  Several tokens: 8-warp CTAs, two per SM.
+template <int MT>
+struct RowsShape {
+    static constexpr int NW = MT == 1 ? 16 : 8;
+    static constexpr int MIN_CTAS = 2;
+};
 
-    // weights (and the global scale) do not depend on the previous kernel
-    load_batch(0);
-    float gsc = 1.f;
-    if constexpr (WK == W_NVFP4_A16)
-        gsc = __ldg(p.gscale);
-    pdl_launch_dependents();
-    pdl_wait();                                   // x comes from the previous kernel
-    stage_x<WK, MT>(p, Kpad, xs, cf, (int)threadIdx.x, RK_THREADS);
-    __syncthreads();
-
-    uint32_t xr[MT][XV];
-    float4 cd[MT];           // int4: (2^-p, X1, X2, -); NVFP4: (2^-p * g, ...)
+// x slice of one lane in registers (XV words per token) and its per-chunk data.
+template <int WK, int MT, int XV>
+__device__ __forceinline__ void rows_load_x(const uint16_t *xs, const float *cf, int Kpad,
+                                            int ks, int lane, int col0, float gsc,
+                                            uint32_t (&xr)[MT][XV], float4 (&cd)[MT])
+{
 #pragma unroll
     for (int m = 0; m < MT; ++m) {
         if constexpr (WK == W_BF16) {
@@ -118,102 +79,114 @@ __global__ void __launch_bounds__(RK_THREADS, (MT == 1 ? 4 : 2)) q4_rows_kernel(
                 cd[m] = make_float4(cf[(size_t)m * (Kpad / 32) + col0 / 32] * gsc, 0.f, 0.f, 0.f);
         }
     }
+}
 
-    for (int j0 = 0; j0 < my_rows; j0 += RB) {
-        if (j0 > 0)
-            load_batch(j0);
-        float part[RB * MT];
+// One lane's share of one row: 16 weight bytes (w4) and its scale word (int4:
+// fp16 scale | fp16 min << 16; NVFP4: two e4m3 group scales) against MT tokens.
+template <int WK, int MT, int XV>
+__device__ __forceinline__ void rows_dot(const uint4 qv, uint32_t swr,
+                                         const uint32_t (&xr)[MT][XV], const float4 (&cd)[MT],
+                                         float *out)
+{
+    const uint32_t w4[4] = {qv.x, qv.y, qv.z, qv.w};
+    if constexpr (WK == W_BF16) {
 #pragma unroll
-        for (int r = 0; r < RB; ++r) {
-            const uint32_t w4[4] = {q[r].x, q[r].y, q[r].z, q[r].w};
-            if constexpr (WK == W_BF16) {
+        for (int m = 0; m < MT; ++m) {
+            float t = 0.f;
 #pragma unroll
-                for (int m = 0; m < MT; ++m) {
-                    float t = 0.f;
+            for (int jj = 0; jj < 4; ++jj)
+                t = fma2_bf16(t, w4[jj], xr[m][jj]);
+            out[m] = t;
+        }
+    } else if constexpr (WK == W_INT4) {
+        float A1[MT], A2[MT];
 #pragma unroll
-                    for (int jj = 0; jj < 4; ++jj)
-                        t = fma2_bf16(t, w4[jj], xr[m][jj]);
-                    part[r * MT + m] = t;
-                }
-            } else if constexpr (WK == W_INT4) {
-                float A1[MT], A2[MT];
+        for (int m = 0; m < MT; ++m) {
+            A1[m] = 0.f;
+            A2[m] = 0.f;
+        }
 #pragma unroll
-                for (int m = 0; m < MT; ++m) {
-                    A1[m] = 0.f;
-                    A2[m] = 0.f;
-                }
+        for (int jj = 0; jj < 4; ++jj) {
+            const uint32_t w8 = w4[jj] >> 8;
+            const uint32_t pa = int4_pair_f16_biased<0x000F000Fu>(w4[jj]);  // cols 0, 4
+            const uint32_t pb = int4_pair_f16_biased<0x00F000F0u>(w4[jj]);  // cols 1, 5
+            const uint32_t pc = int4_pair_f16_biased<0x000F000Fu>(w8);      // cols 2, 6
+            const uint32_t pd = int4_pair_f16_biased<0x00F000F0u>(w8);      // cols 3, 7
 #pragma unroll
-                for (int jj = 0; jj < 4; ++jj) {
-                    const uint32_t w8 = w4[jj] >> 8;
-                    const uint32_t pa = int4_pair_f16_biased<0x000F000Fu>(w4[jj]);  // cols 0, 4
-                    const uint32_t pb = int4_pair_f16_biased<0x00F000F0u>(w4[jj]);  // cols 1, 5
-                    const uint32_t pc = int4_pair_f16_biased<0x000F000Fu>(w8);      // cols 2, 6
-                    const uint32_t pd = int4_pair_f16_biased<0x00F000F0u>(w8);      // cols 3, 7
-#pragma unroll
-                    for (int m = 0; m < MT; ++m) {
-                        A1[m] = fma2_f16(A1[m], pa, xr[m][4 * jj + 0]);
-                        A2[m] = fma2_f16(A2[m], pb, xr[m][4 * jj + 1]);
-                        A1[m] = fma2_f16(A1[m], pc, xr[m][4 * jj + 2]);
-                        A2[m] = fma2_f16(A2[m], pd, xr[m][4 * jj + 3]);
-                    }
-                }
-                const float sc = f16lo_to_f32(sw[r]);
-                const float mn = f16hi_to_f32(sw[r]);
-                const float c1 = fmaf(-1024.f, sc, mn);
-                const float c2 = fmaf(-64.f, sc, mn);
-                const float s16 = sc * 0.0625f;
-#pragma unroll
-                for (int m = 0; m < MT; ++m) {
-                    float t = sc * A1[m];
-                    t = fmaf(s16, A2[m], t);
-                    t = fmaf(c1, cd[m].y, t);
-                    t = fmaf(c2, cd[m].z, t);
-                    part[r * MT + m] = t * cd[m].x;
-                }
-            } else {
-                float Ta[MT], Tb[MT];
-#pragma unroll
-                for (int m = 0; m < MT; ++m) {
-                    Ta[m] = 0.f;
-                    Tb[m] = 0.f;
-                }
-#pragma unroll
-                for (int jj = 0; jj < 4; ++jj) {
-                    uint32_t h[4];
-                    e2m1x8_to_f16x2x4(w4[jj], h);
-#pragma unroll
-                    for (int b = 0; b < 4; ++b) {
-#pragma unroll
-                        for (int m = 0; m < MT; ++m) {
-                            if (jj < 2)
-                                Ta[m] = fma2_f16(Ta[m], h[b], xr[m][4 * jj + b]);
-                            else
-                                Tb[m] = fma2_f16(Tb[m], h[b], xr[m][4 * jj + b]);
-                        }
-                    }
-                }
-                const uint32_t s2 = e4m3x2_to_f16x2(sw[r]);
-                const float sa = f16lo_to_f32(s2);
-                const float sb = f16hi_to_f32(s2);
-#pragma unroll
-                for (int m = 0; m < MT; ++m)
-                    part[r * MT + m] = fmaf(Ta[m], sa, Tb[m] * sb) * cd[m].x;
+            for (int m = 0; m < MT; ++m) {
+                A1[m] = fma2_f16(A1[m], pa, xr[m][4 * jj + 0]);
+                A2[m] = fma2_f16(A2[m], pb, xr[m][4 * jj + 1]);
+                A1[m] = fma2_f16(A1[m], pc, xr[m][4 * jj + 2]);
+                A2[m] = fma2_f16(A2[m], pd, xr[m][4 * jj + 3]);
             }
         }
-        int idx = 0;
-        const float tot = warp_sum_transpose<RB * MT>(part, lane, idx);
-        const int r = idx / MT, m = idx - (idx / MT) * MT;
-        const int j = j0 + r;
-        if ((lane & (32 / (RB * MT) - 1)) == 0 && j < my_rows) {
-            const int row = g + G * j;
-            red[((size_t)row * S + ks) * MT + m] = tot;
+        const float sc = f16lo_to_f32(swr);
+        const float mn = f16hi_to_f32(swr);
+        const float c1 = fmaf(-1024.f, sc, mn);
+        const float c2 = fmaf(-64.f, sc, mn);
+        const float s16 = sc * 0.0625f;
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
+            float t = sc * A1[m];
+            t = fmaf(s16, A2[m], t);
+            t = fmaf(c1, cd[m].y, t);
+            t = fmaf(c2, cd[m].z, t);
+            out[m] = t * cd[m].x;
         }
+    } else {
+        float Ta[MT], Tb[MT];
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
+            Ta[m] = 0.f;
+            Tb[m] = 0.f;
+        }
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+            uint32_t hh[4];
+            e2m1x8_to_f16x2x4(w4[jj], hh);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+#pragma unroll
+                for (int m = 0; m < MT; ++m) {
+                    if (jj < 2)
+                        Ta[m] = fma2_f16(Ta[m], hh[q], xr[m][4 * jj + q]);
+                    else
+                        Tb[m] = fma2_f16(Tb[m], hh[q], xr[m][4 * jj + q]);
+                }
+            }
+        }
+        const uint32_t s2 = e4m3x2_to_f16x2(swr);
+        const float sa = f16lo_to_f32(s2);
+        const float sb = f16hi_to_f32(s2);
+#pragma unroll
+        for (int m = 0; m < MT; ++m)
+            out[m] = fmaf(Ta[m], sa, Tb[m] * sb) * cd[m].x;
     }
+}
 
-    __syncthreads();
-    for (int e = (int)threadIdx.x; e < rows_cta * MT; e += RK_THREADS) {
+// Sum RB x MT partials across the warp and park each row's total for k-step ks.
+template <int RB, int MT, int S>
+__device__ __forceinline__ void rows_park(float (&part)[RB * MT], int lane, int ks, int row0,
+                                          int G, int nvalid, float *red)
+{
+    int idx = 0;
+    const float tot = warp_sum_transpose<RB * MT>(part, lane, idx);
+    const int r = idx / MT, m = idx - (idx / MT) * MT;
+    if ((lane & (32 / (RB * MT) - 1)) == 0 && r < nvalid) {
+        const int row = row0 + G * r;
+        red[((size_t)row * S + ks) * MT + m] = tot;
+    }
+}
+
+// Final pass: each row's S partials summed in k order, stored as bf16.
+template <int MT, int S>
+__device__ __forceinline__ void rows_store(const GemvParams &p, const float *red, int n0,
+                                           int rows_cta, int nthreads)
+{
+    for (int e = (int)threadIdx.x; e < rows_cta * MT; e += nthreads) {
         const int row = e / MT, m = e - (e / MT) * MT;
         float s = 0.f;
+#pragma unroll
         for (int k = 0; k < S; ++k)
             s += red[((size_t)row * S + k) * MT + m];
         if (m < p.mcount)
@@ -221,36 +194,176 @@ __global__ void __launch_bounds__(RK_THREADS, (MT == 1 ? 4 : 2)) q4_rows_kernel(
     }
 }
 
-// ------------------------------------------------------------------ host side
-template <int WK, int MT, int RB>
-static const void *rows_ptr()
+// Physical weight row of logical row n.
+__device__ __forceinline__ int64_t rows_phys(const GemvParams &p, int64_t n)
 {
-    return reinterpret_cast<const void *>(&q4_rows_kernel<WK, MT, RB>);
+    return n < p.n_rows ? (int64_t)p.row_begin + n : (int64_t)p.extra_row;
 }
 
+// Scale word of physical row prow for the lane whose columns start at col0.
 template <int WK>
-static const void *rows_select_kind(int mt, int rb)
+__device__ __forceinline__ uint32_t rows_scale_global(const GemvParams &p, int64_t prow, int col0)
 {
-#define Q4_R(MT_, RB_) if (mt == MT_ && rb == RB_) return rows_ptr<WK, MT_, RB_>();
-    Q4_R(1, 4) Q4_R(1, 8) Q4_R(2, 2) Q4_R(2, 4) Q4_R(4, 1) Q4_R(4, 2)
-#undef Q4_R
+    if constexpr (WK == W_INT4) {
+        const int64_t gi = prow * (p.K / 128) + col0 / 128;
+        return ld_nc_u16(static_cast<const uint16_t *>(p.scale) + gi) | (ld_nc_u16(p.minv + gi) << 16);
+    } else if constexpr (WK == W_NVFP4_A16) {
+        return ld_nc_u16(static_cast<const uint8_t *>(p.scale) + prow * (p.K / 16) + col0 / 16);
+    } else {
+        return 0u;
+    }
+}
+
+// ------------------------------------------------------------ cp.async ring
+template <int WK, int MT, int RB, int S, int NB, int REG>
+__global__ void __launch_bounds__(RowsShape<MT>::NW * 32, RowsShape<MT>::MIN_CTAS)
+q4_rows_kernel(GemvParams p)
+{
+    constexpr int RK_WARPS = RowsShape<MT>::NW;
+    constexpr int RK_THREADS = RK_WARPS * 32;
+    extern __shared__ __align__(16) unsigned char smem[];
+    constexpr int KSTEP = Kind<WK>::KSTEP;
+    constexpr int COLS = Kind<WK>::COLS;
+    constexpr int CH = Kind<WK>::CH;
+    constexpr int XV = (WK == W_BF16) ? 4 : 16;      // x registers per token
+    constexpr int G = RK_WARPS / S;
+    constexpr int NSLOT = NB * RB;
+    constexpr int Kpad = S * KSTEP;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int ks = warp % S;
+    const int g = warp / S;
+    const int col0 = ks * KSTEP + lane * COLS;
+    const bool colok = col0 < p.K;
+    const uint32_t ring = smem_u32(smem) + threadIdx.x * 16;   // slot i at + i * 16 * threads
+    const uint4 *ring_ld = reinterpret_cast<const uint4 *>(smem) + threadIdx.x;
+    constexpr size_t RING = rows_ring_bytes(RK_WARPS, NB, RB);
+    uint16_t *xs = reinterpret_cast<uint16_t *>(smem + RING);
+    float *cf = reinterpret_cast<float *>(smem + RING + (size_t)MT * Kpad * 2);
+    float *red = cf + (size_t)MT * (Kpad / 32) * CH;        // [row][ks][m] partials
+    const int b = blockIdx.x;
+    const int n0 = b * p.rows_q + (b < p.rows_r ? b : p.rows_r);
+    const int rows_cta = p.rows_q + (b < p.rows_r ? 1 : 0);
+    const int my_rows = rows_cta > g ? (rows_cta - g + G - 1) / G : 0;   // rows g + G*j
+    const int my_ring = my_rows > REG ? my_rows - REG : 0;    // rows j >= REG use the ring
+    const int64_t colbyte = (WK == W_BF16) ? (int64_t)col0 * 2 : (int64_t)(col0 / 2);
+
+    // Request ring row jr (row j = REG + jr of this warp) into ring slot `slot`
+    // (one commit group per call, empty past the last row, so wait_group counts
+    // stay uniform).
+    uint32_t sw[NSLOT];
+    auto issue = [&](int jr, int slot) {
+        uint32_t sv = 0u;
+        if (jr < my_ring) {
+            const uint8_t *src = p.w;
+            if (colok) {
+                const int64_t prow = rows_phys(p, n0 + g + G * (REG + jr));
+                src = p.w + prow * p.w_row_bytes + colbyte;
+                sv = rows_scale_global<WK>(p, prow, col0);
+            }
+            cp_async_16(ring + (uint32_t)slot * (RK_THREADS * 16), src, colok ? 16u : 0u);
+        }
+        sw[slot] = sv;
+        cp_async_commit();
+    };
+
+    // the first REG rows of the warp: 128-bit loads straight into registers
+    constexpr int NREG = REG > 0 ? REG : 1;
+    uint4 q[NREG];
+    uint32_t sq[NREG];
+#pragma unroll
+    for (int r = 0; r < NREG; ++r) {
+        q[r] = make_uint4(0u, 0u, 0u, 0u);
+        sq[r] = 0u;
+        if (r < REG && r < my_rows && colok) {
+            const int64_t prow = rows_phys(p, n0 + g + G * r);
+            q[r] = ld_stream_v4(p.w + prow * p.w_row_bytes + colbyte);
+            sq[r] = rows_scale_global<WK>(p, prow, col0);
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < NSLOT; ++i)
+        issue(i, i);
+    float gsc = 1.f;
+    if constexpr (WK == W_NVFP4_A16)
+        gsc = __ldg(p.gscale);
+    pdl_launch_dependents();
+    pdl_wait();                                   // x comes from the previous kernel
+    stage_x<WK, MT>(p, Kpad, xs, cf, (int)threadIdx.x, RK_THREADS);
+    __syncthreads();
+
+    uint32_t xr[MT][XV];
+    float4 cd[MT];           // int4: (2^-p, X1, X2, -); NVFP4: (2^-p * g, ...)
+    rows_load_x<WK, MT, XV>(xs, cf, Kpad, ks, lane, col0, gsc, xr, cd);
+
+    if constexpr (REG > 0) {
+        static_assert(REG == RB, "the register batch is one row batch");
+        float part[RB * MT];
+#pragma unroll
+        for (int r = 0; r < RB; ++r)
+            rows_dot<WK, MT, XV>(q[r], sq[r], xr, cd, part + r * MT);
+        rows_park<RB, MT, S>(part, lane, ks, g, G, my_rows, red);
+    }
+
+    for (int j0 = 0; j0 < my_ring; j0 += NSLOT) {
+#pragma unroll
+        for (int h = 0; h < NB; ++h) {
+            const int jb = j0 + h * RB;
+            if (jb >= my_ring)
+                break;
+            cp_async_wait<(NB - 1) * RB>();       // this batch's RB groups have landed
+            float part[RB * MT];
+#pragma unroll
+            for (int r = 0; r < RB; ++r)
+                rows_dot<WK, MT, XV>(ring_ld[(h * RB + r) * RK_THREADS], sw[h * RB + r], xr, cd,
+                                     part + r * MT);
+            // the slots' contents are in registers now: refill them NB * RB rows ahead
+#pragma unroll
+            for (int r = 0; r < RB; ++r)
+                issue(jb + NSLOT + r, h * RB + r);
+            rows_park<RB, MT, S>(part, lane, ks, g + G * (REG + jb), G, my_ring - jb, red);
+        }
+    }
+    cp_async_wait<0>();                           // nothing left in flight at exit
+    __syncthreads();
+    rows_store<MT, S>(p, red, n0, rows_cta, RK_THREADS);
+}
+
+// ------------------------------------------------------------------ host side
+template <int WK, int MT, int RB, int NB>
+static const void *rows_select_s(int S)
+{
+    constexpr int REG = MT == 1 ? RB : 0;       // one token: first batch in registers
+    if (S == 1) return reinterpret_cast<const void *>(&q4_rows_kernel<WK, MT, RB, 1, NB, REG>);
+    if (S == 2) return reinterpret_cast<const void *>(&q4_rows_kernel<WK, MT, RB, 2, NB, REG>);
+    if (S == 4) return reinterpret_cast<const void *>(&q4_rows_kernel<WK, MT, RB, 4, NB, REG>);
+    if (S == 8) return reinterpret_cast<const void *>(&q4_rows_kernel<WK, MT, RB, 8, NB, REG>);
     return nullptr;
 }
 
-static const void *rows_select(int kind, int mt, int rb)
+// (MT, RB, NB) variants: one token (1, 4, 2), two (2, 4, 2), four (4, 2, 2).
+template <int WK>
+static const void *rows_select_kind(int mt, int nb, int S)
 {
-    if (kind == W_INT4) return rows_select_kind<W_INT4>(mt, rb);
-    if (kind == W_NVFP4_A16) return rows_select_kind<W_NVFP4_A16>(mt, rb);
-    if (kind == W_BF16) return rows_select_kind<W_BF16>(mt, rb);
+    (void)nb;
+    if (mt == 1) return rows_select_s<WK, 1, 4, 2>(S);
+    if (mt == 2) return rows_select_s<WK, 2, 4, 2>(S);
+    if (mt == 4) return rows_select_s<WK, 4, 2, 2>(S);
     return nullptr;
 }
 
-#ifndef Q4_ROWS_RB
-#define Q4_ROWS_RB 0          // rows per warp batch for M = 1; 0 = planner
-#endif
-#ifndef Q4_ROWS_CTAS_PER_SM
-#define Q4_ROWS_CTAS_PER_SM 4
-#endif
+static const void *rows_select(const RowsPlan &pl)
+{
+    if (pl.kind == W_INT4) return rows_select_kind<W_INT4>(pl.mt, pl.nb, pl.S);
+    if (pl.kind == W_NVFP4_A16) return rows_select_kind<W_NVFP4_A16>(pl.mt, pl.nb, pl.S);
+    if (pl.kind == W_BF16) return rows_select_kind<W_BF16>(pl.mt, pl.nb, pl.S);
+    return nullptr;
+}
+
+static int rows_warps(const RowsPlan &pl)
+{
+    return pl.mt == 1 ? RowsShape<1>::NW : RowsShape<2>::NW;
+}
 
 bool rows_eligible(int kind, int K)
 {
@@ -271,49 +384,53 @@ q4_status rows_plan(const DeviceInfo &dev, int kind, int M, int N, int K, RowsPl
     const int kstep = kind == W_BF16 ? 256 : 1024;
     const int ch = kind == W_INT4 ? 4 : (kind == W_BF16 ? 0 : 1);
     plan.S = (K + kstep - 1) / kstep;
-    const int G = RK_WARPS / plan.S;
-    const size_t Kpad = (size_t)plan.S * kstep;
     plan.mt = M >= 4 ? 4 : (M >= 2 ? 2 : 1);
-    plan.rb = plan.mt == 4 ? 2 : (plan.mt == 2 ? 4 : 4);
-    if (plan.mt == 1 && Q4_ROWS_RB > 0)
-        plan.rb = Q4_ROWS_RB;
-    // about four CTAs per SM (one batch of RB rows per warp when the matrix is
-    // small enough), each with a contiguous row range
-    int64_t grid = (int64_t)dev.sms * Q4_ROWS_CTAS_PER_SM;
-    const int64_t rows_one_batch = (int64_t)G * plan.rb;
-    const int64_t want = ((int64_t)N + rows_one_batch - 1) / rows_one_batch;
+    plan.rb = plan.mt == 4 ? 2 : 4;
+    const int nw = plan.mt == 1 ? RowsShape<1>::NW : RowsShape<2>::NW;
+    const int G = nw / plan.S;
+    const size_t Kpad = (size_t)plan.S * kstep;
+    // Grid: one 16-warp CTA per SM per call for one token, two 8-warp CTAs for
+    // several (at least one row per warp group); per-row partials capped at
+    // 24 KB per CTA.
+    int64_t grid = (int64_t)dev.sms * (plan.mt == 1 ? 1 : 2);
+    const int64_t want = ((int64_t)N + G - 1) / G;
     if (want < grid)
         grid = want;
-    if (grid < 1)
-        grid = 1;
-    // per-row partials must fit: cap rows per CTA at 24 KB of partials
     const int64_t rows_limit = (24 * 1024) / ((int64_t)plan.S * plan.mt * 4);
     const int64_t need = ((int64_t)N + rows_limit - 1) / rows_limit;
     if (need > grid)
         grid = need;
+    if (grid < 1)
+        grid = 1;
     if (grid > 0x7fffffff)
         return fail(Q4_ERR_SHAPE, "N=%d too large", N);
     plan.grid = (int)grid;
     const int64_t rows_cap = ((int64_t)N + grid - 1) / grid;
-    plan.smem = (size_t)plan.mt * Kpad * 2 + (size_t)plan.mt * (Kpad / 32) * ch * 4 +
-                (size_t)rows_cap * plan.S * plan.mt * 4;
+    const size_t rest = (size_t)plan.mt * Kpad * 2 + (size_t)plan.mt * (Kpad / 32) * ch * 4 +
+                        (size_t)rows_cap * plan.S * plan.mt * 4;
+    // Two row batches in flight per thread (measured: a deeper ring only delays
+    // the first batches, since 16 warps' cp.async traffic per SM is throttled).
+    plan.nb = 2;
+    plan.smem = rows_ring_bytes(nw, plan.nb, plan.rb) + rest;
     if (plan.smem > dev.smem_optin)
-        return fail(Q4_ERR_SHAPE, "K=%d too large for the register-prefetch kernel", K);
-    const void *k = rows_select(kind, plan.mt, plan.rb);
+        return fail(Q4_ERR_SHAPE, "K=%d too large for the whole-row kernels", K);
+    const void *k = rows_select(plan);
     if (!k)
-        return fail(Q4_ERR_ARG, "no register-prefetch kernel for kind %d", kind);
+        return fail(Q4_ERR_ARG, "no whole-row kernel for kind %d, S=%d", kind, plan.S);
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)plan.smem);
     if (e != cudaSuccess)
-        return cuda_fail(e, "cudaFuncSetAttribute(register-prefetch kernel)");
+        return cuda_fail(e, "cudaFuncSetAttribute(whole-row kernel)");
     return Q4_OK;
 }
 
 q4_status rows_launch(const RowsPlan &plan, GemvParams p, int M, cudaStream_t stream, bool pdl)
 {
-    const void *k = rows_select(plan.kind, plan.mt, plan.rb);
+    const void *k = rows_select(plan);
     p.S = plan.S;
     p.grid = plan.grid;
+    p.rows_q = p.N / plan.grid;
+    p.rows_r = p.N % plan.grid;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
@@ -322,7 +439,7 @@ q4_status rows_launch(const RowsPlan &plan, GemvParams p, int M, cudaStream_t st
         p.mcount = (M - m0) < plan.mt ? (M - m0) : plan.mt;
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3((unsigned)plan.grid);
-        cfg.blockDim = dim3(RK_THREADS);
+        cfg.blockDim = dim3(rows_warps(plan) * 32);
         cfg.dynamicSmemBytes = plan.smem;
         cfg.stream = stream;
         cfg.attrs = pdl ? attr : nullptr;
@@ -330,7 +447,7 @@ q4_status rows_launch(const RowsPlan &plan, GemvParams p, int M, cudaStream_t st
         void *args[] = {&p};
         cudaError_t e = cudaLaunchKernelExC(&cfg, k, args);
         if (e != cudaSuccess)
-            return cuda_fail(e, "launch of the register-prefetch kernel");
+            return cuda_fail(e, "launch of a whole-row kernel");
     }
     return Q4_OK;
 }

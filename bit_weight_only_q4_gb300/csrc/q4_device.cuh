@@ -31,6 +31,27 @@ __device__ __forceinline__ uint2 ld_stream_v2(const void *p)
     return r;
 }
 
+// 16-byte asynchronous global -> shared copy through L2 only (cp.async.cg).
+// src_bytes = 0 writes 16 zero bytes and reads nothing.  Completion is tracked
+// per thread by commit groups.
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src, uint32_t src_bytes)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;"
+                 :: "r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit()
+{
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+// Wait until at most N of this thread's most recent commit groups are pending.
+template <int N>
+__device__ __forceinline__ void cp_async_wait()
+{
+    asm volatile("cp.async.wait_group %0;" :: "n"(N) : "memory");
+}
+
 __device__ __forceinline__ uint32_t ld_nc_u16(const void *p)
 {
     unsigned short r;

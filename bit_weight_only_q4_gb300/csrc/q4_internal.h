@@ -33,6 +33,8 @@ struct GemvParams {
     int64_t TW;               // warps in the grid
     int64_t gran;             // warp ranges are multiples of gran units (1 or S)
     int row_begin, n_rows, extra_row;
+    // whole-row kernels: CTA b owns rows_q (+1 when b < rows_r) rows
+    int rows_q, rows_r;
     // bulk-copy path only
     int64_t T;                // stages = row blocks * S
     int grid;                 // CTAs
@@ -89,7 +91,7 @@ q4_status bulk_plan(const DeviceInfo &dev, int kind, int M, int N, int K, BulkPl
 q4_status bulk_launch(const BulkPlan &plan, GemvParams p, int M, cudaStream_t stream, bool pdl);
 // ---- register-prefetch weight-streaming kernel (gemv_rows.cu)
 struct RowsPlan {
-    int kind = 0, mt = 1, rb = 4, S = 1, grid = 0;
+    int kind = 0, mt = 1, rb = 4, nb = 2, S = 1, grid = 0;
     size_t smem = 0;
 };
 bool rows_eligible(int kind, int K);
