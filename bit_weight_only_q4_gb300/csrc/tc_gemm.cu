@@ -12,14 +12,16 @@
 //   * Warp 0 (one thread) streams, per chunk, the token tile of x (bf16, TMA
 //     tensor load with 128-byte swizzle) and the 128 rows x 32 bytes of packed
 //     codes (TMA tensor load) into a ring of shared-memory stages.
-//   * Sixteen worker warps in four groups dequantise the codes into the A
-//     operand tile (fp16, K-major, 128-byte swizzle; one weight row per thread)
-//     and convert the x tile in place from bf16 to fp16 (for large M a small
-//     kernel converts x once per call instead).  Chunk i goes to group i % 4, so
-//     four chunks are in flight and the per-chunk latency chain (wait, convert,
-//     decode, proxy fence, arrive) overlaps.  int4: w = fp16(c * s + m) (one fused multiply-add, single rounding);
-//     NVFP4: w = E2M1 * e4m3 in fp16, exact (the global scale is applied in the
-//     epilogue).  An x value outside the fp16 range sets Q4_DEVERR_FP16_RANGE.
+//   * Sixteen worker warps dequantise every chunk together into the A operand
+//     tile (fp16, K-major, 128-byte swizzle): thread t takes a quarter row (16
+//     weights) -- row t / 4, columns 16 (t % 4) .. + 15 of the chunk -- so one
+//     chunk's latency chain (wait, convert, decode, proxy fence, arrive) is
+//     short and the tensor core is fed chunk after chunk.  They also convert the
+//     chunk's x tile in place from bf16 to fp16 (for large M a small kernel
+//     converts x once per call instead).  int4: w = fp16(c * s + m) (one fused
+//     multiply-add, single rounding); NVFP4: w = E2M1 * e4m3 in fp16, exact (the
+//     global scale is applied in the epilogue).  An x value outside the fp16
+//     range sets Q4_DEVERR_FP16_RANGE.
 //   * Warp 1 allocates the TMEM accumulator (128 lanes x TN fp32 columns) and one
 //     thread issues tcgen05.mma (kind::f16, M=128, N=TN, K=16) four times per
 //     chunk, then tcgen05.commit frees the stage.
@@ -39,14 +41,16 @@ namespace q4 {
 
 constexpr int TC_ROWS = 128;           // weight rows per tile (MMA M)
 constexpr int TC_KC = 64;              // K columns per chunk (128 bytes of fp16)
-constexpr int TC_GROUPS = 4;           // worker groups: chunk i goes to group i % 4
+constexpr int TC_GROUPS = 4;           // epilogue: four warps share a TMEM lane quadrant
 constexpr int TC_WORKERS = 4 * TC_GROUPS;   // dequant / epilogue warps
 constexpr int TC_THREADS = (2 + TC_WORKERS) * 32;
 constexpr unsigned kErrFp16Range = 2u;
 
 // Per-CTA timestamps (globaltimer ns) for builds with -DQ4_TRACE: slots 0..7
 // start, TMEM ready, final commit seen by the epilogue, end; 8+i producer issued
-// chunk i, 24+i workers (warp 2) finished chunk i, 40+i MMA issued chunk i.
+// chunk i, 24+i workers (warp 2) finished chunk i, 40+i MMA issued chunk i;
+// 56..61 warp 2's clock cycles summed over its chunks: data waits, x conversion,
+// dequant, proxy fence, warp sync + arrive.
 #ifdef Q4_TRACE
 __device__ unsigned long long g_q4_tc_trace[1024 * 64];
 __device__ __forceinline__ unsigned long long tc_now()
@@ -56,12 +60,20 @@ __device__ __forceinline__ unsigned long long tc_now()
     return t;
 }
 #define TC_TRACE(slot) do { if ((slot) < 64 && blockIdx.x < 1024) g_q4_tc_trace[blockIdx.x * 64 + (slot)] = tc_now(); } while (0)
+#define TC_CLK(v) long long v = clock64()
+#define TC_PHASE(slot, a, b) (tc_ph[(slot) - 56] += (b) - (a))
+#define TC_PHASE_DECL long long tc_ph[5] = {0, 0, 0, 0, 0}
+#define TC_PHASE_STORE() do { if (warp == 2 && lane == 0 && blockIdx.x < 1024) for (int q_ = 0; q_ < 5; ++q_) g_q4_tc_trace[blockIdx.x * 64 + 56 + q_] = (unsigned long long)tc_ph[q_]; } while (0)
 extern "C" int q4_tc_trace_copy(unsigned long long *host, int n)
 {
     return (int)cudaMemcpyFromSymbol(host, g_q4_tc_trace, sizeof(unsigned long long) * n);
 }
 #else
 #define TC_TRACE(slot) ((void)0)
+#define TC_CLK(v) ((void)0)
+#define TC_PHASE(slot, a, b) ((void)0)
+#define TC_PHASE_DECL ((void)0)
+#define TC_PHASE_STORE() ((void)0)
 #endif
 
 struct TcParams {
@@ -78,13 +90,11 @@ struct TcParams {
     int tiles_m;               // ceil(M / TN)
     int KS;                    // split-K factor
     int chunks;                // K / 64
-    int ns;                    // ring stages (x and A tiles)
+    int ns;                    // ring stages (super-chunks)
     int tmem_cols;             // power of two >= max(32, TN)
     int x_f16;                 // x already converted to fp16 (large M)
 };
 
-constexpr int TC_CSTAGES = 2;          // code stages, 4 chunks (128 bytes per row) each
-constexpr int TC_SCALE_AHEAD = 8;      // chunks of group scales loaded ahead
 
 // ------------------------------------------------------------ PTX helpers
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int c0, int c1,
@@ -181,25 +191,33 @@ __device__ __forceinline__ uint32_t f16x2_splat(uint32_t h16)
 }
 
 // ------------------------------------------------------------------ kernel
-template <int LAYOUT>   // 0 int4-g128, 1 NVFP4
+// One ring stage holds SC consecutive 64-column chunks ("super-chunk"): the packed
+// codes of the tile's 128 rows (one TMA box, SC * 32 bytes per row), the SC x
+// sub-tiles (TN x 64, 128-byte swizzle) and the SC A sub-tiles (128 x 64 fp16,
+// 128-byte swizzle).  One barrier says the stage's copies landed, one that all
+// sixteen worker warps wrote its A tiles, one that the MMAs reading it finished.
+template <int SC>
+struct TcStage {
+    static constexpr uint32_t A = SC * 16384u;          // A sub-tiles
+    static constexpr uint32_t CODE = SC * 4096u;        // 128 rows x SC * 32 bytes
+};
+
+template <int LAYOUT, int SC>   // LAYOUT 0 int4-g128, 1 NVFP4
 __global__ void __launch_bounds__(TC_THREADS, 1)
 q4_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap wmap,
              TcParams p)
 {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
-    // 1024-byte aligned carve-up: [x stages][A stages][code stages][barriers]
     unsigned char *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const int TN = p.TN;
     const int NS = p.ns;
     const uint32_t x_bytes = (uint32_t)TN * 128;
     const uint32_t x_stride = (x_bytes + 1023) & ~1023u;
-    unsigned char *xbuf = smem;
-    unsigned char *abuf = xbuf + (size_t)NS * x_stride;                 // 16 KB per stage
-    unsigned char *cbuf = abuf + (size_t)NS * 16384;                   // 16 KB per code stage
-    uint64_t *bars = reinterpret_cast<uint64_t *>(cbuf + (size_t)TC_CSTAGES * 16384);
-    // bars: full[NS], afull[NS], empty[NS], done, cfull[C], cempty[C]
-    uint64_t *cbars = bars + 3 * NS + 1;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(cbars + 2 * TC_CSTAGES);
+    const uint32_t stage_bytes = TcStage<SC>::A + (uint32_t)SC * x_stride + TcStage<SC>::CODE;
+    // stage u: [A sub-tiles][x sub-tiles][codes]; barriers after the stages
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + (size_t)NS * stage_bytes);
+    // bars: full[NS], afull[NS], empty[NS], done
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 3 * NS + 1);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -210,22 +228,22 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
     const int ks = rem - tile_m * p.KS;
     const int n0 = tile_n * TC_ROWS;
     const int m0 = tile_m * TN;
-    const int c0 = (int)((int64_t)ks * p.chunks / p.KS);
-    const int c1 = (int)((int64_t)(ks + 1) * p.chunks / p.KS);
-    const int nch = c1 - c0;
+    // split-K on super-chunk boundaries
+    const int sup_total = (p.chunks + SC - 1) / SC;
+    const int u0 = (int)((int64_t)ks * sup_total / p.KS);
+    const int u1 = (int)((int64_t)(ks + 1) * sup_total / p.KS);
+    const int nsup = u1 - u0;
+    const int c0 = u0 * SC;
+    const int c1 = (u1 * SC) < p.chunks ? u1 * SC : p.chunks;
 
     if (threadIdx.x == 0) {
         TC_TRACE(0);
         for (int i = 0; i < NS; ++i) {
             mbar_init(smem_u32(&bars[i]), 1);                  // TMA arrive + bytes
-            mbar_init(smem_u32(&bars[NS + i]), 4);             // the chunk's worker group
+            mbar_init(smem_u32(&bars[NS + i]), TC_WORKERS);    // every worker warp
             mbar_init(smem_u32(&bars[2 * NS + i]), 1);         // MMA commit
         }
         mbar_init(smem_u32(&bars[3 * NS]), 1);                 // final commit
-        for (int i = 0; i < TC_CSTAGES; ++i) {
-            mbar_init(smem_u32(&cbars[i]), 1);                 // TMA arrive + bytes
-            mbar_init(smem_u32(&cbars[TC_CSTAGES + i]), TC_WORKERS);
-        }
         mbar_init_fence();
     }
     if (warp == 1) {
@@ -243,173 +261,209 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
         // ------------------------------------------------------------ producer
         pdl_launch_dependents();
         if (lane == 0) {
-            int issued = 0, cissued = 0;
-            for (int i = 0; i < nch; ++i) {
-                const int s = i % NS, use = i / NS;
+            int issued = 0;
+            for (int u = 0; u < nsup; ++u) {
+                const int s = u % NS, use = u / NS;
                 if (use > 0 && !mbar_wait(smem_u32(&bars[2 * NS + s]), (use - 1) & 1, p.err))
                     break;
-                if (i % 4 == 0) {
-                    // codes of chunks i .. i+3: 128 rows x 128 bytes in one copy
-                    const int j = i / 4, cs = j % TC_CSTAGES, cuse = j / TC_CSTAGES;
-                    if (cuse > 0 &&
-                        !mbar_wait(smem_u32(&cbars[TC_CSTAGES + cs]), (cuse - 1) & 1, p.err))
-                        break;
-                    const uint32_t cfull = smem_u32(&cbars[cs]);
-                    mbar_arrive_expect_tx(cfull, 16384);
-                    tma_load_2d(smem_u32(cbuf + (size_t)cs * 16384), &wmap, (c0 + i) * (TC_KC / 2),
-                                n0, cfull);
-                    cissued = j + 1;
-                }
-                if (i == 0)
-                    pdl_wait();                // x comes from the previous kernel
+                const int kc = c0 + u * SC;
+                const int nv = (c1 - kc) < SC ? (c1 - kc) : SC;
+                unsigned char *st = smem + (size_t)s * stage_bytes;
                 const uint32_t full = smem_u32(&bars[s]);
-                mbar_arrive_expect_tx(full, x_bytes);
-                tma_load_2d(smem_u32(xbuf + (size_t)s * x_stride), &xmap, (c0 + i) * TC_KC, m0, full);
-                TC_TRACE(8 + i);
-                issued = i + 1;
+                mbar_arrive_expect_tx(full, TcStage<SC>::CODE + (uint32_t)nv * x_bytes);
+                // codes of the super-chunk: 128 rows x SC * 32 bytes in one copy
+                tma_load_2d(smem_u32(st + TcStage<SC>::A + SC * x_stride), &wmap, kc * (TC_KC / 2),
+                            n0, full);
+                if (u == 0)
+                    pdl_wait();                // x comes from the previous kernel
+                for (int c = 0; c < nv; ++c)
+                    tma_load_2d(smem_u32(st + TcStage<SC>::A + c * x_stride), &xmap, (kc + c) * TC_KC,
+                                m0, full);
+                TC_TRACE(8 + u);
+                issued = u + 1;
             }
             // drain: every issued copy has landed before the CTA can exit
-            for (int i = issued - NS > 0 ? issued - NS : 0; i < issued; ++i)
-                mbar_wait(smem_u32(&bars[i % NS]), (i / NS) & 1, p.err);
-            for (int j = cissued - TC_CSTAGES > 0 ? cissued - TC_CSTAGES : 0; j < cissued; ++j)
-                mbar_wait(smem_u32(&cbars[j % TC_CSTAGES]), (j / TC_CSTAGES) & 1, p.err);
+            for (int u = issued - NS > 0 ? issued - NS : 0; u < issued; ++u)
+                mbar_wait(smem_u32(&bars[u % NS]), (u / NS) & 1, p.err);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------- MMA issue
         if (lane == 0) {
             const uint32_t idesc = idesc_f16(TN);
-            for (int i = 0; i < nch; ++i) {
-                const int s = i % NS, use = i / NS;
+            for (int u = 0; u < nsup; ++u) {
+                const int s = u % NS, use = u / NS;
                 if (!mbar_wait(smem_u32(&bars[NS + s]), use & 1, p.err))
                     break;
                 tc_fence_after();
-                const uint32_t a0 = smem_u32(abuf + (size_t)s * 16384);
-                const uint32_t b0 = smem_u32(xbuf + (size_t)s * x_stride);
+                const int kc = c0 + u * SC;
+                const int nv = (c1 - kc) < SC ? (c1 - kc) : SC;
+                const uint32_t st = smem_u32(smem + (size_t)s * stage_bytes);
+                for (int c = 0; c < nv; ++c) {
 #pragma unroll
-                for (int kk = 0; kk < TC_KC / 16; ++kk)
-                    mma_f16(tmem_base, smem_desc_sw128(a0 + kk * 32), smem_desc_sw128(b0 + kk * 32),
-                            idesc, (i > 0 || kk > 0) ? 1u : 0u);
+                    for (int kk = 0; kk < TC_KC / 16; ++kk)
+                        mma_f16(tmem_base, smem_desc_sw128(st + c * 16384 + kk * 32),
+                                smem_desc_sw128(st + TcStage<SC>::A + c * x_stride + kk * 32), idesc,
+                                (u > 0 || c > 0 || kk > 0) ? 1u : 0u);
+                }
                 mma_commit(smem_u32(&bars[2 * NS + s]));
-                TC_TRACE(40 + i);
+                TC_TRACE(40 + u);
             }
             mma_commit(smem_u32(&bars[3 * NS]));
         }
     } else {
         // ------------------------------------------------------------- workers
+        // Dequant mapping: a warp reads 256 contiguous code bytes per step (no
+        // bank conflicts): L = 4 SC lanes per code row, 32 / L rows per step, SC
+        // steps.  In step k a lane takes 16 weights: row 8 w + (32 / L) k + lane / L,
+        // chunk c = (lane % L) / 4, columns 16 (lane % 4) .. + 15 of that chunk.
+        constexpr int L = 4 * SC;
+        constexpr int RPS = 32 / L;
+        constexpr int SA = 4;                    // super-chunks of scales loaded ahead
         const int w = warp - 2;                  // 0..15
-        const int grp = w >> 2;                  // worker group: chunks i % 4 == grp
+        const int grp = w >> 2;                  // epilogue: column share of the quadrant
         const int quad = warp & 3;               // TMEM lane quadrant of this warp
-        const int r = quad * 32 + lane;          // weight row within the tile
-        const int n = n0 + r;
-        const bool nok = n < p.N;
-        const int gtid = (w & 3) * 32 + lane;    // 0..127 within the group
-        auto load_scale = [&](int kc) -> uint32_t {
-            if (!nok)
+        const int wt = w * 32 + lane;            // 0..511
+        const int cl = lane % L;
+        const int c = cl >> 2;
+        const int qd = cl & 3;
+        int rowk[SC];
+        bool rok[SC];
+#pragma unroll
+        for (int k = 0; k < SC; ++k) {
+            rowk[k] = 8 * w + RPS * k + lane / L;
+            rok[k] = n0 + rowk[k] < p.N;
+        }
+        auto load_scale = [&](int u, int k) -> uint32_t {
+            const int kc = c0 + u * SC + c;
+            if (!rok[k] || kc >= c1)
                 return 0u;
+            const int64_t n = n0 + rowk[k];
             if constexpr (LAYOUT == 0) {
-                const int64_t gi = (int64_t)n * (p.K / 128) + (kc * TC_KC) / 128;
+                const int64_t gi = n * (p.K / 128) + (kc * TC_KC) / 128;
                 return ld_nc_u16(static_cast<const uint16_t *>(p.scale) + gi) |
                        (ld_nc_u16(p.minv + gi) << 16);
             } else {
-                // the four e4m3 scales of the chunk's 64 codes
-                return *reinterpret_cast<const uint32_t *>(
-                    static_cast<const uint8_t *>(p.scale) + (int64_t)n * (p.K / 16) + kc * 4);
+                return ld_nc_u8(static_cast<const uint8_t *>(p.scale) + n * (p.K / 16) + kc * 4 + qd);
             }
         };
-        // group scales come from HBM: keep TC_SCALE_AHEAD of this group's chunks
-        // of them in flight
-        uint32_t scq[TC_SCALE_AHEAD];
+        uint32_t scq[SA][SC];
 #pragma unroll
-        for (int j = 0; j < TC_SCALE_AHEAD; ++j) {
-            const int ii = grp + j * TC_GROUPS;
-            scq[j] = ii < nch ? load_scale(c0 + ii) : 0u;
-        }
+        for (int j = 0; j < SA; ++j)
+#pragma unroll
+            for (int k = 0; k < SC; ++k)
+                scq[j][k] = j < nsup ? load_scale(j, k) : 0u;
         bool range_bad = false;
-        for (int i = grp; i < nch; i += TC_GROUPS) {
-            const int s = i % NS, use = i / NS;
-            const uint32_t sc = scq[0];
+        TC_PHASE_DECL;
+        for (int u = 0; u < nsup; ++u) {
+            const int s = u % NS, use = u / NS;
+            uint32_t sc[SC];
 #pragma unroll
-            for (int j = 0; j + 1 < TC_SCALE_AHEAD; ++j)
-                scq[j] = scq[j + 1];
-            const int inext = i + TC_SCALE_AHEAD * TC_GROUPS;
-            scq[TC_SCALE_AHEAD - 1] = inext < nch ? load_scale(c0 + inext) : 0u;
-            const int cs = (i / 4) % TC_CSTAGES, cuse = (i / 4) / TC_CSTAGES;
-            if (!mbar_wait(smem_u32(&cbars[cs]), cuse & 1, p.err))
-                break;
+            for (int k = 0; k < SC; ++k) {
+                sc[k] = scq[0][k];
+#pragma unroll
+                for (int j = 0; j + 1 < SA; ++j)
+                    scq[j][k] = scq[j + 1][k];
+                scq[SA - 1][k] = u + SA < nsup ? load_scale(u + SA, k) : 0u;
+            }
+            const int kc = c0 + u * SC;
+            const int nv = (c1 - kc) < SC ? (c1 - kc) : SC;
+            unsigned char *st = smem + (size_t)s * stage_bytes;
+            TC_CLK(t0);
             if (!mbar_wait(smem_u32(&bars[s]), use & 1, p.err))
                 break;
-            // x tile: bf16 -> fp16 in place (element-wise, swizzle-agnostic)
-            uint4 *xv = reinterpret_cast<uint4 *>(xbuf + (size_t)s * x_stride);
-            for (int v = p.x_f16 ? TN * 8 : gtid; v < TN * 8; v += 128) {
-                const uint4 t = xv[v];
-                const uint32_t e[4] = {t.x, t.y, t.z, t.w};
-                uint32_t o[4];
-                float mx = 0.f;
+            TC_CLK(t1);
+            TC_PHASE(56, t0, t1);
+            // x sub-tiles: bf16 -> fp16 in place (element-wise, swizzle-agnostic).
+            // Only tiles of at most 64 tokens are converted here (larger M arrive
+            // in fp16), so a thread has at most SC 16-byte vectors: the loop is
+            // unrolled and interleaves with the code loads below.
+            if (!p.x_f16) {
+                const int per = TN * 8;                  // vectors per sub-tile
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const float lo = bf16_bits_to_f32(e[j] & 0xffffu);
-                    const float hi = bf16_bits_to_f32(e[j] >> 16);
-                    mx = fmaxf(mx, fmaxf(fabsf(lo), fabsf(hi)));
-                    __half2 h = __floats2half2_rn(lo, hi);
-                    o[j] = *reinterpret_cast<uint32_t *>(&h);
-                }
-                if (mx >= 65520.f && mx <= 3.4e38f)
-                    range_bad = true;
-                xv[v] = make_uint4(o[0], o[1], o[2], o[3]);
-            }
-            // A row r: the chunk's 64 codes of row r -> eight 16-byte fp16 chunks
-            const uint4 *crow = reinterpret_cast<const uint4 *>(cbuf + (size_t)cs * 16384 + r * 128 +
-                                                                (i % 4) * 32);
-            const uint4 cw0 = crow[0], cw1 = crow[1];
-            const uint32_t words[8] = {cw0.x, cw0.y, cw0.z, cw0.w, cw1.x, cw1.y, cw1.z, cw1.w};
-            unsigned char *arow = abuf + (size_t)s * 16384 + (size_t)r * 128;
-            uint32_t sgs[4] = {0u, 0u, 0u, 0u};
-            if constexpr (LAYOUT == 1) {
-                const uint32_t s01 = e4m3x2_to_f16x2(sc & 0xffffu);
-                const uint32_t s23 = e4m3x2_to_f16x2(sc >> 16);
-                sgs[0] = f16x2_splat(s01 & 0xffffu);
-                sgs[1] = f16x2_splat(s01 >> 16);
-                sgs[2] = f16x2_splat(s23 & 0xffffu);
-                sgs[3] = f16x2_splat(s23 >> 16);
-            }
+                for (int j = 0; j < SC; ++j) {
+                    const int v = wt + j * TC_WORKERS * 32;
+                    if (v < nv * per) {
+                        const int sub = (v >= per) + (v >= 2 * per) + (v >= 3 * per);
+                        uint4 *xv = reinterpret_cast<uint4 *>(st + TcStage<SC>::A + sub * x_stride) +
+                                    (v - sub * per);
+                        const uint4 t = *xv;
+                        const uint32_t e[4] = {t.x, t.y, t.z, t.w};
+                        uint32_t o[4];
+                        float mx = 0.f;
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {               // 8 K columns per 16-byte chunk
-                uint32_t o[4];
-                if constexpr (LAYOUT == 0) {
-                    const uint32_t s2 = f16x2_splat(sc & 0xffffu);
-                    const uint32_t m2 = f16x2_splat(sc >> 16);
-#pragma unroll
-                    for (int b = 0; b < 4; ++b) {
-                        // byte b -> (1024 + c_lo, 1024 + 16 c_hi) -> (c_lo, c_hi)
-                        const uint32_t t = prmt(words[j], 0u, (uint32_t)(b | (4 << 4) | (b << 8) | (4 << 12)));
-                        uint32_t v2;
-                        asm("lop3.b32 %0, %1, 0x00F0000F, 0x64006400, 0xEA;" : "=r"(v2) : "r"(t));
-                        v2 = hfma2(v2, 0x2C003C00u, 0xD400E400u);   // * (1, 1/16) + (-1024, -64)
-                        o[b] = hfma2(v2, s2, m2);                   // c * s + min, one rounding
+                        for (int q = 0; q < 4; ++q) {
+                            const float lo = bf16_bits_to_f32(e[q] & 0xffffu);
+                            const float hi = bf16_bits_to_f32(e[q] >> 16);
+                            mx = fmaxf(mx, fmaxf(fabsf(lo), fabsf(hi)));
+                            __half2 h = __floats2half2_rn(lo, hi);
+                            o[q] = *reinterpret_cast<uint32_t *>(&h);
+                        }
+                        if (mx >= 65520.f && mx <= 3.4e38f)
+                            range_bad = true;
+                        *xv = make_uint4(o[0], o[1], o[2], o[3]);
                     }
-                } else {
-                    uint32_t h[4];
-                    e2m1x8_to_f16x2x4(words[j], h);
-#pragma unroll
-                    for (int b = 0; b < 4; ++b)
-                        o[b] = hmul2(h[b], sgs[j >> 1]);           // exact in fp16
                 }
-                *reinterpret_cast<uint4 *>(arow + ((j ^ (r & 7)) << 4)) =
-                    make_uint4(o[0], o[1], o[2], o[3]);
             }
+            TC_CLK(t2);
+            TC_PHASE(57, t1, t2);
+            const unsigned char *codes = st + TcStage<SC>::A + SC * x_stride;
+#pragma unroll
+            for (int k = 0; k < SC; ++k) {
+                const int rd = rowk[k];
+                const uint2 cw = *reinterpret_cast<const uint2 *>(codes + rd * (SC * 32) + cl * 8);
+                const uint32_t words[2] = {cw.x, cw.y};
+                unsigned char *arow = st + c * 16384 + rd * 128;
+                uint32_t sg = 0u;
+                if constexpr (LAYOUT == 1)
+                    sg = f16x2_splat(e4m3x2_to_f16x2(sc[k] & 0xffu) & 0xffffu);
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {           // 8 K columns per 16-byte chunk
+                    uint32_t o[4];
+                    if constexpr (LAYOUT == 0) {
+                        const uint32_t s2 = f16x2_splat(sc[k] & 0xffffu);
+                        const uint32_t m2 = f16x2_splat(sc[k] >> 16);
+#pragma unroll
+                        for (int b = 0; b < 4; ++b) {
+                            // byte b -> (1024 + c_lo, 1024 + 16 c_hi) -> (c_lo, c_hi)
+                            const uint32_t t = prmt(words[j], 0u, (uint32_t)(b | (4 << 4) | (b << 8) | (4 << 12)));
+                            uint32_t v2;
+                            asm("lop3.b32 %0, %1, 0x00F0000F, 0x64006400, 0xEA;" : "=r"(v2) : "r"(t));
+                            v2 = hfma2(v2, 0x2C003C00u, 0xD400E400u);   // * (1, 1/16) + (-1024, -64)
+                            o[b] = hfma2(v2, s2, m2);                   // c * s + min, one rounding
+                        }
+                    } else {
+                        uint32_t h[4];
+                        e2m1x8_to_f16x2x4(words[j], h);
+#pragma unroll
+                        for (int b = 0; b < 4; ++b)
+                            o[b] = hmul2(h[b], sg);                    // exact in fp16
+                    }
+                    const int seg = 2 * qd + j;
+                    *reinterpret_cast<uint4 *>(arow + ((seg ^ (rd & 7)) << 4)) =
+                        make_uint4(o[0], o[1], o[2], o[3]);
+                }
+            }
+            TC_CLK(t3);
+            TC_PHASE(58, t2, t3);
             fence_proxy_async();
+            TC_CLK(t4);
+            TC_PHASE(59, t3, t4);
             __syncwarp();
-            if (lane == 0) {
+            if (lane == 0)
                 mbar_arrive(smem_u32(&bars[NS + s]));
-                mbar_arrive(smem_u32(&cbars[TC_CSTAGES + cs]));
-            }
-            if (warp == 2 && lane == 0) TC_TRACE(24 + i);
+            TC_CLK(t5);
+            TC_PHASE(60, t4, t5);
+            if (warp == 2 && lane == 0) TC_TRACE(24 + u);
         }
+        TC_PHASE_STORE();
         if (range_bad && p.err)
             atomicOr(p.err, kErrFp16Range);
 
         // ------------------------------------------------------------ epilogue
-        const bool ok = nch > 0 && mbar_wait(smem_u32(&bars[3 * NS]), 0, p.err);
+        const int r = quad * 32 + lane;          // TMEM lane = weight row within the tile
+        const int n = n0 + r;
+        const bool nok = n < p.N;
+        const bool ok = nsup > 0 && mbar_wait(smem_u32(&bars[3 * NS]), 0, p.err);
         tc_fence_after();
         if (warp == 2 && lane == 0) TC_TRACE(2);
         float gsc = 1.f;
@@ -538,8 +592,8 @@ static int tc_tn(int M)
     return (M + 15) / 16 * 16 < 16 ? 16 : (M + 15) / 16 * 16;
 }
 
-// Split-K factor: enough CTAs to cover the SMs when the tile grid is small,
-// keeping at least four K chunks per CTA.
+// Split-K factor: as many CTAs as fit in one wave (one CTA per SM) when the tile
+// grid is small, keeping at least four K chunks per CTA.
 static int tc_ks(const DeviceInfo &dev, int M, int N, int K)
 {
     const int TN = tc_tn(M);
@@ -547,7 +601,7 @@ static int tc_ks(const DeviceInfo &dev, int M, int N, int K)
     const int chunks = K / TC_KC;
     if (tiles * 2 > dev.sms)
         return 1;
-    int ks = (int)((dev.sms + tiles - 1) / tiles);
+    int ks = (int)(dev.sms / tiles);
     if (ks > chunks / 4)
         ks = chunks / 4;
     if (ks > 16)
@@ -555,6 +609,8 @@ static int tc_ks(const DeviceInfo &dev, int M, int N, int K)
     return ks < 1 ? 1 : ks;
 }
 
+// x is converted inside the GEMM for tiles of up to 64 tokens (at most SC
+// vectors per thread), by a separate pass for more.
 static bool tc_preconvert(int M) { return M > 64; }
 
 static size_t tc_xf16_bytes(int M, int K)
@@ -648,19 +704,32 @@ q4_status tc_launch(int kind, const void *x, const uint8_t *codes, const void *s
         xsrc = wsb;
         p.x_f16 = 1;
     }
-    // ring depth: as many stages as fit beside the barriers
+    // Stage = SC chunks (A sub-tiles, x sub-tiles, codes).  The largest SC that
+    // still leaves four stages in flight (three, two) amortises each hand-off
+    // over more weights without starving the copies.
     const size_t x_stride = ((size_t)p.TN * 128 + 1023) / 1024 * 1024;
-    const size_t stage = x_stride + 16384;
-    // budget: alignment slack (1 KB) + static shared memory (1 KB) + code stages
-    // + barriers, the rest for x / A stages
-    int ns = (int)((dev.smem_optin - 2048 - 512 - TC_CSTAGES * 16384) / stage);
-    if (ns > 6)
-        ns = 6;
+    const size_t budget = dev.smem_optin - 1024 /* alignment */ - 1024 /* static */ - 256;
+    int sc = 1, ns = 0;
+    for (int need = 4; need >= 2 && ns == 0; --need)
+        for (int cand = 4; cand >= 1; cand /= 2) {
+            const size_t stage = (size_t)cand * (16384 + x_stride + 4096);
+            const int fit = (int)(budget / stage);
+            if (fit >= need) {
+                sc = cand;
+                ns = fit > 8 ? 8 : fit;
+                break;
+            }
+        }
+#ifdef Q4_TC_SC
+    sc = Q4_TC_SC;
+    ns = (int)(budget / ((size_t)sc * (16384 + x_stride + 4096)));
+    ns = ns > 8 ? 8 : ns;
+#endif
     if (ns < 2)
         return fail(Q4_ERR_SHAPE, "tensor-core tile does not fit in shared memory");
     p.ns = ns;
-    const size_t smem = 1024 + (size_t)ns * stage + TC_CSTAGES * 16384 +
-                        (3 * ns + 1 + 2 * TC_CSTAGES) * 8 + 16;
+    const size_t stage = (size_t)sc * (16384 + x_stride + 4096);
+    const size_t smem = 1024 + (size_t)ns * stage + (3 * ns + 1) * 8 + 16;
 
     CUtensorMap xmap, wmap;
     {
@@ -680,7 +749,7 @@ q4_status tc_launch(int kind, const void *x, const uint8_t *codes, const void *s
     {
         cuuint64_t dims[2] = {(cuuint64_t)K / 2, (cuuint64_t)N};
         cuuint64_t strides[1] = {(cuuint64_t)K / 2};
-        cuuint32_t box[2] = {2 * TC_KC, TC_ROWS};        // 4 chunks of codes
+        cuuint32_t box[2] = {(cuuint32_t)(sc * TC_KC / 2), TC_ROWS};   // SC chunks of codes
         cuuint32_t estr[2] = {1, 1};
         CUresult r = enc(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(codes),
                          dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -689,8 +758,15 @@ q4_status tc_launch(int kind, const void *x, const uint8_t *codes, const void *s
         if (r != CUDA_SUCCESS)
             return fail(Q4_ERR_CUDA, "cuTensorMapEncodeTiled(codes) failed (%d)", (int)r);
     }
-    const void *k = kind == W_INT4 ? reinterpret_cast<const void *>(&q4_tc_kernel<0>)
-                                   : reinterpret_cast<const void *>(&q4_tc_kernel<1>);
+    const void *k = nullptr;
+    if (kind == W_INT4)
+        k = sc == 4 ? reinterpret_cast<const void *>(&q4_tc_kernel<0, 4>)
+            : sc == 2 ? reinterpret_cast<const void *>(&q4_tc_kernel<0, 2>)
+                      : reinterpret_cast<const void *>(&q4_tc_kernel<0, 1>);
+    else
+        k = sc == 4 ? reinterpret_cast<const void *>(&q4_tc_kernel<1, 4>)
+            : sc == 2 ? reinterpret_cast<const void *>(&q4_tc_kernel<1, 2>)
+                      : reinterpret_cast<const void *>(&q4_tc_kernel<1, 1>);
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess)
         return cuda_fail(e, "cudaFuncSetAttribute(tensor-core kernel)");
