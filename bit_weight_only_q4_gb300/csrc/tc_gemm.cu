@@ -52,18 +52,18 @@ constexpr unsigned kErrFp16Range = 2u;
 // 56..61 warp 2's clock cycles summed over its chunks: data waits, x conversion,
 // dequant, proxy fence, warp sync + arrive.
 #ifdef Q4_TRACE
-__device__ unsigned long long g_q4_tc_trace[1024 * 64];
+__device__ unsigned long long g_q4_tc_trace[8 * 1024 * 64];   // 8 most recent calls
 __device__ __forceinline__ unsigned long long tc_now()
 {
     unsigned long long t;
     asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
     return t;
 }
-#define TC_TRACE(slot) do { if ((slot) < 64 && blockIdx.x < 1024) g_q4_tc_trace[blockIdx.x * 64 + (slot)] = tc_now(); } while (0)
+#define TC_TRACE(slot) do { if ((slot) < 64 && blockIdx.x < 1024) g_q4_tc_trace[((p.call & 7) * 1024 + blockIdx.x) * 64 + (slot)] = tc_now(); } while (0)
 #define TC_CLK(v) long long v = clock64()
 #define TC_PHASE(slot, a, b) (tc_ph[(slot) - 56] += (b) - (a))
 #define TC_PHASE_DECL long long tc_ph[5] = {0, 0, 0, 0, 0}
-#define TC_PHASE_STORE() do { if (warp == 2 && lane == 0 && blockIdx.x < 1024) for (int q_ = 0; q_ < 5; ++q_) g_q4_tc_trace[blockIdx.x * 64 + 56 + q_] = (unsigned long long)tc_ph[q_]; } while (0)
+#define TC_PHASE_STORE() do { if (warp == 2 && lane == 0 && blockIdx.x < 1024) for (int q_ = 0; q_ < 5; ++q_) g_q4_tc_trace[((p.call & 7) * 1024 + blockIdx.x) * 64 + 56 + q_] = (unsigned long long)tc_ph[q_]; } while (0)
 extern "C" int q4_tc_trace_copy(unsigned long long *host, int n)
 {
     return (int)cudaMemcpyFromSymbol(host, g_q4_tc_trace, sizeof(unsigned long long) * n);
@@ -93,6 +93,7 @@ struct TcParams {
     int ns;                    // ring stages (super-chunks)
     int tmem_cols;             // power of two >= max(32, TN)
     int x_f16;                 // x already converted to fp16 (large M)
+    int call;                  // launch index (phase-trace builds only)
 };
 
 
@@ -274,8 +275,11 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
                 // codes of the super-chunk: 128 rows x SC * 32 bytes in one copy
                 tma_load_2d(smem_u32(st + TcStage<SC>::A + SC * x_stride), &wmap, kc * (TC_KC / 2),
                             n0, full);
-                if (u == 0)
+                if (u == 0) {
+                    TC_TRACE(61);
                     pdl_wait();                // x comes from the previous kernel
+                    TC_TRACE(62);
+                }
                 for (int c = 0; c < nv; ++c)
                     tma_load_2d(smem_u32(st + TcStage<SC>::A + c * x_stride), &xmap, (kc + c) * TC_KC,
                                 m0, full);
@@ -310,6 +314,13 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
             }
             mma_commit(smem_u32(&bars[3 * NS]));
         }
+        // free the accumulator as soon as every worker has read it back
+        __syncwarp();
+        asm volatile("bar.sync 3, %0;" ::"r"((TC_WORKERS + 1) * 32) : "memory");
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;"
+                     ::"r"(tmem_base), "r"(p.tmem_cols) : "memory");
+        if (lane == 0) TC_TRACE(63);
     } else {
         // ------------------------------------------------------------- workers
         // Dequant mapping: a warp reads 256 contiguous code bytes per step (no
@@ -470,10 +481,18 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
         if constexpr (LAYOUT == 1)
             gsc = __ldg(p.gscale);
         const int tile = tile_n * p.tiles_m + tile_m;
-        for (int cb = grp * 16; cb < TN; cb += 16 * TC_GROUPS) {
+        const int ncb = (TN + 16 * TC_GROUPS - 1) / (16 * TC_GROUPS);   // same for every worker
+        for (int it = 0; it < ncb; ++it) {
+            const int cb = grp * 16 + it * 16 * TC_GROUPS;
             uint32_t v[16];
-            tmem_ld16(tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)cb, v);
-            if (!ok)
+            if (cb < TN)
+                tmem_ld16(tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)cb, v);
+            if (it == ncb - 1) {
+                // last TMEM read done: let warp 1 free the accumulator now
+                tc_fence_before();
+                asm volatile("bar.arrive 3, %0;" ::"r"((TC_WORKERS + 1) * 32) : "memory");
+            }
+            if (!ok || cb >= TN)
                 continue;
             if (p.KS == 1) {
 #pragma unroll
@@ -500,13 +519,38 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
             asm volatile("bar.sync 2, %0;" ::"r"(TC_WORKERS * 32) : "memory");
             if (last_flag) {
                 __threadfence();
-                for (int c = grp; c < TN; c += TC_GROUPS) {
+                // Each thread sums groups of four rows of one token column: all KS
+                // partials of a group are loaded (16 bytes each) before the adds,
+                // which run in k order, so the result does not depend on timing.
+                const size_t kstride4 = (size_t)TN * TC_ROWS / 4;
+                const float4 *part = reinterpret_cast<const float4 *>(
+                    p.ws + (size_t)tile * p.KS * TN * TC_ROWS);
+                for (int g4 = wt; g4 < TN * (TC_ROWS / 4); g4 += TC_WORKERS * 32) {
+                    const int c = g4 / (TC_ROWS / 4), q = g4 % (TC_ROWS / 4);
+                    float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
+                    for (int k0 = 0; k0 < p.KS; k0 += 8) {
+                        float4 v[8];
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            if (k0 + j < p.KS)
+                                v[j] = __ldcg(part + (k0 + j) * kstride4 + (size_t)c * (TC_ROWS / 4) + q);
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            if (k0 + j < p.KS) {
+                                sum.x += v[j].x; sum.y += v[j].y;
+                                sum.z += v[j].z; sum.w += v[j].w;
+                            }
+                    }
                     const int m = m0 + c;
-                    float sum = 0.f;
-                    for (int k2 = 0; k2 < p.KS; ++k2)
-                        sum += __ldcg(p.ws + ((size_t)(tile * p.KS + k2) * TN + c) * TC_ROWS + r);
-                    if (nok && m < p.M)
-                        p.y[(int64_t)m * p.N + n] = f32_to_bf16_bits(sum * gsc);
+                    const int nb = n0 + 4 * q;
+                    if (m < p.M) {
+                        uint16_t *yr = p.y + (int64_t)m * p.N;
+                        const float o[4] = {sum.x, sum.y, sum.z, sum.w};
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            if (nb + i < p.N)
+                                yr[nb + i] = f32_to_bf16_bits(o[i] * gsc);
+                    }
                 }
                 if (w == 0 && lane == 0)
                     p.tickets[tile] = 0u;
@@ -514,15 +558,8 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
         }
     }
 
-    tc_fence_before();
     __syncthreads();
     if (threadIdx.x == 0) TC_TRACE(3);
-    if (warp == 1) {
-        __syncwarp();
-        tc_fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;"
-                     ::"r"(tmem_base), "r"(p.tmem_cols) : "memory");
-    }
 }
 
 // x (bf16) -> fp16 once per call for large M, so that the GEMM's CTAs do not each
@@ -593,7 +630,9 @@ static int tc_tn(int M)
 }
 
 // Split-K factor: as many CTAs as fit in one wave (one CTA per SM) when the tile
-// grid is small, keeping at least four K chunks per CTA.
+// grid is small, keeping at least four K chunks per CTA and at most eight
+// partials per tile (the last CTA of a tile sums them; more would lengthen that
+// tail more than the extra CTAs shorten the main loop).
 static int tc_ks(const DeviceInfo &dev, int M, int N, int K)
 {
     const int TN = tc_tn(M);
@@ -604,8 +643,8 @@ static int tc_ks(const DeviceInfo &dev, int M, int N, int K)
     int ks = (int)(dev.sms / tiles);
     if (ks > chunks / 4)
         ks = chunks / 4;
-    if (ks > 16)
-        ks = 16;
+    if (ks > 8)
+        ks = 8;
     return ks < 1 ? 1 : ks;
 }
 
@@ -659,6 +698,10 @@ q4_status tc_launch(int kind, const void *x, const uint8_t *codes, const void *s
     p.M = M;
     p.N = N;
     p.K = K;
+#ifdef Q4_TRACE
+    static int trace_calls = 0;
+    p.call = trace_calls++;
+#endif
     p.TN = tc_tn(M);
     p.tiles_m = (M + p.TN - 1) / p.TN;
     p.KS = tc_ks(dev, M, N, K);
