@@ -247,33 +247,67 @@ def run_decode_step(args, device):
     """One decode step of the synthetic 28-layer int4 stack (hidden 2048, FFN
     8192): per layer q, k, v, gate, up read x; o reads v; down reads up; the
     next layer's x is down's output; then the restricted head (2049 rows).
-    196 + 1 calls per step, replayed from one CUDA graph; 1.007 GB of weights."""
+    Projections that share an input run as one call on their concatenated rows
+    (q|k|v: N = 6144; gate|up: N = 16384), 4 calls per layer + the head = 113
+    per step; --no-fuse runs the 7 separate calls per layer (197 per step).
+    Replayed from one CUDA graph; 1.007 GB of weights per step."""
     import torch
     from bit_weight_only_q4_gb300 import layout, q4, synth
     from tests import parity as P
     c = synth.DECODE_STACK_28
-    mats = []
+    H, F = c["hidden"], c["ffn"]
+    fuse = not getattr(args, "no_fuse", False)
+    layers = []
     for layer in range(c["layers"]):
-        mats.append({k: P.int4_dev(v) for k, v in synth.decode_stack_layer(layer).items()})
+        m = {k: P.int4_dev(v) for k, v in synth.decode_stack_layer(layer).items()}
+        if fuse:
+            cat = lambda names: tuple(torch.cat([m[n][i] for n in names], 0).contiguous()
+                                      for i in range(3))
+            layers.append({"qkv": cat(("q", "k", "v")), "o": m["o"],
+                           "gu": cat(("gate", "up")), "down": m["down"]})
+        else:
+            layers.append(m)
     head = P.bf16_dev(synth.decode_stack_head())
     x0 = P.bf16_dev(synth.decode_stack_input())
-    H, F = c["hidden"], c["ffn"]
-    buf = {n: torch.empty((1, F if n in ("gate", "up") else H), dtype=torch.bfloat16,
-                          device=device) for n in ("q", "k", "v", "o", "gate", "up", "down")}
     logits = torch.empty((1, c["head_rows"]), dtype=torch.bfloat16, device=device)
-    ws = q4.alloc_workspace(q4.LAYOUT_INT4G128, 1, F, F, device)
-    src = {"q": "x", "k": "x", "v": "x", "o": "v", "gate": "x", "up": "x", "down": "up"}
+    shapes = [(3 * H, H), (H, H), (2 * F, H), (H, F)] if fuse else \
+        [(N, K) for _, N, K in synth.DECODE_LAYER_PROJS]
+    ws_n = max(q4.workspace_bytes(q4.LAYOUT_INT4G128, 1, N, K) for N, K in shapes)
+    ws = torch.zeros(ws_n, dtype=torch.uint8, device=device) if ws_n else None
     wbytes = sum(layout.weight_bytes("int4", N, K) for _, N, K in synth.DECODE_LAYER_PROJS) \
         * c["layers"] + 2 * c["head_rows"] * H
+    if fuse:
+        y_qkv = torch.empty((1, 3 * H), dtype=torch.bfloat16, device=device)
+        y_o = torch.empty((1, H), dtype=torch.bfloat16, device=device)
+        y_gu = torch.empty((1, 2 * F), dtype=torch.bfloat16, device=device)
+        y_down = torch.empty((1, H), dtype=torch.bfloat16, device=device)
+        v_view = y_qkv[:, 2 * H:]            # v's rows of the fused output
+        up_view = y_gu[:, F:]                # up's rows
 
-    def step(_):
-        x = x0
-        for layer in range(c["layers"]):
-            for name, N, K in synth.DECODE_LAYER_PROJS:
-                inp = x if src[name] == "x" else buf[src[name]]
-                q4.q4_linear_int4g128(inp, *mats[layer][name], y=buf[name], workspace=ws)
-            x = buf["down"]
-        q4.audio_head_logits_restricted(x, head, 0, c["head_rows"], -1, logits=logits)
+        def step(_):
+            x = x0
+            for L in layers:
+                q4.q4_linear_int4g128(x, *L["qkv"], y=y_qkv, workspace=ws)
+                q4.q4_linear_int4g128(v_view, *L["o"], y=y_o, workspace=ws)
+                q4.q4_linear_int4g128(x, *L["gu"], y=y_gu, workspace=ws)
+                q4.q4_linear_int4g128(up_view, *L["down"], y=y_down, workspace=ws)
+                x = y_down
+            q4.audio_head_logits_restricted(x, head, 0, c["head_rows"], -1, logits=logits)
+        launches = 4 * c["layers"] + 1
+    else:
+        buf = {n: torch.empty((1, F if n in ("gate", "up") else H), dtype=torch.bfloat16,
+                              device=device) for n in ("q", "k", "v", "o", "gate", "up", "down")}
+        src = {"q": "x", "k": "x", "v": "x", "o": "v", "gate": "x", "up": "x", "down": "up"}
+
+        def step(_):
+            x = x0
+            for L in layers:
+                for name, N, K in synth.DECODE_LAYER_PROJS:
+                    inp = x if src[name] == "x" else buf[src[name]]
+                    q4.q4_linear_int4g128(inp, *L[name], y=buf[name], workspace=ws)
+                x = buf["down"]
+            q4.audio_head_logits_restricted(x, head, 0, c["head_rows"], -1, logits=logits)
+        launches = len(synth.DECODE_LAYER_PROJS) * c["layers"] + 1
 
     stream = torch.cuda.Stream(device)
     ms = _graph_time(torch, stream, step, 1, args.steps)
@@ -281,8 +315,8 @@ def run_decode_step(args, device):
     gbs = wbytes / (ms * 1e-3) / 1e9
     return {"workload": c["name"], "ms_per_step": round(ms, 4), "weight_bytes": wbytes,
             "value": round(gbs, 1), "unit": "GB/s", "hbm_frac": round(gbs / peak, 4),
-            "steps_per_s": round(1e3 / ms, 1), "launches_per_step": 197,
-            "pdl": not args.no_pdl}
+            "steps_per_s": round(1e3 / ms, 1), "launches_per_step": launches,
+            "fused_projections": fuse, "pdl": not args.no_pdl}
 
 
 def run_batched(args, device):
@@ -615,6 +649,8 @@ def main(argv=None):
                     help="nvfp4_gemv is the bench line; the others print their own "
                          "measurement lines")
     ap.add_argument("--no-pdl", action="store_true")
+    ap.add_argument("--no-fuse", action="store_true",
+                    help="decode_step: run q, k, v and gate, up as separate calls")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--profile", action="store_true",

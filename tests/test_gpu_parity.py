@@ -210,6 +210,42 @@ def test_decode_stack_layers_per_call_parity(q4, oracle_mod):
         x = outs["down"]
 
 
+def test_decode_stack_fused_projections(q4, oracle_mod):
+    """Projections sharing an input as one call on concatenated rows (q|k|v,
+    gate|up), as the decode-step bench runs them; o and down read their inputs
+    as slices of the fused outputs.  Each call is checked against the oracle on
+    the concatenated matrix and the GPU's own bf16 input."""
+    import numpy as np
+    x = synth.decode_stack_input()
+    for layer in (0, 27):
+        mats = synth.decode_stack_layer(layer)
+        cat = lambda names: synth.Int4Matrix(
+            np.concatenate([mats[n].qweight for n in names]),
+            np.concatenate([mats[n].scale for n in names]),
+            np.concatenate([mats[n].minv for n in names]))
+        qkv, gu = cat(("q", "k", "v")), cat(("gate", "up"))
+        xd = P.bf16_dev(x)
+        y_qkv = q4.q4_linear_int4g128(xd, *P.int4_dev(qkv))
+        yo, ao = oracle_mod.linear_int4g128(x, qkv.qweight, qkv.scale, qkv.minv, with_abs=True)
+        P.check(y_qkv, yo, ao, f"layer {layer} qkv")
+        v = y_qkv[:, 4096:]
+        y_o = q4.q4_linear_int4g128(v, *P.int4_dev(mats["o"]))
+        w = mats["o"]
+        yo, ao = oracle_mod.linear_int4g128(P.bf16_bits_host(v), w.qweight, w.scale, w.minv,
+                                             with_abs=True)
+        P.check(y_o, yo, ao, f"layer {layer} o from the v slice")
+        y_gu = q4.q4_linear_int4g128(xd, *P.int4_dev(gu))
+        yo, ao = oracle_mod.linear_int4g128(x, gu.qweight, gu.scale, gu.minv, with_abs=True)
+        P.check(y_gu, yo, ao, f"layer {layer} gate|up")
+        up = y_gu[:, 8192:]
+        y_d = q4.q4_linear_int4g128(up, *P.int4_dev(mats["down"]))
+        w = mats["down"]
+        yo, ao = oracle_mod.linear_int4g128(P.bf16_bits_host(up), w.qweight, w.scale, w.minv,
+                                             with_abs=True)
+        P.check(y_d, yo, ao, f"layer {layer} down from the up slice")
+        x = P.bf16_bits_host(y_d)
+
+
 # ------------------------------------------------------ batched decode config
 @pytest.mark.parametrize("shape_index", [0, 1])
 @pytest.mark.parametrize("M", [1, 3, 8, 16, 32, 48])
