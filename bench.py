@@ -387,6 +387,33 @@ def run_prefill(args, device):
     return res
 
 
+def run_quantize(args, device):
+    """Round-to-nearest quantisers from bf16 (packing, not the decode path): a
+    16384 x 2048 and an 8192 x 8192 matrix (weights N(0, 0.02)) into both layouts.
+    Bytes counted: the bf16 read once plus the packed write (NVFP4 reads the
+    matrix a second time for its global amax; that read is not counted)."""
+    import torch
+    from bit_weight_only_q4_gb300 import layout, q4, synth
+    peak, _ = _peaks()
+    res = {"workload": "round-to-nearest quantisers, bf16 -> int4-g128 / NVFP4",
+           "runs": []}
+    for (N, K) in ((16384, 2048), (8192, 8192)):
+        g = torch.Generator(device="cpu").manual_seed(N + K)
+        w = (torch.randn((N, K), generator=g) * 0.02).to(torch.bfloat16).to(device)
+        for lay in ("int4", "nvfp4"):
+            if lay == "int4":
+                fn = lambda i, w=w: q4.q4_quantize_int4g128(w)
+            else:
+                fn = lambda i, w=w: q4.q4_quantize_nvfp4(w)
+            stream = torch.cuda.Stream(device)
+            ms = _graph_time(torch, stream, fn, 5, max(3, args.steps // 5)) / 5
+            nbytes = 2 * N * K + layout.weight_bytes(lay, N, K)
+            gbs = nbytes / (ms * 1e-3) / 1e9
+            res["runs"].append({"layout": lay, "N": N, "K": K, "us": round(ms * 1e3, 2),
+                                "GBps": round(gbs, 1), "hbm_frac": round(gbs / peak, 4)})
+    return res
+
+
 def _bf16_peak():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -404,7 +431,8 @@ def run_extra(args, local):
     libbuild.build()
     q4.load()
     q4.set_launch_flags(q4.FLAG_PDL if not args.no_pdl else 0)
-    fn = {"decode_step": run_decode_step, "batched": run_batched, "prefill": run_prefill}
+    fn = {"decode_step": run_decode_step, "batched": run_batched, "prefill": run_prefill,
+          "quantize": run_quantize}
     r = fn[args.workload](args, device)
     r["metric"] = METRIC
     r["data"] = "synthetic (seeded PCG64)"
@@ -644,7 +672,7 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=200000)
     ap.add_argument("--warmup", type=int, default=2000)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--workload", choices=("nvfp4_gemv", "int4_gemv", "decode_step", "batched",
+    ap.add_argument("--workload", choices=("nvfp4_gemv", "int4_gemv", "decode_step", "batched", "quantize",
                                            "prefill"), default="nvfp4_gemv",
                     help="nvfp4_gemv is the bench line; the others print their own "
                          "measurement lines")
@@ -671,7 +699,7 @@ def main(argv=None):
             run_reference(args, world, rank)
         elif args.profile:
             run_profile(args, local)
-        elif args.workload in ("decode_step", "batched", "prefill"):
+        elif args.workload in ("decode_step", "batched", "prefill", "quantize"):
             run_extra(args, local)
         else:
             run_gpu(args, world, rank, local)

@@ -375,4 +375,39 @@ q4_status q4_dequant_nvfp4_f32(const uint8_t *codes, const uint8_t *scale_e4m3,
                                 static_cast<cudaStream_t>(stream));
 }
 
+q4_status q4_quantize_int4g128(const void *w, uint8_t *qweight, void *scale, void *minv, int N,
+                               int K, void *stream)
+{
+    if (!w || !qweight || !scale || !minv)
+        return fail(Q4_ERR_NULL, "NULL argument");
+    if (N < 1 || K < 128 || K % 128)
+        return fail(Q4_ERR_SHAPE, "int4-g128 quantiser needs N >= 1, K %% 128 == 0");
+    if (!aligned(w, 8) || !aligned(qweight, 2) || !aligned(scale, 2) || !aligned(minv, 2))
+        return fail(Q4_ERR_ALIGN, "w must be 8-byte, qweight/scale/min 2-byte aligned");
+    DeviceInfo dev;
+    q4_status s = current_device(dev);
+    if (s != Q4_OK)
+        return s;
+    return launch_quantize_int4(static_cast<const uint16_t *>(w), qweight,
+                                static_cast<uint16_t *>(scale), static_cast<uint16_t *>(minv),
+                                N, K, static_cast<cudaStream_t>(stream));
+}
+
+q4_status q4_quantize_nvfp4(const void *w, uint8_t *codes, uint8_t *scale_e4m3,
+                            float *global_scale, int N, int K, void *stream)
+{
+    if (!w || !codes || !scale_e4m3 || !global_scale)
+        return fail(Q4_ERR_NULL, "NULL argument");
+    if (N < 1 || K < 16 || K % 16)
+        return fail(Q4_ERR_SHAPE, "NVFP4 quantiser needs N >= 1, K %% 16 == 0");
+    if (!aligned(w, 16) || !aligned(codes, 8) || !aligned(global_scale, 4))
+        return fail(Q4_ERR_ALIGN, "w must be 16-byte, codes 8-byte, global scale 4-byte aligned");
+    DeviceInfo dev;
+    q4_status s = current_device(dev);
+    if (s != Q4_OK)
+        return s;
+    return launch_quantize_nvfp4(static_cast<const uint16_t *>(w), codes, scale_e4m3,
+                                 global_scale, N, K, static_cast<cudaStream_t>(stream));
+}
+
 }  // extern "C"

@@ -114,4 +114,10 @@ q4_status launch_dequant_int4(const uint8_t *q, const uint16_t *s, const uint16_
 q4_status launch_dequant_nvfp4(const uint8_t *q, const uint8_t *s, const float *g,
                                float *w, int N, int K, cudaStream_t st);
 
+// ---- round-to-nearest quantisers (quantize.cu)
+q4_status launch_quantize_int4(const uint16_t *w, uint8_t *q, uint16_t *s, uint16_t *m, int N,
+                               int K, cudaStream_t st);
+q4_status launch_quantize_nvfp4(const uint16_t *w, uint8_t *q, uint8_t *s, float *gscale, int N,
+                                int K, cudaStream_t st);
+
 }  // namespace q4

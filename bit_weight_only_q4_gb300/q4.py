@@ -69,6 +69,8 @@ def load() -> ctypes.CDLL:
             "q4_device_error_flags": ([ctypes.POINTER(ctypes.c_uint), i], st),
             "q4_dequant_int4g128_f32": ([p, p, p, p, i, i, p], st),
             "q4_dequant_nvfp4_f32": ([p, p, p, p, i, i, p], st),
+            "q4_quantize_int4g128": ([p, p, p, p, i, i, p], st),
+            "q4_quantize_nvfp4": ([p, p, p, p, i, i, p], st),
         }
         for name, (args, res) in sig.items():
             fn = getattr(L, name)
@@ -83,7 +85,8 @@ def symbols() -> list[str]:
     return ["q4_abi_version", "q4_status_string", "q4_last_error_string",
             "q4_set_launch_flags", "q4_get_launch_flags", "q4_workspace_bytes",
             "q4_linear_int4g128", "q4_linear_nvfp4", "audio_head_logits_restricted",
-            "q4_linear_int4g128_noalloc", "q4_device_error_flags", "q4_dequant_int4g128_f32", "q4_dequant_nvfp4_f32"]
+            "q4_linear_int4g128_noalloc", "q4_device_error_flags", "q4_dequant_int4g128_f32",
+            "q4_dequant_nvfp4_f32", "q4_quantize_int4g128", "q4_quantize_nvfp4"]
 
 
 def _check(status: int) -> None:
@@ -237,3 +240,28 @@ linear_int4g128 = q4_linear_int4g128
 linear_nvfp4 = q4_linear_nvfp4
 dequant_int4g128_f32 = q4_dequant_int4g128_f32
 dequant_nvfp4_f32 = q4_dequant_nvfp4_f32
+
+
+def q4_quantize_int4g128(w, stream=None):
+    """(qweight uint8 [N, K/2], scale fp16 [N, K/128], min fp16 [N, K/128]) of the
+    round-to-nearest min/max int4-g128 quantisation of bf16 weights w [N, K]."""
+    _cuda(w, "w", torch.bfloat16)
+    N, K = w.shape
+    q = torch.empty((N, K // 2), dtype=torch.uint8, device=w.device)
+    s = torch.empty((N, K // 128), dtype=torch.float16, device=w.device)
+    m = torch.empty((N, K // 128), dtype=torch.float16, device=w.device)
+    _check(load().q4_quantize_int4g128(_ptr(w), _ptr(q), _ptr(s), _ptr(m), N, K,
+                                       _stream(stream)))
+    return q, s, m
+
+
+def q4_quantize_nvfp4(w, stream=None):
+    """(codes uint8 [N, K/2], e4m3 scales uint8 [N, K/16], global scale fp32 [1]) of
+    the round-to-nearest NVFP4 quantisation of bf16 weights w [N, K]."""
+    _cuda(w, "w", torch.bfloat16)
+    N, K = w.shape
+    q = torch.empty((N, K // 2), dtype=torch.uint8, device=w.device)
+    s = torch.empty((N, K // 16), dtype=torch.uint8, device=w.device)
+    g = torch.empty((1,), dtype=torch.float32, device=w.device)
+    _check(load().q4_quantize_nvfp4(_ptr(w), _ptr(q), _ptr(s), _ptr(g), N, K, _stream(stream)))
+    return q, s, g

@@ -185,6 +185,38 @@ q4_status q4_dequant_nvfp4_f32(const uint8_t *codes, const uint8_t *scale_e4m3,
                                const float *global_scale, float *w, int N, int K,
                                void *stream);
 
+/*
+ * Round-to-nearest quantisers: BF16 weights w [N, K] (row-major, device memory)
+ * into the two layouts, for packing a checkpoint (not for the decode path).
+ * Every arithmetic step is one IEEE fp32 operation rounded to nearest even.
+ *
+ * q4_quantize_int4g128 ("rumik-oss-1-int4", "Format (rumik-int4-g128-minmax-v1)";
+ * the min/max form the layout's name refers to): per row and group of 128
+ * columns, lo = min w, hi = max w; scale = fp16((hi - lo) / 15); min = fp16(lo);
+ * code = clamp(rint((w - min) / scale), 0, 15) (0 when the fp16 scale is 0).
+ * Outputs qweight [N, K/2] (low nibble = even column), scale and min fp16
+ * [N, K/128].  K % 128 == 0; w 8-byte, the outputs 2-byte aligned.  Values whose
+ * magnitude exceeds the fp16 range give an infinite scale or min.
+ *
+ * q4_quantize_nvfp4 ("VoxCPM2 NVFP4 (GPTQ)", "NVFP4 settings": E2M1 codes, group
+ * 16, e4m3 group scales, one global scale; the pages' checkpoint used GPTQ, whose
+ * error feedback is not reproduced -- this is plain rounding in the same format):
+ * G = amax(w) / (6 * 448) (1 for an all-zero matrix); per group of 16 columns
+ * s = e4m3((amax_group / 6) / G), nearest even, saturating at 448;
+ * code = E2M1(w / (e4m3(s) * G)), nearest even, saturating at 6, magnitude 0
+ * stored as +0.  Outputs codes [N, K/2] (low nibble = even column), e4m3 scales
+ * [N, K/16] and the fp32 global scale (one float in device memory, overwritten;
+ * decoding multiplies by it).  K % 16 == 0; w 16-byte, codes 8-byte, the global
+ * scale 4-byte aligned.  Runs three kernels and a 4-byte memset on `stream`.
+ *
+ * The pages have no counterpart to these entry points' signatures; the layouts
+ * they write are the pages'.
+ */
+q4_status q4_quantize_int4g128(const void *w_bf16, uint8_t *qweight, void *scale_f16,
+                               void *min_f16, int N, int K, void *stream);
+q4_status q4_quantize_nvfp4(const void *w_bf16, uint8_t *codes, uint8_t *scale_e4m3,
+                            float *global_scale, int N, int K, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

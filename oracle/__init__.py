@@ -14,6 +14,10 @@ Sources, cited by page title and section:
   * "Rumik TTS Fast Inference", "What Made It Faster" / Figure 3: the head
     restricted to the current codebook's 2,049 rows.
 
+The quantisers (round-to-nearest, min/max for int4, amax-based for NVFP4) and the
+fp16 / e4m3 / E2M1 encoders they use are written out from the formats'
+definitions in ``oracle.c``.
+
 Parity is pinned for every function here by the ``-m "not gpu"`` tests in
 ``tests/test_oracle_pins.py`` (tables, special cases, brute force, invariants).
 """
@@ -67,8 +71,14 @@ def _load():
     lib.q4o_linear_nvfp4.argtypes = [p, p, p, f32, i64, i64, i64, p, p]
     lib.q4o_head_restricted.argtypes = [p, p, i64, i64, i64, i64, i64, p, p]
     lib.q4o_num_threads.restype = ctypes.c_int
+    for name in ("q4o_f32_to_fp16_array", "q4o_f32_to_e4m3_array", "q4o_f32_to_e2m1_array"):
+        getattr(lib, name).argtypes = [p, p, i64]
+    lib.q4o_quantize_int4g128.argtypes = [p, i64, i64, p, p, p]
+    lib.q4o_quantize_nvfp4.argtypes = [p, i64, i64, p, p, p]
     for name in ("q4o_dequant_int4g128", "q4o_dequant_nvfp4", "q4o_linear_int4g128",
-                 "q4o_linear_nvfp4", "q4o_head_restricted"):
+                 "q4o_linear_nvfp4", "q4o_head_restricted", "q4o_f32_to_fp16_array",
+                 "q4o_f32_to_e4m3_array", "q4o_f32_to_e2m1_array", "q4o_quantize_int4g128",
+                 "q4o_quantize_nvfp4"):
         getattr(lib, name).restype = None
     _lib = lib
     return lib
@@ -189,3 +199,54 @@ def head_restricted(h_bf16_bits, head_bf16_bits, row_begin: int, n_rows: int,
     _load().q4o_head_restricted(_ptr(h), _ptr(H_), row_begin, n_rows, extra_row, M, Hd,
                                 _ptr(out), _ptr(a) if with_abs else None)
     return (out, a) if with_abs else out
+
+
+# ------------------------------------------------------------------ encoders
+def _encode(fn: str, x, out_dtype) -> np.ndarray:
+    a = np.ascontiguousarray(np.asarray(x, dtype=np.float32))
+    out = np.empty(a.shape, out_dtype)
+    getattr(_load(), fn)(_ptr(a), _ptr(out), a.size)
+    return out
+
+
+def f32_to_fp16_bits(x) -> np.ndarray:
+    """IEEE binary16 bits, round to nearest even, overflow to infinity."""
+    return _encode("q4o_f32_to_fp16_array", x, np.uint16)
+
+
+def f32_to_e4m3_bits(x) -> np.ndarray:
+    """float8_e4m3fn bits, round to nearest even, saturating at +-448."""
+    return _encode("q4o_f32_to_e4m3_array", x, np.uint8)
+
+
+def f32_to_e2m1_codes(x) -> np.ndarray:
+    """E2M1 nibbles (bit 3 sign), nearest with ties to even, saturating at +-6,
+    magnitude 0 stored as +0."""
+    return _encode("q4o_f32_to_e2m1_array", x, np.uint8)
+
+
+# ------------------------------------------------------------------ quantise
+def quantize_int4g128(w_bf16_bits):
+    """(qweight [N,K/2] u8, scale fp16 bits [N,K/128], min fp16 bits [N,K/128])."""
+    w = _c(w_bf16_bits, np.uint16)
+    N, K = w.shape
+    if K % 128:
+        raise ValueError("int4g128 quantiser: K % 128 != 0")
+    q = np.zeros((N, K // 2), np.uint8)
+    s = np.empty((N, K // 128), np.uint16)
+    m = np.empty((N, K // 128), np.uint16)
+    _load().q4o_quantize_int4g128(_ptr(w), N, K, _ptr(q), _ptr(s), _ptr(m))
+    return q, s, m
+
+
+def quantize_nvfp4(w_bf16_bits):
+    """(codes [N,K/2] u8, e4m3 scales [N,K/16] u8, fp32 global scale)."""
+    w = _c(w_bf16_bits, np.uint16)
+    N, K = w.shape
+    if K % 16:
+        raise ValueError("nvfp4 quantiser: K % 16 != 0")
+    q = np.zeros((N, K // 2), np.uint8)
+    s = np.empty((N, K // 16), np.uint8)
+    g = np.zeros(1, np.float32)
+    _load().q4o_quantize_nvfp4(_ptr(w), N, K, _ptr(q), _ptr(s), _ptr(g))
+    return q, s, np.float32(g[0])

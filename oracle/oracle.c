@@ -36,6 +36,19 @@
  *     infinities, S.1111.111 is NaN (same spec, FP8 E4M3).
  *   - The linear layer accumulates x[m,k] * w[n,k] in fp64 and returns fp64,
  *     unrounded.
+ *   - Quantisers (round-to-nearest, from BF16 weights; the pages' own checkpoints
+ *     were made with min/max rounding [INT4] and with GPTQ [NVFP4] -- GPTQ's
+ *     error feedback is out of scope, the format is the same):
+ *       int4-g128: per group of 128 columns lo = min, hi = max;
+ *         scale = fp16((hi - lo) / 15), min = fp16(lo), code = clamp(rint((w -
+ *         min) / scale), 0, 15), code 0 when the fp16 scale is 0.
+ *       NVFP4: G = amax(W) / (6 * 448) (1 when amax is 0), per group of 16
+ *         columns s = e4m3((amax_g / 6) / G) (round to nearest even, saturating
+ *         at 448), S = e4m3(s) * G, code = E2M1(w / S) (nearest, ties to even,
+ *         saturating at 6; a code of magnitude 0 is stored as +0).
+ *       Every step is one IEEE fp32 operation rounded to nearest even; the
+ *       conversions to fp16, e4m3 and E2M1 are written out below from the
+ *       formats' definitions.
  *
  * Build: plain C99 with OpenMP over output rows, -ffp-contract=off so that no
  * multiply-add is fused behind the reader's back.
@@ -104,6 +117,98 @@ double q4o_e2m1_value(uint8_t nibble)
     else
         v = ldexp((double)(2 + f), e - 2);         /* (1 + f/2) * 2^(e-1) */
     return sign ? -v : v;
+}
+
+/* ------------------------------------------------------------- encoders */
+
+/* Round-to-nearest-even of a finite double that is an exact multiple of the
+ * target spacing times an integer plus a fraction: rint() under the default
+ * rounding mode. */
+static double rne(double v) { return nearbyint(v); }
+
+/* fp32 -> IEEE binary16, round to nearest even, overflow to infinity. */
+uint16_t q4o_f32_to_fp16(float x)
+{
+    if (isnan(x))
+        return 0x7e00;
+    uint16_t sign = signbit(x) ? 0x8000 : 0;
+    double a = fabs((double)x);
+    if (a >= 65520.0)                               /* half-way above 65504 and beyond */
+        return sign | 0x7c00;
+    if (a < ldexp(1.0, -14)) {                      /* subnormal: multiples of 2^-24 */
+        double m = rne(a * ldexp(1.0, 24));         /* 0 .. 1024 (1024 = smallest normal) */
+        return sign | (uint16_t)m;
+    }
+    int e;
+    frexp(a, &e);                                   /* a = f * 2^e, f in [0.5, 1) */
+    e -= 1;                                         /* 2^e <= a < 2^(e+1) */
+    double m = rne(a * ldexp(1.0, 10 - e));         /* 1024 .. 2048 */
+    if (m == 2048.0) {
+        m = 1024.0;
+        e += 1;
+    }
+    if (e + 15 >= 31)
+        return sign | 0x7c00;
+    return sign | (uint16_t)(((e + 15) << 10) | ((int)m - 1024));
+}
+
+/* fp32 -> float8_e4m3fn, round to nearest even, saturating at +-448; NaN -> 0x7f. */
+uint8_t q4o_f32_to_e4m3(float x)
+{
+    if (isnan(x))
+        return 0x7f;
+    uint8_t sign = signbit(x) ? 0x80 : 0;
+    double a = fabs((double)x);
+    if (a < ldexp(1.0, -6)) {                       /* subnormal: multiples of 2^-9 */
+        double m = rne(a * ldexp(1.0, 9));          /* 0 .. 8 (8 = smallest normal) */
+        return sign | (uint8_t)m;
+    }
+    if (a >= 448.0)
+        return sign | 0x7e;
+    int e;
+    frexp(a, &e);
+    e -= 1;
+    double m = rne(a * ldexp(1.0, 3 - e));          /* 8 .. 16 */
+    if (m == 16.0) {
+        m = 8.0;
+        e += 1;
+    }
+    /* a < 448 = 1.75 * 2^8, so e <= 8 and, for e == 8, m <= 14 */
+    return sign | (uint8_t)(((e + 7) << 3) | ((int)m - 8));
+}
+
+/* fp32 -> E2M1 nibble (bit 3 sign), nearest with ties to even, saturating at
+ * +-6; a result of magnitude 0 is returned as +0 (code 0). */
+uint8_t q4o_f32_to_e2m1(float x)
+{
+    double a = fabs((double)x);
+    uint8_t mag;
+    if (a < 1.0) {                                  /* subnormal: multiples of 0.5 */
+        mag = (uint8_t)rne(a * 2.0);                /* 0, 1, 2 (2 = 1.0) */
+    } else if (a >= 6.0) {
+        mag = 7;
+    } else {
+        int e;
+        frexp(a, &e);
+        e -= 1;                                     /* 0 .. 2 */
+        double m = rne(a * ldexp(1.0, 1 - e));      /* 2 .. 4 */
+        if (m == 4.0) {
+            m = 2.0;
+            e += 1;
+        }
+        mag = (e > 2) ? 7 : (uint8_t)(((e + 1) << 1) | ((int)m - 2));
+    }
+    if (mag == 0)
+        return 0;
+    return (signbit(x) ? 8 : 0) | mag;
+}
+
+static float bf16_to_f32(uint16_t b)
+{
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
 }
 
 /* The 4-bit code of column k in a row of packed bytes: the low nibble holds the
@@ -228,6 +333,103 @@ void q4o_head_restricted(const uint16_t *h_bf16, const uint16_t *head_bf16,
             logits[m * cols + j] = acc;
             if (abslog)
                 abslog[m * cols + j] = aacc;
+        }
+    }
+}
+
+/* Array forms of the three encoders (for the tests). */
+void q4o_f32_to_fp16_array(const float *x, uint16_t *out, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i) out[i] = q4o_f32_to_fp16(x[i]);
+}
+void q4o_f32_to_e4m3_array(const float *x, uint8_t *out, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i) out[i] = q4o_f32_to_e4m3(x[i]);
+}
+void q4o_f32_to_e2m1_array(const float *x, uint8_t *out, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i) out[i] = q4o_f32_to_e2m1(x[i]);
+}
+
+/* -------------------------------------------------------------- quantise */
+
+/* int4-g128 min/max round-to-nearest quantiser [INT4]: w_bf16 [N, K] ->
+ * qweight [N, K/2] (low nibble = even column), scale and min fp16 [N, K/128]. */
+void q4o_quantize_int4g128(const uint16_t *w_bf16, int64_t N, int64_t K, uint8_t *qweight,
+                           uint16_t *scale, uint16_t *minv)
+{
+    const int64_t groups = K / 128;
+#pragma omp parallel for schedule(static)
+    for (int64_t n = 0; n < N; ++n) {
+        for (int64_t g = 0; g < groups; ++g) {
+            const uint16_t *w = w_bf16 + n * K + g * 128;
+            float lo = bf16_to_f32(w[0]), hi = lo;
+            for (int k = 1; k < 128; ++k) {
+                float v = bf16_to_f32(w[k]);
+                if (v < lo) lo = v;
+                if (v > hi) hi = v;
+            }
+            float range = hi - lo;                  /* one fp32 rounding */
+            uint16_t s16 = q4o_f32_to_fp16(range / 15.0f);
+            uint16_t m16 = q4o_f32_to_fp16(lo);
+            scale[n * groups + g] = s16;
+            minv[n * groups + g] = m16;
+            float s = (float)q4o_fp16_value(s16);
+            float m = (float)q4o_fp16_value(m16);
+            uint8_t *row = qweight + n * (K / 2) + g * 64;
+            for (int k = 0; k < 128; ++k) {
+                int c = 0;
+                if (s > 0.0f) {
+                    float d = bf16_to_f32(w[k]) - m;  /* fp32 */
+                    float q = d / s;                  /* fp32 */
+                    double r = rne((double)q);
+                    c = r < 0.0 ? 0 : (r > 15.0 ? 15 : (int)r);
+                }
+                if (k % 2 == 0)
+                    row[k / 2] = (uint8_t)c;
+                else
+                    row[k / 2] |= (uint8_t)(c << 4);
+            }
+        }
+    }
+}
+
+/* NVFP4 round-to-nearest quantiser [NVFP4]: w_bf16 [N, K] -> E2M1 codes [N, K/2]
+ * (low nibble = even column), e4m3 group scales [N, K/16], fp32 global scale. */
+void q4o_quantize_nvfp4(const uint16_t *w_bf16, int64_t N, int64_t K, uint8_t *codes,
+                        uint8_t *scale_e4m3, float *global_scale)
+{
+    float amax = 0.0f;
+    for (int64_t i = 0; i < N * K; ++i) {
+        float a = fabsf(bf16_to_f32(w_bf16[i]));
+        if (a > amax) amax = a;
+    }
+    const float G = amax > 0.0f ? amax / 2688.0f : 1.0f;   /* 2688 = 6 * 448 */
+    *global_scale = G;
+    const int64_t groups = K / 16;
+#pragma omp parallel for schedule(static)
+    for (int64_t n = 0; n < N; ++n) {
+        for (int64_t g = 0; g < groups; ++g) {
+            const uint16_t *w = w_bf16 + n * K + g * 16;
+            float ag = 0.0f;
+            for (int k = 0; k < 16; ++k) {
+                float a = fabsf(bf16_to_f32(w[k]));
+                if (a > ag) ag = a;
+            }
+            float t = ag / 6.0f;
+            uint8_t s8 = q4o_f32_to_e4m3(t / G);
+            scale_e4m3[n * groups + g] = s8;
+            float S = (float)q4o_e4m3_value(s8) * G;          /* fp32 product */
+            uint8_t *row = codes + n * (K / 2) + g * 8;
+            for (int k = 0; k < 16; ++k) {
+                uint8_t c = 0;
+                if (S > 0.0f)
+                    c = q4o_f32_to_e2m1(bf16_to_f32(w[k]) / S);
+                if (k % 2 == 0)
+                    row[k / 2] = c;
+                else
+                    row[k / 2] |= (uint8_t)(c << 4);
+            }
         }
     }
 }

@@ -1,0 +1,209 @@
+"""Pins of the oracle's encoders (fp32 -> fp16 / e4m3 / E2M1) and round-to-nearest
+quantisers against what does not depend on the oracle: numpy's and torch's
+conversions, brute-force nearest levels, exact round trips on inputs built from
+known codes, and error bounds that follow from the formats.
+
+Quantiser definitions (pages "rumik-oss-1-int4", "Format"; "VoxCPM2 NVFP4 (GPTQ)",
+"NVFP4 settings"; the rounding rules are this repository's reading):
+  int4-g128: scale = fp16((max - min) / 15), min = fp16(min), code = nearest.
+  NVFP4: G = amax / 2688, group scale = e4m3(amax_g / 6 / G), code = nearest E2M1.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+E2M1_MAG = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+
+
+def _bf16_bits(a: np.ndarray) -> np.ndarray:
+    t = torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16).copy()
+
+
+def _bf16_values(bits: np.ndarray) -> np.ndarray:
+    return (bits.astype(np.uint32) << 16).view(np.float32)
+
+
+# ------------------------------------------------------------------ encoders
+def test_fp16_encoder_matches_numpy(oracle_mod):
+    rng = np.random.default_rng(11)
+    x = np.concatenate([
+        rng.standard_normal(20000).astype(np.float32) * np.float32(10.0) ** rng.integers(-9, 5, 20000),
+        np.array([65504, 65519.99, 65520, 1e6, 6e-8, 3e-8, 2.98e-8, 0.0, -0.0, 6.1e-5], np.float32),
+    ]).astype(np.float32)
+    # exact midpoints between neighbouring fp16 values (ties go to the even one)
+    h = rng.integers(0, 0x7bff, 5000).astype(np.uint16)
+    lo = h.view(np.float16).astype(np.float64)
+    hi = (h + 1).view(np.float16).astype(np.float64)
+    mid = ((lo + hi) / 2).astype(np.float32)
+    x = np.concatenate([x, mid[np.isfinite(mid)]])
+    got = oracle_mod.f32_to_fp16_bits(x)
+    want = x.astype(np.float16).view(np.uint16)
+    np.testing.assert_array_equal(got, want)
+
+
+def test_e4m3_encoder_matches_torch_and_saturates(oracle_mod):
+    rng = np.random.default_rng(12)
+    x = (rng.standard_normal(20000) * 2.0 ** rng.integers(-12, 9, 20000)).astype(np.float32)
+    codes = np.arange(0, 0x7e, dtype=np.uint8)         # finite positive e4m3 values
+    vals = torch.from_numpy(codes).view(torch.float8_e4m3fn).float().numpy().astype(np.float64)
+    mids = ((vals[:-1] + vals[1:]) / 2).astype(np.float32)
+    x = np.concatenate([x, mids, -mids])
+    x = x[np.abs(x) < 464.0]                            # torch's cast does not saturate
+    got = oracle_mod.f32_to_e4m3_bits(x)
+    want = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    np.testing.assert_array_equal(got, want)
+    big = np.array([464.0, 500.0, 1e30, np.inf, -480.0], np.float32)
+    np.testing.assert_array_equal(oracle_mod.f32_to_e4m3_bits(big),
+                                  np.array([0x7e, 0x7e, 0x7e, 0x7e, 0xfe], np.uint8))
+
+
+def _nearest_e2m1(v: float) -> int:
+    """Brute force: the nearest of the 16 E2M1 values, ties to the even fraction
+    bit, saturating; magnitude 0 as +0."""
+    a = min(abs(v), 6.0)
+    d = np.abs(E2M1_MAG - a)
+    best = np.flatnonzero(d == d.min())
+    mag = int(best[0]) if len(best) == 1 else int([b for b in best if b % 2 == 0][0])
+    if mag == 0:
+        return 0
+    return (8 if v < 0 else 0) | mag
+
+
+def test_e2m1_encoder_is_nearest_level(oracle_mod):
+    rng = np.random.default_rng(13)
+    x = np.concatenate([rng.uniform(-8, 8, 4000),
+                        (E2M1_MAG[:-1] + E2M1_MAG[1:]) / 2,       # ties
+                        -(E2M1_MAG[:-1] + E2M1_MAG[1:]) / 2,
+                        E2M1_MAG, -E2M1_MAG, [7.0, -100.0, 1e-9, -1e-9]]).astype(np.float32)
+    got = oracle_mod.f32_to_e2m1_codes(x)
+    want = np.array([_nearest_e2m1(float(v)) for v in x], np.uint8)
+    np.testing.assert_array_equal(got, want)
+
+
+# ------------------------------------------------------------ int4 quantiser
+def test_int4_quantiser_round_trip_on_representable_groups(oracle_mod):
+    rng = np.random.default_rng(14)
+    N, K = 6, 512
+    codes = rng.integers(0, 16, (N, K))
+    codes[:, ::128] = 0                                 # every group spans 0 .. 15
+    codes[:, 1::128] = 15
+    e = rng.integers(-9, -3, (N, K // 128))             # scale = 2^e, min = -j * scale
+    j = rng.integers(0, 16, (N, K // 128))
+    s = np.ldexp(1.0, e)
+    m = -j * s
+    w = codes * np.repeat(s, 128, 1) + np.repeat(m, 128, 1)
+    q, sb, mb = oracle_mod.quantize_int4g128(_bf16_bits(w))
+    np.testing.assert_array_equal(sb.view(np.float16).astype(np.float64), s)
+    np.testing.assert_array_equal(mb.view(np.float16).astype(np.float64), m)
+    lo, hi = q & 0x0f, q >> 4
+    got = np.empty((N, K), int)
+    got[:, 0::2], got[:, 1::2] = lo, hi
+    np.testing.assert_array_equal(got, codes)
+
+
+def test_int4_quantiser_codes_are_nearest_and_params_within_half_ulp(oracle_mod):
+    rng = np.random.default_rng(15)
+    wb = _bf16_bits(rng.standard_normal((8, 1024)) * 0.05)
+    w = _bf16_values(wb).astype(np.float64)
+    q, sb, mb = oracle_mod.quantize_int4g128(wb)
+    s = np.repeat(sb.view(np.float16).astype(np.float64), 128, 1)
+    m = np.repeat(mb.view(np.float16).astype(np.float64), 128, 1)
+    codes = np.empty(w.shape, int)
+    codes[:, 0::2], codes[:, 1::2] = q & 0x0f, q >> 4
+    levels = np.arange(16)[None, None, :] * s[..., None] + m[..., None]
+    d = np.abs(w[..., None] - levels)
+    best = d.min(-1)
+    chosen = np.take_along_axis(d, codes[..., None], -1)[..., 0]
+    # the chosen level is the nearest (up to fp32 rounding of (w - min) / scale)
+    assert np.all(chosen <= best + 1e-6 * s)
+    # scale and min are the fp16 values nearest to (hi - lo)/15 and lo
+    g = w.reshape(8, 8, 128)
+    lo, hi = g.min(-1), g.max(-1)
+    s16 = sb.view(np.float16).astype(np.float64)
+    m16 = mb.view(np.float16).astype(np.float64)
+    ulp = lambda v: np.spacing(np.abs(v).astype(np.float16)).astype(np.float64)
+    assert np.all(np.abs(s16 - (hi - lo) / 15) <= ulp(s16) / 2 * (1 + 1e-6) + 1e-12)
+    assert np.all(np.abs(m16 - lo) <= ulp(m16) / 2 * (1 + 1e-6))
+
+
+def test_int4_quantiser_error_matches_uniform_rounding_model(oracle_mod):
+    """On N(0,1) weights the step is range/15 with E[range of 128 normals] ~ 5.2,
+    so the RMS error is ~ E[range]/15/sqrt(12) ~ 0.10 of the weights' RMS."""
+    from scipy import integrate, stats
+    n = 128
+    er, _ = integrate.quad(lambda x: 1 - stats.norm.cdf(x) ** n - stats.norm.sf(x) ** n,
+                           -12, 12, limit=200)
+    predicted = er / 15 / math.sqrt(12)
+    rng = np.random.default_rng(16)
+    wb = _bf16_bits(rng.standard_normal((256, 4096)))
+    w = _bf16_values(wb).astype(np.float64)
+    q, sb, mb = oracle_mod.quantize_int4g128(wb)
+    dq = oracle_mod.dequant_int4g128(q, sb, mb).astype(np.float64)
+    rel = np.linalg.norm(dq - w) / np.linalg.norm(w)
+    assert 0.095 < predicted < 0.105
+    assert abs(rel - predicted) < 0.06 * predicted
+
+
+def test_int4_quantiser_degenerate_groups(oracle_mod):
+    w = np.zeros((2, 256), np.float32)
+    w[1, :128] = 0.5                                    # constant group
+    q, sb, mb = oracle_mod.quantize_int4g128(_bf16_bits(w))
+    assert np.all(q == 0)
+    assert np.all(sb == 0)
+    np.testing.assert_array_equal(mb.view(np.float16).astype(np.float32), [[0, 0], [0.5, 0]])
+
+
+# ----------------------------------------------------------- NVFP4 quantiser
+def test_nvfp4_quantiser_round_trip_on_representable_groups(oracle_mod):
+    rng = np.random.default_rng(17)
+    N, K = 5, 256
+    G0 = 2.0 ** -8
+    e4m3_vals = torch.arange(0x08, 0x7f, dtype=torch.uint8).view(torch.float8_e4m3fn).float().numpy()
+    s_g = rng.choice(e4m3_vals, (N, K // 16)).astype(np.float64)
+    s_g[0, 0] = 448.0                                   # fixes amax = 6 * 448 * G0
+    mags = rng.integers(1, 8, (N, K))
+    signs = rng.integers(0, 2, (N, K))
+    mags[:, ::16] = 7                                   # every group reaches +-6
+    codes = (signs << 3) | mags
+    val = np.where(signs == 1, -1.0, 1.0) * E2M1_MAG[mags]
+    w = val * np.repeat(s_g, 16, 1) * G0
+    q, sb, g = oracle_mod.quantize_nvfp4(_bf16_bits(w))
+    assert g == np.float32(G0)
+    np.testing.assert_array_equal(
+        torch.from_numpy(sb).view(torch.float8_e4m3fn).float().numpy(), s_g.astype(np.float32))
+    got = np.empty((N, K), int)
+    got[:, 0::2], got[:, 1::2] = q & 0x0f, q >> 4
+    np.testing.assert_array_equal(got, codes)
+
+
+def test_nvfp4_quantiser_codes_are_nearest_and_bounded(oracle_mod):
+    rng = np.random.default_rng(18)
+    wb = _bf16_bits(rng.standard_normal((6, 512)) * 0.02)
+    w = _bf16_values(wb).astype(np.float64)
+    q, sb, g = oracle_mod.quantize_nvfp4(wb)
+    amax = np.abs(w).max()
+    assert abs(float(g) - amax / 2688) <= 2 ** -23 * amax / 2688
+    S = np.repeat(torch.from_numpy(sb).view(torch.float8_e4m3fn).float().numpy().astype(np.float64),
+                  16, 1) * float(g)
+    codes = np.empty(w.shape, int)
+    codes[:, 0::2], codes[:, 1::2] = q & 0x0f, q >> 4
+    assert not np.any(codes == 8)                      # -0 is stored as +0
+    val = np.where(codes & 8, -1.0, 1.0) * E2M1_MAG[codes & 7]
+    r = w / S
+    allv = np.concatenate([E2M1_MAG, -E2M1_MAG[1:]])
+    best = np.abs(r[..., None] - allv).min(-1)
+    assert np.all(np.abs(r - val) <= best + 1e-6)
+    # a group's largest weight divided by its scale is within e4m3 rounding of 6
+    ag = np.abs(w).reshape(6, 32, 16).max(-1)
+    ratio = ag / (S[:, ::16])
+    assert np.all((ratio > 6 / 1.07) & (ratio < 6 * 1.07))
+
+
+def test_nvfp4_quantiser_zero_matrix(oracle_mod):
+    q, sb, g = oracle_mod.quantize_nvfp4(np.zeros((3, 32), np.uint16))
+    assert np.all(q == 0) and np.all(sb == 0) and g == np.float32(1.0)
