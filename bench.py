@@ -387,6 +387,31 @@ def run_prefill(args, device):
     return res
 
 
+def run_embedding(args, device):
+    """int8 token-embedding gather + dequant ([277404, 2048] table, the full
+    vocabulary of the pages' model) for M = 1 and M = 48 tokens per call, chained
+    in a CUDA graph with PDL.  Bytes per call: M rows of 2048 int8 codes and one
+    fp16 scale read, M x 2048 bf16 written."""
+    import torch
+    from bit_weight_only_q4_gb300 import q4
+    V, H = 277404, 2048
+    g = torch.Generator(device="cpu").manual_seed(7)
+    q = torch.randint(-128, 128, (V, H), generator=g, dtype=torch.int8).to(device)
+    sc = (torch.rand(V, generator=g) * 0.02 + 1e-4).to(torch.float16).to(device)
+    peak, _ = _peaks()
+    res = {"workload": "int8 embedding gather, V=277404, H=2048", "runs": []}
+    for M in (1, 48):
+        ids = torch.randint(0, V, (M,), generator=g, dtype=torch.int32).to(device)
+        out = torch.empty((M, H), dtype=torch.bfloat16, device=device)
+        fn = lambda i, ids=ids, out=out: q4.q4_embedding_int8(ids, q, sc, out=out)
+        stream = torch.cuda.Stream(device)
+        ms = _graph_time(torch, stream, fn, 50, max(3, args.steps // 50)) / 50
+        nbytes = M * (H + 2 + 2 * H + 4)
+        res["runs"].append({"M": M, "us_per_call": round(ms * 1e3, 3),
+                            "GBps": round(nbytes / (ms * 1e-3) / 1e9, 1)})
+    return res
+
+
 def run_quantize(args, device):
     """Round-to-nearest quantisers from bf16 (packing, not the decode path): a
     16384 x 2048 and an 8192 x 8192 matrix (weights N(0, 0.02)) into both layouts.
@@ -432,7 +457,7 @@ def run_extra(args, local):
     q4.load()
     q4.set_launch_flags(q4.FLAG_PDL if not args.no_pdl else 0)
     fn = {"decode_step": run_decode_step, "batched": run_batched, "prefill": run_prefill,
-          "quantize": run_quantize}
+          "quantize": run_quantize, "embedding": run_embedding}
     r = fn[args.workload](args, device)
     r["metric"] = METRIC
     r["data"] = "synthetic (seeded PCG64)"
@@ -672,7 +697,7 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=200000)
     ap.add_argument("--warmup", type=int, default=2000)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--workload", choices=("nvfp4_gemv", "int4_gemv", "decode_step", "batched", "quantize",
+    ap.add_argument("--workload", choices=("nvfp4_gemv", "int4_gemv", "decode_step", "batched", "quantize", "embedding",
                                            "prefill"), default="nvfp4_gemv",
                     help="nvfp4_gemv is the bench line; the others print their own "
                          "measurement lines")
@@ -699,7 +724,7 @@ def main(argv=None):
             run_reference(args, world, rank)
         elif args.profile:
             run_profile(args, local)
-        elif args.workload in ("decode_step", "batched", "prefill", "quantize"):
+        elif args.workload in ("decode_step", "batched", "prefill", "quantize", "embedding"):
             run_extra(args, local)
         else:
             run_gpu(args, world, rank, local)

@@ -375,6 +375,25 @@ q4_status q4_dequant_nvfp4_f32(const uint8_t *codes, const uint8_t *scale_e4m3,
                                 static_cast<cudaStream_t>(stream));
 }
 
+q4_status q4_embedding_int8(const int32_t *ids, const int8_t *qweight, const void *scale,
+                            void *out, int M, int V, int H, void *stream)
+{
+    if (!ids || !qweight || !scale || !out)
+        return fail(Q4_ERR_NULL, "NULL argument");
+    if (M < 1 || V < 1 || H < 16 || H % 16)
+        return fail(Q4_ERR_SHAPE, "embedding gather needs M, V >= 1 and H %% 16 == 0 (H=%d)", H);
+    if (!aligned(qweight, 16) || !aligned(out, 16) || !aligned(ids, 4) || !aligned(scale, 2))
+        return fail(Q4_ERR_ALIGN, "qweight and out must be 16-byte, ids 4-byte, scale 2-byte aligned");
+    DeviceInfo dev;
+    q4_status s = current_device(dev);
+    if (s != Q4_OK)
+        return s;
+    const bool pdl = (g_flags.load() & Q4_FLAG_PDL) != 0;
+    return launch_embedding_int8(ids, qweight, static_cast<const uint16_t *>(scale),
+                                 static_cast<uint16_t *>(out), M, V, H,
+                                 static_cast<cudaStream_t>(stream), pdl);
+}
+
 q4_status q4_quantize_int4g128(const void *w, uint8_t *qweight, void *scale, void *minv, int N,
                                int K, void *stream)
 {

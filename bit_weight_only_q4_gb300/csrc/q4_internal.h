@@ -114,6 +114,10 @@ q4_status launch_dequant_int4(const uint8_t *q, const uint16_t *s, const uint16_
 q4_status launch_dequant_nvfp4(const uint8_t *q, const uint8_t *s, const float *g,
                                float *w, int N, int K, cudaStream_t st);
 
+// ---- int8 token-embedding gather (embedding.cu)
+q4_status launch_embedding_int8(const int32_t *ids, const int8_t *q, const uint16_t *sc,
+                                uint16_t *out, int M, int V, int H, cudaStream_t st, bool pdl);
+
 // ---- round-to-nearest quantisers (quantize.cu)
 q4_status launch_quantize_int4(const uint16_t *w, uint8_t *q, uint16_t *s, uint16_t *m, int N,
                                int K, cudaStream_t st);

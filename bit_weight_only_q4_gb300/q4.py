@@ -70,6 +70,7 @@ def load() -> ctypes.CDLL:
             "q4_dequant_int4g128_f32": ([p, p, p, p, i, i, p], st),
             "q4_dequant_nvfp4_f32": ([p, p, p, p, i, i, p], st),
             "q4_quantize_int4g128": ([p, p, p, p, i, i, p], st),
+            "q4_embedding_int8": ([p, p, p, p, i, i, i, p], st),
             "q4_quantize_nvfp4": ([p, p, p, p, i, i, p], st),
         }
         for name, (args, res) in sig.items():
@@ -86,7 +87,8 @@ def symbols() -> list[str]:
             "q4_set_launch_flags", "q4_get_launch_flags", "q4_workspace_bytes",
             "q4_linear_int4g128", "q4_linear_nvfp4", "audio_head_logits_restricted",
             "q4_linear_int4g128_noalloc", "q4_device_error_flags", "q4_dequant_int4g128_f32",
-            "q4_dequant_nvfp4_f32", "q4_quantize_int4g128", "q4_quantize_nvfp4"]
+            "q4_dequant_nvfp4_f32", "q4_quantize_int4g128", "q4_quantize_nvfp4",
+            "q4_embedding_int8"]
 
 
 def _check(status: int) -> None:
@@ -265,3 +267,17 @@ def q4_quantize_nvfp4(w, stream=None):
     g = torch.empty((1,), dtype=torch.float32, device=w.device)
     _check(load().q4_quantize_nvfp4(_ptr(w), _ptr(q), _ptr(s), _ptr(g), N, K, _stream(stream)))
     return q, s, g
+
+
+def q4_embedding_int8(ids, qweight, scale, out=None, stream=None):
+    """bf16 [M, H] rows of the int8 token embedding for int32 ids [M]."""
+    _cuda(ids, "ids", torch.int32)
+    _cuda(qweight, "qweight", torch.int8)
+    _cuda(scale, "scale", torch.float16)
+    V, H = qweight.shape
+    M = ids.numel()
+    if out is None:
+        out = torch.empty((M, H), dtype=torch.bfloat16, device=qweight.device)
+    _check(load().q4_embedding_int8(_ptr(ids), _ptr(qweight), _ptr(scale), _ptr(out), M, V, H,
+                                    _stream(stream)))
+    return out

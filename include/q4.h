@@ -172,6 +172,9 @@ q4_status audio_head_logits_restricted(const void *h, const void *head, int R_to
  * that output is not valid.  Activations inside the range are converted exactly
  * (down to 2^-17; smaller values are rounded to fp16 subnormals). */
 #define Q4_DEVERR_FP16_RANGE 0x2u
+/* Bit 2: q4_embedding_int8 met a token id outside 0 .. V-1 and wrote a row of
+ * zeros for it. */
+#define Q4_DEVERR_INDEX 0x4u
 q4_status q4_device_error_flags(unsigned *flags, int clear);
 
 /*
@@ -184,6 +187,21 @@ q4_status q4_dequant_int4g128_f32(const uint8_t *qweight, const void *scale,
 q4_status q4_dequant_nvfp4_f32(const uint8_t *codes, const uint8_t *scale_e4m3,
                                const float *global_scale, float *w, int N, int K,
                                void *stream);
+
+/*
+ * Token-embedding gather with int8 dequantisation ("rumik-oss-1-int4", "Format":
+ * embed_tokens.qweight int8 [V, H], scale fp16 [V]): for each of the M token ids
+ * (int32, device memory, typically written by the sampler of the previous step),
+ * out[m, k] = bf16(q[ids[m], k] * scale[ids[m]]).  The codes are read as signed
+ * two's complement with one symmetric scale per row (the page gives the shapes
+ * only); the product is exact in fp32 and rounded once to bf16 (nearest even).
+ * An id outside 0 .. V-1 writes a row of zeros and sets Q4_DEVERR_INDEX; nothing
+ * outside the table is read.  H % 16 == 0; qweight and out 16-byte aligned, ids
+ * 4-byte, scale 2-byte.  With Q4_FLAG_PDL the ids are read after the previous
+ * kernel in the stream has finished (griddepcontrol.wait).
+ */
+q4_status q4_embedding_int8(const int32_t *ids, const int8_t *qweight, const void *scale_f16,
+                            void *out_bf16, int M, int V, int H, void *stream);
 
 /*
  * Round-to-nearest quantisers: BF16 weights w [N, K] (row-major, device memory)

@@ -75,10 +75,11 @@ def _load():
         getattr(lib, name).argtypes = [p, p, i64]
     lib.q4o_quantize_int4g128.argtypes = [p, i64, i64, p, p, p]
     lib.q4o_quantize_nvfp4.argtypes = [p, i64, i64, p, p, p]
+    lib.q4o_embedding_int8.argtypes = [p, p, p, i64, i64, i64, p]
     for name in ("q4o_dequant_int4g128", "q4o_dequant_nvfp4", "q4o_linear_int4g128",
                  "q4o_linear_nvfp4", "q4o_head_restricted", "q4o_f32_to_fp16_array",
                  "q4o_f32_to_e4m3_array", "q4o_f32_to_e2m1_array", "q4o_quantize_int4g128",
-                 "q4o_quantize_nvfp4"):
+                 "q4o_quantize_nvfp4", "q4o_embedding_int8"):
         getattr(lib, name).restype = None
     _lib = lib
     return lib
@@ -250,3 +251,18 @@ def quantize_nvfp4(w_bf16_bits):
     g = np.zeros(1, np.float32)
     _load().q4o_quantize_nvfp4(_ptr(w), N, K, _ptr(q), _ptr(s), _ptr(g))
     return q, s, np.float32(g[0])
+
+
+# ------------------------------------------------------------------ embedding
+def embedding_int8(ids, qweight, scale_f16_bits) -> np.ndarray:
+    """fp64 [M, H]: rows ids of the int8 embedding times their fp16 row scale
+    (zeros for an id outside 0 .. V-1)."""
+    i = _c(np.asarray(ids, dtype=np.int32).reshape(-1), np.int32)
+    q = _c(qweight, np.int8)
+    s = _c(scale_f16_bits, np.uint16)
+    V, H = q.shape
+    if s.shape != (V,):
+        raise ValueError("embedding: scale must be [V]")
+    out = np.empty((i.size, H), np.float64)
+    _load().q4o_embedding_int8(_ptr(i), _ptr(q), _ptr(s), i.size, V, H, _ptr(out))
+    return out

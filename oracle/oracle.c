@@ -36,6 +36,10 @@
  *     infinities, S.1111.111 is NaN (same spec, FP8 E4M3).
  *   - The linear layer accumulates x[m,k] * w[n,k] in fp64 and returns fp64,
  *     unrounded.
+ *   - [EMB] "rumik-oss-1-int4", "Format": embed_tokens qweight int8 [V, 2048],
+ *     scale fp16 [V].  Reading: signed two's-complement codes, one symmetric scale
+ *     per row, e[t, k] = q[t, k] * scale[t] (exact in fp64); an id outside
+ *     0 .. V-1 gives a row of zeros.
  *   - Quantisers (round-to-nearest, from BF16 weights; the pages' own checkpoints
  *     were made with min/max rounding [INT4] and with GPTQ [NVFP4] -- GPTQ's
  *     error feedback is out of scope, the format is the same):
@@ -430,6 +434,24 @@ void q4o_quantize_nvfp4(const uint16_t *w_bf16, int64_t N, int64_t K, uint8_t *c
                 else
                     row[k / 2] |= (uint8_t)(c << 4);
             }
+        }
+    }
+}
+
+/* ------------------------------------------------------------- embedding */
+
+/* Gather and dequantise embedding rows [EMB]: out[m, k] = q[ids[m], k] *
+ * scale[ids[m]] in fp64 (exact), zeros for an id outside 0 .. V-1. */
+void q4o_embedding_int8(const int32_t *ids, const int8_t *qweight, const uint16_t *scale,
+                        int64_t M, int64_t V, int64_t H, double *out)
+{
+    for (int64_t m = 0; m < M; ++m) {
+        const int64_t t = ids[m];
+        for (int64_t k = 0; k < H; ++k) {
+            if (t < 0 || t >= V)
+                out[m * H + k] = 0.0;
+            else
+                out[m * H + k] = (double)qweight[t * H + k] * q4o_fp16_value(scale[t]);
         }
     }
 }

@@ -317,3 +317,37 @@ def test_int4_layout_bytes_reproduce_checkpoint_size():
     assert abs(total / 1e9 - nums["int4_checkpoint_gb"]) < 0.01
     assert nums["codebook_head_rows"] == 2048 + 1
     assert int4_bytes_per_weight() == 0.5 + 2 * 2 / nums["group_size_int4"]
+
+
+# ------------------------------------------------------------ int8 embedding
+def test_embedding_unit_scale_returns_signed_codes(oracle_mod):
+    """Scale 1.0: the gathered rows are the int8 codes themselves, read as
+    two's complement (bytes 0x80..0xff are -128..-1)."""
+    raw = np.arange(256, dtype=np.uint8).reshape(2, 128)
+    q = raw.view(np.int8)
+    s = np.full(2, 0x3C00, np.uint16)                  # fp16 1.0
+    out = oracle_mod.embedding_int8([1, 0, 1], q, s)
+    want = np.where(raw >= 128, raw.astype(np.int64) - 256, raw).astype(np.float64)
+    np.testing.assert_array_equal(out, want[[1, 0, 1]])
+
+
+def test_embedding_row_selection_and_scale(oracle_mod):
+    """One-hot rows: id t picks row t and multiplies by scale[t] only."""
+    V, H = 5, 16
+    q = np.zeros((V, H), np.int8)
+    for t in range(V):
+        q[t, t] = 1 + t
+    s = np.array([0x3800, 0x4000, 0x4400, 0x3400, 0xC000], np.uint16)  # .5 2 4 .25 -2
+    sv = np.array([0.5, 2.0, 4.0, 0.25, -2.0])
+    out = oracle_mod.embedding_int8([4, 2, 0], q, s)
+    for m, t in enumerate([4, 2, 0]):
+        want = np.zeros(H)
+        want[t] = (1 + t) * sv[t]
+        np.testing.assert_array_equal(out[m], want)
+
+
+def test_embedding_ids_outside_the_table_give_zeros(oracle_mod):
+    q = np.ones((3, 8), np.int8)
+    s = np.full(3, 0x3C00, np.uint16)
+    out = oracle_mod.embedding_int8([-1, 3, 2**31 - 1, 1], q, s)
+    assert np.all(out[:3] == 0) and np.all(out[3] == 1)
