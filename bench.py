@@ -158,6 +158,7 @@ class Workload:
     """Seeded inputs on the device, a ring of weight copies and one call per step."""
 
     def __init__(self, name: str, device):
+        import numpy as np
         import torch
         from bit_weight_only_q4_gb300 import layout, q4, synth
         from tests import parity as P
@@ -174,6 +175,14 @@ class Workload:
             self.layout = "nvfp4"
             self.desc = c["name"]
             base = P.nvfp4_dev(w)
+        elif name == "int8_gemv":
+            c = synth.INT8_GEMV_16384
+            x, w = synth.int8_gemv_16384()
+            self.M, self.N, self.K = c["M"], c["N"], c["K"]
+            self.layout = "int8"
+            self.desc = c["name"]
+            base = (torch.from_numpy(w.qweight),
+                    torch.from_numpy(w.scale.view(np.int16)).view(torch.float16))
         elif name == "int4_gemv":
             c = synth.INT4_GEMV_2048
             x, w = synth.int4_gemv_2048()
@@ -191,7 +200,8 @@ class Workload:
         self.ring = [tuple(t.to(device).clone() for t in base) for _ in range(self.copies)]
         self.y = torch.empty((self.M, self.N), dtype=torch.bfloat16, device=device)
         lay = q4.LAYOUT_NVFP4 if self.layout == "nvfp4" else q4.LAYOUT_INT4G128
-        self.ws = q4.alloc_workspace(lay, self.M, self.N, self.K, device)
+        self.ws = None if self.layout == "int8" else \
+            q4.alloc_workspace(lay, self.M, self.N, self.K, device)
         self.ring_bytes = self.copies * wbytes
         self.l2 = l2
 
@@ -201,6 +211,8 @@ class Workload:
         y = self.y if y is None else y
         if self.layout == "nvfp4":
             self.q4.q4_linear_nvfp4(x, *w, y=y, workspace=self.ws)
+        elif self.layout == "int8":
+            self.q4.q4_linear_int8(x, *w, y=y)
         else:
             self.q4.q4_linear_int4g128(x, *w, y=y, workspace=self.ws)
 
@@ -478,7 +490,7 @@ def run_profile(args, local):
     libbuild.build()
     q4.load()
     q4.set_launch_flags(0)
-    if args.workload in ("nvfp4_gemv", "int4_gemv"):
+    if args.workload in ("nvfp4_gemv", "int4_gemv", "int8_gemv"):
         wl = Workload(args.workload, device)
         call, desc = wl.call, wl.desc
     elif args.workload == "prefill":
@@ -639,6 +651,12 @@ def time_oracle(workload: str, budget_s: float = 12.0, steps: int | None = None)
 
         def run(rows):
             oracle.linear_nvfp4(x, w.codes[:rows], w.scale[:rows], w.global_scale)
+    elif workload == "int8_gemv":
+        x, w = synth.int8_gemv_16384()
+        N, K, lay = w.N, w.K, "int8"
+
+        def run(rows):
+            oracle.linear_int8(x, w.qweight[:rows], w.scale[:rows])
     else:
         x, w = synth.int4_gemv_2048()
         N, K, lay = w.N, w.K, "int4"
@@ -674,7 +692,8 @@ def run_reference(args, world, rank):
     if rank != 0:
         return
     wl_desc = {"nvfp4_gemv": "nvfp4 GEMV M=1 N=16384 K=2048",
-               "int4_gemv": "int4-g128 GEMV M=1 N=2048 K=2048"}[args.workload]
+               "int4_gemv": "int4-g128 GEMV M=1 N=2048 K=2048",
+               "int8_gemv": "int8 weight-only GEMV M=1 N=16384 K=2048"}[args.workload]
     budget = min(150.0, max(10.0, 2.0 * (args.steps + args.warmup)))
     cb = time_oracle(args.workload, budget_s=budget, steps=args.steps)
     line = {
@@ -697,7 +716,7 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=200000)
     ap.add_argument("--warmup", type=int, default=2000)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--workload", choices=("nvfp4_gemv", "int4_gemv", "decode_step", "batched", "quantize", "embedding",
+    ap.add_argument("--workload", choices=("nvfp4_gemv", "int4_gemv", "int8_gemv", "decode_step", "batched", "quantize", "embedding",
                                            "prefill"), default="nvfp4_gemv",
                     help="nvfp4_gemv is the bench line; the others print their own "
                          "measurement lines")

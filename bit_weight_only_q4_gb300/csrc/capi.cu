@@ -375,6 +375,42 @@ q4_status q4_dequant_nvfp4_f32(const uint8_t *codes, const uint8_t *scale_e4m3,
                                 static_cast<cudaStream_t>(stream));
 }
 
+q4_status q4_linear_int8(const void *x, const int8_t *qweight, const void *scale, void *y,
+                         int M, int N, int K, void *stream)
+{
+    if (!scale)
+        return fail(Q4_ERR_NULL, "scale must not be NULL");
+    if (K < 16 || K % 16)
+        return fail(Q4_ERR_SHAPE, "INT8 weight-only needs K >= 16 and K %% 16 == 0 (K=%d)", K);
+    q4_status s = check_common(M, N, K, nullptr, 0, 0, x, qweight, y);
+    if (s != Q4_OK)
+        return s;
+    if (!aligned(scale, 2))
+        return fail(Q4_ERR_ALIGN, "scale must be 2-byte aligned");
+    if (!rows_eligible(W_INT8, K))
+        return fail(Q4_ERR_SHAPE, "INT8 weight-only supports K up to 8192 (K=%d)", K);
+    DeviceInfo dev;
+    if ((s = current_device(dev)) != Q4_OK)
+        return s;
+    GemvParams p = {};
+    p.x = static_cast<const uint16_t *>(x);
+    p.w = reinterpret_cast<const uint8_t *>(qweight);
+    p.w_row_bytes = K;
+    p.scale = scale;
+    p.y = static_cast<uint16_t *>(y);
+    p.ldy = N;
+    p.N = N;
+    p.K = K;
+    p.row_begin = 0;
+    p.n_rows = N;
+    p.extra_row = -1;
+    RowsPlan plan;
+    if ((s = rows_plan(dev, W_INT8, M, N, K, plan)) != Q4_OK)
+        return s;
+    return rows_launch(plan, p, M, static_cast<cudaStream_t>(stream),
+                       (g_flags.load() & Q4_FLAG_PDL) != 0);
+}
+
 q4_status q4_embedding_int8(const int32_t *ids, const int8_t *qweight, const void *scale,
                             void *out, int M, int V, int H, void *stream)
 {

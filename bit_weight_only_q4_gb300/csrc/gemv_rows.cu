@@ -65,6 +65,17 @@ __device__ __forceinline__ void rows_load_x(const uint16_t *xs, const float *cf,
             const uint4 t = *reinterpret_cast<const uint4 *>(xs + (size_t)m * Kpad + col0);
             xr[m][0] = t.x; xr[m][1] = t.y; xr[m][2] = t.z; xr[m][3] = t.w;
             cd[m] = make_float4(1.f, 0.f, 0.f, 0.f);
+        } else if constexpr (WK == W_INT8) {
+            const uint4 *src = reinterpret_cast<const uint4 *>(xs + (size_t)m * Kpad) + ks * 64;
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const uint4 t = src[i * 32 + lane];
+                xr[m][4 * i + 0] = t.x; xr[m][4 * i + 1] = t.y;
+                xr[m][4 * i + 2] = t.z; xr[m][4 * i + 3] = t.w;
+            }
+            const float4 c4 = reinterpret_cast<const float4 *>(cf)[(size_t)m * (Kpad / 32) + col0 / 32];
+            // x' sum over this lane's 16 columns (first or second half of the chunk)
+            cd[m] = make_float4(c4.x, (lane & 1) ? c4.z : c4.y, 0.f, 0.f);
         } else {
             const uint4 *src = reinterpret_cast<const uint4 *>(xs + (size_t)m * Kpad) + ks * 128;
 #pragma unroll
@@ -98,6 +109,29 @@ __device__ __forceinline__ void rows_dot(const uint4 qv, uint32_t swr,
                 t = fma2_bf16(t, w4[jj], xr[m][jj]);
             out[m] = t;
         }
+    } else if constexpr (WK == W_INT8) {
+        // 16 signed codes: (q ^ 0x80) = q + 128 in the low byte of the fp16 magic
+        // 1024, i.e. 1152 + q, two per register; sum_k (1152 + q) x' - 1152 X = sum_k q x'
+        float A[MT];
+#pragma unroll
+        for (int m = 0; m < MT; ++m)
+            A[m] = 0.f;
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+            const uint32_t v = w4[jj] ^ 0x80808080u;
+            uint32_t pa, pb;
+            asm("prmt.b32 %0, %1, %2, 0x4140;" : "=r"(pa) : "r"(v), "r"(0x64646464u));   // cols 0, 1
+            asm("prmt.b32 %0, %1, %2, 0x4342;" : "=r"(pb) : "r"(v), "r"(0x64646464u));   // cols 2, 3
+#pragma unroll
+            for (int m = 0; m < MT; ++m) {
+                A[m] = fma2_f16(A[m], pa, xr[m][2 * jj + 0]);
+                A[m] = fma2_f16(A[m], pb, xr[m][2 * jj + 1]);
+            }
+        }
+        const float sc = f16lo_to_f32(swr);
+#pragma unroll
+        for (int m = 0; m < MT; ++m)
+            out[m] = fmaf(-1152.f, cd[m].y, A[m]) * cd[m].x * sc;
     } else if constexpr (WK == W_INT4) {
         float A1[MT], A2[MT];
 #pragma unroll
@@ -209,6 +243,9 @@ __device__ __forceinline__ uint32_t rows_scale_global(const GemvParams &p, int64
         return ld_nc_u16(static_cast<const uint16_t *>(p.scale) + gi) | (ld_nc_u16(p.minv + gi) << 16);
     } else if constexpr (WK == W_NVFP4_A16) {
         return ld_nc_u16(static_cast<const uint8_t *>(p.scale) + prow * (p.K / 16) + col0 / 16);
+    } else if constexpr (WK == W_INT8) {
+        (void)col0;
+        return ld_nc_u16(static_cast<const uint16_t *>(p.scale) + prow);
     } else {
         return 0u;
     }
@@ -225,7 +262,7 @@ q4_rows_kernel(GemvParams p)
     constexpr int KSTEP = Kind<WK>::KSTEP;
     constexpr int COLS = Kind<WK>::COLS;
     constexpr int CH = Kind<WK>::CH;
-    constexpr int XV = (WK == W_BF16) ? 4 : 16;      // x registers per token
+    constexpr int XV = (WK == W_BF16) ? 4 : ((WK == W_INT8) ? 8 : 16);   // x registers per token
     constexpr int G = RK_WARPS / S;
     constexpr int NSLOT = NB * RB;
     constexpr int Kpad = S * KSTEP;
@@ -246,7 +283,8 @@ q4_rows_kernel(GemvParams p)
     const int rows_cta = p.rows_q + (b < p.rows_r ? 1 : 0);
     const int my_rows = rows_cta > g ? (rows_cta - g + G - 1) / G : 0;   // rows g + G*j
     const int my_ring = my_rows > REG ? my_rows - REG : 0;    // rows j >= REG use the ring
-    const int64_t colbyte = (WK == W_BF16) ? (int64_t)col0 * 2 : (int64_t)(col0 / 2);
+    const int64_t colbyte = (WK == W_BF16) ? (int64_t)col0 * 2
+                            : (WK == W_INT8) ? (int64_t)col0 : (int64_t)(col0 / 2);
 
     // Request ring row jr (row j = REG + jr of this warp) into ring slot `slot`
     // (one commit group per call, empty past the last row, so wait_group counts
@@ -338,6 +376,9 @@ static const void *rows_select_s(int S)
     if (S == 2) return reinterpret_cast<const void *>(&q4_rows_kernel<WK, MT, RB, 2, NB, REG>);
     if (S == 4) return reinterpret_cast<const void *>(&q4_rows_kernel<WK, MT, RB, 4, NB, REG>);
     if (S == 8) return reinterpret_cast<const void *>(&q4_rows_kernel<WK, MT, RB, 8, NB, REG>);
+    if constexpr (WK == W_INT8 && MT == 1) {    // K up to 8192 int8 columns: 16 k-steps
+        if (S == 16) return reinterpret_cast<const void *>(&q4_rows_kernel<WK, MT, RB, 16, NB, REG>);
+    }
     return nullptr;
 }
 
@@ -357,6 +398,7 @@ static const void *rows_select(const RowsPlan &pl)
     if (pl.kind == W_INT4) return rows_select_kind<W_INT4>(pl.mt, pl.nb, pl.S);
     if (pl.kind == W_NVFP4_A16) return rows_select_kind<W_NVFP4_A16>(pl.mt, pl.nb, pl.S);
     if (pl.kind == W_BF16) return rows_select_kind<W_BF16>(pl.mt, pl.nb, pl.S);
+    if (pl.kind == W_INT8) return rows_select_kind<W_INT8>(pl.mt, pl.nb, pl.S);
     return nullptr;
 }
 
@@ -365,12 +407,18 @@ static int rows_warps(const RowsPlan &pl)
     return pl.mt == 1 ? RowsShape<1>::NW : RowsShape<2>::NW;
 }
 
+static int rows_kstep(int kind)
+{
+    return kind == W_BF16 ? 256 : (kind == W_INT8 ? 512 : 1024);
+}
+
 bool rows_eligible(int kind, int K)
 {
-    const int kstep = kind == W_BF16 ? 256 : 1024;
+    const int kstep = rows_kstep(kind);
     const int S = (K + kstep - 1) / kstep;
-    if (S != 1 && S != 2 && S != 4 && S != 8)
+    if (S != 1 && S != 2 && S != 4 && S != 8 && !(kind == W_INT8 && S == 16))
         return false;
+    if (kind == W_INT8) return K % 16 == 0;
     if (kind == W_INT4) return K % 128 == 0;
     if (kind == W_NVFP4_A16) return K % 32 == 0;
     if (kind == W_BF16) return K % 8 == 0;
@@ -381,10 +429,12 @@ q4_status rows_plan(const DeviceInfo &dev, int kind, int M, int N, int K, RowsPl
 {
     plan = RowsPlan{};
     plan.kind = kind;
-    const int kstep = kind == W_BF16 ? 256 : 1024;
-    const int ch = kind == W_INT4 ? 4 : (kind == W_BF16 ? 0 : 1);
+    const int kstep = rows_kstep(kind);
+    const int ch = (kind == W_INT4 || kind == W_INT8) ? 4 : (kind == W_BF16 ? 0 : 1);
     plan.S = (K + kstep - 1) / kstep;
     plan.mt = M >= 4 ? 4 : (M >= 2 ? 2 : 1);
+    if (plan.S > 8)
+        plan.mt = 1;                 // 16 k-steps need the 16-warp one-token CTA
     plan.rb = plan.mt == 4 ? 2 : 4;
     const int nw = plan.mt == 1 ? RowsShape<1>::NW : RowsShape<2>::NW;
     const int G = nw / plan.S;

@@ -43,7 +43,7 @@ struct GemvParams {
     unsigned *err;            // device error flags (bounded waits that timed out)
 };
 
-enum WeightKind { W_INT4 = 0, W_NVFP4_A16 = 1, W_NVFP4_A8 = 2, W_BF16 = 3 };
+enum WeightKind { W_INT4 = 0, W_NVFP4_A16 = 1, W_NVFP4_A8 = 2, W_BF16 = 3, W_INT8 = 4 };
 
 struct DeviceInfo {
     int device = -1;

@@ -26,11 +26,12 @@ namespace q4 {
 template <int WK>
 struct Kind {
     // columns held by one lane's 16 weight bytes
-    static constexpr int COLS = (WK == W_BF16) ? 8 : 32;
+    static constexpr int COLS = (WK == W_BF16) ? 8 : ((WK == W_INT8) ? 16 : 32);
     static constexpr int KSTEP = 32 * COLS;
     // floats of per-chunk data in shared memory: int4 (2^-p, X1, X2, 0),
     // NVFP4 (2^-p), bf16 none
-    static constexpr int CH = (WK == W_INT4) ? 4 : ((WK == W_BF16) ? 0 : 1);
+    // INT8: (2^-p, sum of x' over the chunk's first 16 columns, over its last 16, 0)
+    static constexpr int CH = (WK == W_INT4 || WK == W_INT8) ? 4 : ((WK == W_BF16) ? 0 : 1);
 };
 
 template <int RW>
@@ -47,6 +48,20 @@ struct UnitRegs {
 // vector loads a lane issues per k-step are each conflict-free across the warp.
 // For int4 each vector holds the pairs (x'[8j+t], x'[8j+t+4]), t = 0..3 -- the
 // order the nibble decoder produces codes in.
+// INT8 (16 columns per lane, k-steps of 512): vector i of lane l (columns
+// 16 l + 8 i .. + 7) at index ks * 64 + i * 32 + l.
+template <int WK>
+__device__ __forceinline__ int xs_vec_index_kind(int k0)
+{
+    if constexpr (WK == W_INT8) {
+        const int ks = k0 >> 9, kk = k0 & 511;
+        return ks * 64 + ((kk & 15) >> 3) * 32 + (kk >> 4);
+    } else {
+        const int ks = k0 >> 10, kk = k0 & 1023;
+        return ks * 128 + ((kk & 31) >> 3) * 32 + (kk >> 5);
+    }
+}
+
 __device__ __forceinline__ int xs_vec_index(int k0)
 {
     const int ks = k0 >> 10, kk = k0 & 1023;
@@ -118,7 +133,7 @@ __device__ void stage_x(const GemvParams &p, int Kpad, uint16_t *xs, float *cf, 
                 xq[2 * i + 1] = __high2float(hh);
             }
             if (active)
-                reinterpret_cast<uint4 *>(xs + (size_t)m * Kpad)[xs_vec_index(k0)] =
+                reinterpret_cast<uint4 *>(xs + (size_t)m * Kpad)[xs_vec_index_kind<WK>(k0)] =
                     make_uint4(h[0], h[1], h[2], h[3]);
             if constexpr (WK == W_INT4) {
                 // h[i] holds columns (i, i+4): even columns are i = 0, 2
@@ -131,6 +146,18 @@ __device__ void stage_x(const GemvParams &p, int Kpad, uint16_t *xs, float *cf, 
                 if (active && (k0 % 32) == 0)
                     reinterpret_cast<float4 *>(cf)[(size_t)m * (Kpad / 32) + k0 / 32] =
                         make_float4(pow2f(-pw), s_even, s_odd, 0.f);
+            } else if constexpr (WK == W_INT8) {
+                // sums of x' over the chunk's first and last 16 columns (the two
+                // lanes of the chunk): blocks t = 0, 1 and t = 2, 3
+                float sh = 0.f;
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    sh += xq[i];
+                sh += __shfl_xor_sync(0xffffffffu, sh, 1);
+                const float other = __shfl_xor_sync(0xffffffffu, sh, 2);
+                if (active && (k0 % 32) == 0)
+                    reinterpret_cast<float4 *>(cf)[(size_t)m * (Kpad / 32) + k0 / 32] =
+                        make_float4(pow2f(-pw), sh, other, 0.f);
             } else {
                 if (active && (k0 % 32) == 0)
                     cf[(size_t)m * (Kpad / 32) + k0 / 32] = pow2f(-pw);

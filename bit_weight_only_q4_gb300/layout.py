@@ -3,7 +3,9 @@
 int4-g128-minmax ("rumik-oss-1-int4", "Format"): 4-bit codes plus an fp16 scale
 and an fp16 min per 128 columns of a row.  NVFP4 weight-only ("VoxCPM2 NVFP4
 (GPTQ)", "NVFP4 settings"): 4-bit E2M1 codes plus one e4m3 scale per 16 columns
-and one fp32 global scale per matrix.  These are the algorithmic bytes a
+and one fp32 global scale per matrix.  INT8 weight-only (the reading of "Rumik
+TTS Fast Inference", "What Made It Faster"): int8 codes plus one fp16 scale per
+row.  These are the algorithmic bytes a
 weight-streaming kernel must move; the benchmark divides them by time.
 """
 from __future__ import annotations
@@ -26,6 +28,8 @@ def weight_bytes(layout: str, N: int, K: int) -> int:
         return N * K // 2 + 2 * 2 * N * (K // INT4_GROUP)
     if layout == "nvfp4":
         return N * K // 2 + N * (K // NVFP4_GROUP) + 4
+    if layout == "int8":                  # int8 codes + one fp16 scale per row
+        return N * K + 2 * N
     raise ValueError(layout)
 
 

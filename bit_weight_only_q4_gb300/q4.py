@@ -71,6 +71,7 @@ def load() -> ctypes.CDLL:
             "q4_dequant_nvfp4_f32": ([p, p, p, p, i, i, p], st),
             "q4_quantize_int4g128": ([p, p, p, p, i, i, p], st),
             "q4_embedding_int8": ([p, p, p, p, i, i, i, p], st),
+            "q4_linear_int8": ([p, p, p, p, i, i, i, p], st),
             "q4_quantize_nvfp4": ([p, p, p, p, i, i, p], st),
         }
         for name, (args, res) in sig.items():
@@ -88,7 +89,7 @@ def symbols() -> list[str]:
             "q4_linear_int4g128", "q4_linear_nvfp4", "audio_head_logits_restricted",
             "q4_linear_int4g128_noalloc", "q4_device_error_flags", "q4_dequant_int4g128_f32",
             "q4_dequant_nvfp4_f32", "q4_quantize_int4g128", "q4_quantize_nvfp4",
-            "q4_embedding_int8"]
+            "q4_embedding_int8", "q4_linear_int8"]
 
 
 def _check(status: int) -> None:
@@ -281,3 +282,17 @@ def q4_embedding_int8(ids, qweight, scale, out=None, stream=None):
     _check(load().q4_embedding_int8(_ptr(ids), _ptr(qweight), _ptr(scale), _ptr(out), M, V, H,
                                     _stream(stream)))
     return out
+
+
+def q4_linear_int8(x, qweight, scale, y=None, stream=None):
+    """y[M, N] (bf16) = x[M, K] (bf16) W^T, W int8 [N, K] with an fp16 scale per row."""
+    _cuda(x, "x", torch.bfloat16)
+    _cuda(qweight, "qweight", torch.int8)
+    _cuda(scale, "scale", torch.float16)
+    M, K = x.shape
+    N = qweight.shape[0]
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    _check(load().q4_linear_int8(_ptr(x), _ptr(qweight), _ptr(scale), _ptr(y), M, N, K,
+                                 _stream(stream)))
+    return y

@@ -100,6 +100,28 @@ def nvfp4_matrix(rng: np.random.Generator, N: int, K: int,
     return Nvfp4Matrix(q, s, np.float32(global_scale))
 
 
+@dataclass
+class Int8Matrix:
+    qweight: np.ndarray          # int8 [N, K]
+    scale: np.ndarray            # uint16 fp16 bits [N]
+
+    @property
+    def N(self) -> int:
+        return self.qweight.shape[0]
+
+    @property
+    def K(self) -> int:
+        return self.qweight.shape[1]
+
+
+def int8_matrix(rng: np.random.Generator, N: int, K: int) -> Int8Matrix:
+    """INT8 weight-only matrix: codes uniform over -128..127, fp16 row scales
+    U[2e-4, 1e-3] (a weight's absolute maximum over 127 for weights ~ N(0, 0.02))."""
+    q = rng.integers(-128, 128, size=(N, K), dtype=np.int8)
+    s = rng.uniform(2e-4, 1e-3, size=N).astype(np.float16)
+    return Int8Matrix(q, s.view(np.uint16).copy())
+
+
 def head_matrix(rng: np.random.Generator, rows: int = 2049, hidden: int = 2048,
                 std: float = 0.02) -> np.ndarray:
     """bf16 bits [rows, hidden] of the restricted audio head."""
@@ -110,6 +132,8 @@ def head_matrix(rng: np.random.Generator, rows: int = 2049, hidden: int = 2048,
 # Each workload is named by what it is and its sizes; the seed is part of it.
 
 INT4_GEMV_2048 = dict(name="int4-g128 GEMV M=1 N=2048 K=2048", seed=0, M=1, N=2048, K=2048)
+INT8_GEMV_16384 = dict(name="int8 weight-only GEMV M=1 N=16384 K=2048", seed=5, M=1,
+                       N=16384, K=2048)
 NVFP4_GEMV_16384 = dict(name="nvfp4 GEMV M=1 N=16384 K=2048", seed=1, M=1, N=16384, K=2048)
 DECODE_STACK_28 = dict(name="int4-g128 decode step, 28 layers, hidden 2048, ffn 8192, "
                             "restricted head 2049x2048", seed=2, layers=28, hidden=2048,
@@ -131,6 +155,14 @@ def int4_gemv_2048():
     c = INT4_GEMV_2048
     rng = rng_for(c["seed"])
     w = int4_matrix(rng, c["N"], c["K"])
+    x = activations(rng, c["M"], c["K"])
+    return x, w
+
+
+def int8_gemv_16384():
+    c = INT8_GEMV_16384
+    rng = rng_for(c["seed"])
+    w = int8_matrix(rng, c["N"], c["K"])
     x = activations(rng, c["M"], c["K"])
     return x, w
 

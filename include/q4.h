@@ -189,6 +189,19 @@ q4_status q4_dequant_nvfp4_f32(const uint8_t *codes, const uint8_t *scale_e4m3,
                                void *stream);
 
 /*
+ * INT8 weight-only linear ("Rumik TTS Fast Inference", "What Made It Faster": INT8
+ * weight-only decode projections; the layout is not given there).  Reading, after
+ * the int8 scheme "rumik-oss-1-int4" gives for its embedding: qweight int8 [N, K]
+ * (signed), scale fp16 [N] (one per output row), w[n, k] = q[n, k] * scale[n].
+ * y[M, N] = x[M, K] W^T with x, y bf16, fp32 accumulation, bf16 store.  Runs the
+ * whole-row CUDA-core kernel (one launch per 1, 2 or 4 tokens; K > 4096 one token
+ * per launch); no workspace.  K % 16 == 0 and K <= 8192; x, qweight, y 16-byte
+ * aligned, scale 2-byte.
+ */
+q4_status q4_linear_int8(const void *x_bf16, const int8_t *qweight, const void *scale_f16,
+                         void *y_bf16, int M, int N, int K, void *stream);
+
+/*
  * Token-embedding gather with int8 dequantisation ("rumik-oss-1-int4", "Format":
  * embed_tokens.qweight int8 [V, H], scale fp16 [V]): for each of the M token ids
  * (int32, device memory, typically written by the sampler of the previous step),

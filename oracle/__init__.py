@@ -76,10 +76,13 @@ def _load():
     lib.q4o_quantize_int4g128.argtypes = [p, i64, i64, p, p, p]
     lib.q4o_quantize_nvfp4.argtypes = [p, i64, i64, p, p, p]
     lib.q4o_embedding_int8.argtypes = [p, p, p, i64, i64, i64, p]
+    lib.q4o_dequant_int8.argtypes = [p, p, i64, i64, p]
+    lib.q4o_linear_int8.argtypes = [p, p, p, i64, i64, i64, p, p]
     for name in ("q4o_dequant_int4g128", "q4o_dequant_nvfp4", "q4o_linear_int4g128",
                  "q4o_linear_nvfp4", "q4o_head_restricted", "q4o_f32_to_fp16_array",
                  "q4o_f32_to_e4m3_array", "q4o_f32_to_e2m1_array", "q4o_quantize_int4g128",
-                 "q4o_quantize_nvfp4", "q4o_embedding_int8"):
+                 "q4o_quantize_nvfp4", "q4o_embedding_int8", "q4o_dequant_int8",
+                 "q4o_linear_int8"):
         getattr(lib, name).restype = None
     _lib = lib
     return lib
@@ -266,3 +269,32 @@ def embedding_int8(ids, qweight, scale_f16_bits) -> np.ndarray:
     out = np.empty((i.size, H), np.float64)
     _load().q4o_embedding_int8(_ptr(i), _ptr(q), _ptr(s), i.size, V, H, _ptr(out))
     return out
+
+
+# ------------------------------------------------------- INT8 weight-only
+def dequant_int8(qweight, scale_f16_bits) -> np.ndarray:
+    """fp32 [N, K] weights q * scale of the INT8 weight-only layout (exact)."""
+    q = _c(qweight, np.int8)
+    s = _c(scale_f16_bits, np.uint16)
+    N, K = q.shape
+    if s.shape != (N,):
+        raise ValueError("int8 shapes: qweight [N,K], scale [N]")
+    w = np.empty((N, K), np.float32)
+    _load().q4o_dequant_int8(_ptr(q), _ptr(s), N, K, _ptr(w))
+    return w
+
+
+def linear_int8(x_bf16_bits, qweight, scale_f16_bits, with_abs: bool = False):
+    """fp64 y [M, N] for the INT8 weight-only layout (see ``linear_int4g128``)."""
+    x = _c(np.atleast_2d(x_bf16_bits), np.uint16)
+    q = _c(qweight, np.int8)
+    s = _c(scale_f16_bits, np.uint16)
+    M, K = x.shape
+    N = q.shape[0]
+    if q.shape[1] != K or s.shape != (N,):
+        raise ValueError("int8 linear: shape mismatch")
+    y = np.empty((M, N), np.float64)
+    a = np.empty((M, N), np.float64) if with_abs else None
+    _load().q4o_linear_int8(_ptr(x), _ptr(q), _ptr(s), M, N, K, _ptr(y),
+                            _ptr(a) if with_abs else None)
+    return (y, a) if with_abs else y

@@ -36,6 +36,10 @@
  *     infinities, S.1111.111 is NaN (same spec, FP8 E4M3).
  *   - The linear layer accumulates x[m,k] * w[n,k] in fp64 and returns fp64,
  *     unrounded.
+ *   - [INT8] "Rumik TTS Fast Inference", "What Made It Faster": INT8 weight-only
+ *     decode projections, layout unstated.  Reading (the int8 scheme [EMB] gives
+ *     for the same model family): qweight int8 [N, K], one fp16 scale per output
+ *     row, w[n, k] = q[n, k] * scale[n], exact in fp32.
  *   - [EMB] "rumik-oss-1-int4", "Format": embed_tokens qweight int8 [V, 2048],
  *     scale fp16 [V].  Reading: signed two's-complement codes, one symmetric scale
  *     per row, e[t, k] = q[t, k] * scale[t] (exact in fp64); an id outside
@@ -270,6 +274,21 @@ void q4o_dequant_nvfp4(const uint8_t *codes, const uint8_t *scale_e4m3,
 /* y[m,n] = sum_k x[m,k] * w[n,k] in fp64, x bf16 [M,K] row-major.  Also returns
  * sum_k |x[m,k] * w[n,k]| (the scale of the per-element tolerance) when absy is
  * not NULL.  Each row of weights is decoded into a scratch row first. */
+/* One INT8 weight: q * scale, exact in fp32 [INT8]. */
+static float int8_weight(const uint8_t *qweight, const uint16_t *scale, int64_t K, int64_t n,
+                         int64_t k)
+{
+    return (float)((double)(int8_t)qweight[n * K + k] * q4o_fp16_value(scale[n]));
+}
+
+void q4o_dequant_int8(const int8_t *qweight, const uint16_t *scale, int64_t N, int64_t K,
+                      float *w)
+{
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t k = 0; k < K; ++k)
+            w[n * K + k] = int8_weight((const uint8_t *)qweight, scale, K, n, k);
+}
+
 static void linear_rows(int layout, const uint16_t *x, const uint8_t *packed,
                         const void *scale, const uint16_t *minv, float global_scale,
                         int64_t M, int64_t N, int64_t K, double *y, double *absy)
@@ -282,7 +301,9 @@ static void linear_rows(int layout, const uint16_t *x, const uint8_t *packed,
             for (int64_t k = 0; k < K; ++k)
                 wrow[k] = (layout == 0)
                     ? int4_weight(packed, (const uint16_t *)scale, minv, K, n, k)
-                    : nvfp4_weight(packed, (const uint8_t *)scale, global_scale, K, n, k);
+                    : (layout == 1)
+                    ? nvfp4_weight(packed, (const uint8_t *)scale, global_scale, K, n, k)
+                    : int8_weight(packed, (const uint16_t *)scale, K, n, k);
             for (int64_t m = 0; m < M; ++m) {
                 double acc = 0.0, aacc = 0.0;
                 for (int64_t k = 0; k < K; ++k) {
@@ -297,6 +318,12 @@ static void linear_rows(int layout, const uint16_t *x, const uint8_t *packed,
         }
         free(wrow);
     }
+}
+
+void q4o_linear_int8(const uint16_t *x_bf16, const int8_t *qweight, const uint16_t *scale_f16,
+                     int64_t M, int64_t N, int64_t K, double *y, double *absy)
+{
+    linear_rows(2, x_bf16, (const uint8_t *)qweight, scale_f16, NULL, 0.0f, M, N, K, y, absy);
 }
 
 void q4o_linear_int4g128(const uint16_t *x_bf16, const uint8_t *qweight,

@@ -351,3 +351,30 @@ def test_embedding_ids_outside_the_table_give_zeros(oracle_mod):
     s = np.full(3, 0x3C00, np.uint16)
     out = oracle_mod.embedding_int8([-1, 3, 2**31 - 1, 1], q, s)
     assert np.all(out[:3] == 0) and np.all(out[3] == 1)
+
+
+# --------------------------------------------------- INT8 weight-only linear
+def test_int8_linear_integer_case_is_integer_matmul(oracle_mod):
+    """Scale 1.0 and small-integer x: the oracle equals numpy's integer matmul of
+    the signed codes (two's complement)."""
+    rng = np.random.default_rng(21)
+    q = rng.integers(-128, 128, (9, 64)).astype(np.int8)
+    xi = rng.integers(-3, 4, (2, 64))
+    xb = (xi.astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)   # exact bf16
+    s = np.full(9, 0x3C00, np.uint16)
+    y = oracle_mod.linear_int8(xb, q, s)
+    np.testing.assert_array_equal(y, xi @ q.astype(np.int64).T)
+
+
+def test_int8_row_scale_applies_per_output_row(oracle_mod):
+    """One-hot x picks column k; row n's output is q[n, k] * scale[n]."""
+    q = np.array([[3, -7, 0, 0], [-128, 127, 1, 0]], np.int8)
+    s = np.array([0x3800, 0xC200], np.uint16)           # 0.5, -3.0
+    for k in range(4):
+        x = np.zeros((1, 4), np.float32)
+        x[0, k] = 1.0
+        xb = (x.view(np.uint32) >> 16).astype(np.uint16)
+        y = oracle_mod.linear_int8(xb, q, s)
+        np.testing.assert_array_equal(y[0], [q[0, k] * 0.5, q[1, k] * -3.0])
+    w = oracle_mod.dequant_int8(q, s)
+    np.testing.assert_array_equal(w, q.astype(np.float32) * np.array([[0.5], [-3.0]], np.float32))
