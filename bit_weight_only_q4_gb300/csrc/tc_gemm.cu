@@ -12,11 +12,10 @@
 //   * Warp 0 (one thread) streams, per chunk, the token tile of x (bf16, TMA
 //     tensor load with 128-byte swizzle) and the 128 rows x 32 bytes of packed
 //     codes (TMA tensor load) into a ring of shared-memory stages.
-//   * Sixteen worker warps dequantise every chunk together into the A operand
-//     tile (fp16, K-major, 128-byte swizzle): thread t takes a quarter row (16
-//     weights) -- row t / 4, columns 16 (t % 4) .. + 15 of the chunk -- so one
-//     chunk's latency chain (wait, convert, decode, proxy fence, arrive) is
-//     short and the tensor core is fed chunk after chunk.  They also convert the
+//   * Sixteen worker warps in two groups of eight take the stages in turn and
+//     dequantise them into the A operand tiles (fp16, K-major, 128-byte
+//     swizzle): a thread takes 16 weights of one row per step, and a warp's code
+//     reads are 256 contiguous bytes (no bank conflicts).  They also convert the
 //     chunk's x tile in place from bf16 to fp16 (for large M a small kernel
 //     converts x once per call instead).  int4: w = fp16(c * s + m) (one fused
 //     multiply-add, single rounding); NVFP4: w = E2M1 * e4m3 in fp16, exact (the
@@ -203,7 +202,7 @@ struct TcStage {
     static constexpr uint32_t CODE = SC * 4096u;        // 128 rows x SC * 32 bytes
 };
 
-template <int LAYOUT, int SC>   // LAYOUT 0 int4-g128, 1 NVFP4
+template <int LAYOUT, int SC, int G>   // LAYOUT 0 int4-g128, 1 NVFP4; G worker groups
 __global__ void __launch_bounds__(TC_THREADS, 1)
 q4_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap wmap,
              TcParams p)
@@ -241,7 +240,7 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
         TC_TRACE(0);
         for (int i = 0; i < NS; ++i) {
             mbar_init(smem_u32(&bars[i]), 1);                  // TMA arrive + bytes
-            mbar_init(smem_u32(&bars[NS + i]), TC_WORKERS);    // every worker warp
+            mbar_init(smem_u32(&bars[NS + i]), TC_WORKERS / G);   // the stage's worker group
             mbar_init(smem_u32(&bars[2 * NS + i]), 1);         // MMA commit
         }
         mbar_init(smem_u32(&bars[3 * NS]), 1);                 // final commit
@@ -323,25 +322,32 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
         if (lane == 0) TC_TRACE(63);
     } else {
         // ------------------------------------------------------------- workers
-        // Dequant mapping: a warp reads 256 contiguous code bytes per step (no
-        // bank conflicts): L = 4 SC lanes per code row, 32 / L rows per step, SC
-        // steps.  In step k a lane takes 16 weights: row 8 w + (32 / L) k + lane / L,
-        // chunk c = (lane % L) / 4, columns 16 (lane % 4) .. + 15 of that chunk.
+        // G groups of WG = 16 / G warps take the stages in turn (group gi the
+        // stages gi, gi + G, ...), so G stages are dequantised at once.
+        // Dequant mapping inside a group: a warp reads 256 contiguous code bytes
+        // per step (no bank conflicts): L = 4 SC lanes per code row, 32 / L rows per
+        // step, STEPS = SC * G steps.  In step k a lane takes 16 weights: row
+        // (128 / WG) wg + (32 / L) k + lane / L, chunk c = (lane % L) / 4, columns
+        // 16 (lane % 4) .. + 15 of that chunk.
+        constexpr int WG = TC_WORKERS / G;
         constexpr int L = 4 * SC;
         constexpr int RPS = 32 / L;
-        constexpr int SA = 4;                    // super-chunks of scales loaded ahead
+        constexpr int STEPS = SC * G;
+        constexpr int SA = 4;                    // stages of scales loaded ahead
         const int w = warp - 2;                  // 0..15
         const int grp = w >> 2;                  // epilogue: column share of the quadrant
         const int quad = warp & 3;               // TMEM lane quadrant of this warp
-        const int wt = w * 32 + lane;            // 0..511
+        const int gi = w / WG;                   // worker group
+        const int wg = w % WG;                   // warp within the group
+        const int wt = wg * 32 + lane;           // thread within the group
         const int cl = lane % L;
         const int c = cl >> 2;
         const int qd = cl & 3;
-        int rowk[SC];
-        bool rok[SC];
+        int rowk[STEPS];
+        bool rok[STEPS];
 #pragma unroll
-        for (int k = 0; k < SC; ++k) {
-            rowk[k] = 8 * w + RPS * k + lane / L;
+        for (int k = 0; k < STEPS; ++k) {
+            rowk[k] = (128 / WG) * wg + RPS * k + lane / L;
             rok[k] = n0 + rowk[k] < p.N;
         }
         auto load_scale = [&](int u, int k) -> uint32_t {
@@ -357,24 +363,24 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
                 return ld_nc_u8(static_cast<const uint8_t *>(p.scale) + n * (p.K / 16) + kc * 4 + qd);
             }
         };
-        uint32_t scq[SA][SC];
+        uint32_t scq[SA][STEPS];
 #pragma unroll
         for (int j = 0; j < SA; ++j)
 #pragma unroll
-            for (int k = 0; k < SC; ++k)
-                scq[j][k] = j < nsup ? load_scale(j, k) : 0u;
+            for (int k = 0; k < STEPS; ++k)
+                scq[j][k] = gi + j * G < nsup ? load_scale(gi + j * G, k) : 0u;
         bool range_bad = false;
         TC_PHASE_DECL;
-        for (int u = 0; u < nsup; ++u) {
+        for (int u = gi; u < nsup; u += G) {
             const int s = u % NS, use = u / NS;
-            uint32_t sc[SC];
+            uint32_t sc[STEPS];
 #pragma unroll
-            for (int k = 0; k < SC; ++k) {
+            for (int k = 0; k < STEPS; ++k) {
                 sc[k] = scq[0][k];
 #pragma unroll
                 for (int j = 0; j + 1 < SA; ++j)
                     scq[j][k] = scq[j + 1][k];
-                scq[SA - 1][k] = u + SA < nsup ? load_scale(u + SA, k) : 0u;
+                scq[SA - 1][k] = u + SA * G < nsup ? load_scale(u + SA * G, k) : 0u;
             }
             const int kc = c0 + u * SC;
             const int nv = (c1 - kc) < SC ? (c1 - kc) : SC;
@@ -386,13 +392,13 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
             TC_PHASE(56, t0, t1);
             // x sub-tiles: bf16 -> fp16 in place (element-wise, swizzle-agnostic).
             // Only tiles of at most 64 tokens are converted here (larger M arrive
-            // in fp16), so a thread has at most SC 16-byte vectors: the loop is
+            // in fp16), so a thread has at most SC * G 16-byte vectors: the loop is
             // unrolled and interleaves with the code loads below.
             if (!p.x_f16) {
                 const int per = TN * 8;                  // vectors per sub-tile
 #pragma unroll
-                for (int j = 0; j < SC; ++j) {
-                    const int v = wt + j * TC_WORKERS * 32;
+                for (int j = 0; j < SC * G; ++j) {
+                    const int v = wt + j * WG * 32;
                     if (v < nv * per) {
                         const int sub = (v >= per) + (v >= 2 * per) + (v >= 3 * per);
                         uint4 *xv = reinterpret_cast<uint4 *>(st + TcStage<SC>::A + sub * x_stride) +
@@ -419,7 +425,7 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
             TC_PHASE(57, t1, t2);
             const unsigned char *codes = st + TcStage<SC>::A + SC * x_stride;
 #pragma unroll
-            for (int k = 0; k < SC; ++k) {
+            for (int k = 0; k < STEPS; ++k) {
                 const int rd = rowk[k];
                 const uint2 cw = *reinterpret_cast<const uint2 *>(codes + rd * (SC * 32) + cl * 8);
                 const uint32_t words[2] = {cw.x, cw.y};
@@ -525,7 +531,7 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
                 const size_t kstride4 = (size_t)TN * TC_ROWS / 4;
                 const float4 *part = reinterpret_cast<const float4 *>(
                     p.ws + (size_t)tile * p.KS * TN * TC_ROWS);
-                for (int g4 = wt; g4 < TN * (TC_ROWS / 4); g4 += TC_WORKERS * 32) {
+                for (int g4 = w * 32 + lane; g4 < TN * (TC_ROWS / 4); g4 += TC_WORKERS * 32) {
                     const int c = g4 / (TC_ROWS / 4), q = g4 % (TC_ROWS / 4);
                     float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
                     for (int k0 = 0; k0 < p.KS; k0 += 8) {
@@ -677,6 +683,23 @@ size_t tc_workspace_bytes(int M, int N, int K, int sms)
     return tc_xf16_bytes(M, K) + tc_split_bytes(M, N, K, sms);
 }
 
+template <int LAYOUT>
+static const void *tc_select_layout(int sc, int groups)
+{
+    if (groups == 2)
+        return sc == 4 ? reinterpret_cast<const void *>(&q4_tc_kernel<LAYOUT, 4, 2>)
+             : sc == 2 ? reinterpret_cast<const void *>(&q4_tc_kernel<LAYOUT, 2, 2>)
+                       : reinterpret_cast<const void *>(&q4_tc_kernel<LAYOUT, 1, 2>);
+    return sc == 4 ? reinterpret_cast<const void *>(&q4_tc_kernel<LAYOUT, 4, 1>)
+         : sc == 2 ? reinterpret_cast<const void *>(&q4_tc_kernel<LAYOUT, 2, 1>)
+                   : reinterpret_cast<const void *>(&q4_tc_kernel<LAYOUT, 1, 1>);
+}
+
+static const void *tc_select(int kind, int sc, int groups)
+{
+    return kind == W_INT4 ? tc_select_layout<0>(sc, groups) : tc_select_layout<1>(sc, groups);
+}
+
 q4_status tc_launch(int kind, const void *x, const uint8_t *codes, const void *scale,
                     const void *minv, const float *gscale, void *y, int M, int N, int K,
                     void *ws, size_t ws_bytes, cudaStream_t stream, bool pdl)
@@ -801,15 +824,14 @@ q4_status tc_launch(int kind, const void *x, const uint8_t *codes, const void *s
         if (r != CUDA_SUCCESS)
             return fail(Q4_ERR_CUDA, "cuTensorMapEncodeTiled(codes) failed (%d)", (int)r);
     }
-    const void *k = nullptr;
-    if (kind == W_INT4)
-        k = sc == 4 ? reinterpret_cast<const void *>(&q4_tc_kernel<0, 4>)
-            : sc == 2 ? reinterpret_cast<const void *>(&q4_tc_kernel<0, 2>)
-                      : reinterpret_cast<const void *>(&q4_tc_kernel<0, 1>);
-    else
-        k = sc == 4 ? reinterpret_cast<const void *>(&q4_tc_kernel<1, 4>)
-            : sc == 2 ? reinterpret_cast<const void *>(&q4_tc_kernel<1, 2>)
-                      : reinterpret_cast<const void *>(&q4_tc_kernel<1, 1>);
+    // two worker groups, two stages dequantised at once (measured: prefill
+    // GEMMs 5-22% faster than one group of 16 warps; batched decode unchanged)
+#ifdef Q4_TC_GROUPS
+    const int groups = Q4_TC_GROUPS;
+#else
+    const int groups = 2;
+#endif
+    const void *k = tc_select(kind, sc, groups);
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess)
         return cuda_fail(e, "cudaFuncSetAttribute(tensor-core kernel)");
