@@ -179,7 +179,8 @@ const char *q4_last_error_string(void) { return g_last_error; }
 
 q4_status q4_set_launch_flags(unsigned flags)
 {
-    const unsigned known = Q4_FLAG_PDL | Q4_FLAG_FORCE_CUDA_CORE | Q4_FLAG_FORCE_TENSOR_CORE;
+    const unsigned known =
+        Q4_FLAG_PDL | Q4_FLAG_FORCE_CUDA_CORE | Q4_FLAG_FORCE_TENSOR_CORE | Q4_FLAG_TC_SKINNY;
     if (flags & ~known)
         return fail(Q4_ERR_ARG, "unknown launch flags 0x%x", flags & ~known);
     if ((flags & Q4_FLAG_FORCE_CUDA_CORE) && (flags & Q4_FLAG_FORCE_TENSOR_CORE))
@@ -238,7 +239,7 @@ q4_status q4_linear_int4g128(const void *x, const uint8_t *qweight, const void *
         ((flags & Q4_FLAG_FORCE_TENSOR_CORE) || M >= kTensorCoreMinM))
         return tc_launch(W_INT4, x, qweight, scale, minv, nullptr, y, M, N, K, workspace,
                          workspace_bytes, static_cast<cudaStream_t>(stream),
-                         (flags & Q4_FLAG_PDL) != 0);
+                         (flags & Q4_FLAG_PDL) != 0, (flags & Q4_FLAG_TC_SKINNY) != 0);
     GemvParams p = {};
     p.x = static_cast<const uint16_t *>(x);
     p.w = qweight;
@@ -278,7 +279,7 @@ q4_status q4_linear_nvfp4(const void *x, const uint8_t *codes, const uint8_t *sc
         ((flags & Q4_FLAG_FORCE_TENSOR_CORE) || M >= kTensorCoreMinM))
         return tc_launch(W_NVFP4_A16, x, codes, scale_e4m3, nullptr, global_scale, y, M, N, K,
                          workspace, workspace_bytes, static_cast<cudaStream_t>(stream),
-                         (flags & Q4_FLAG_PDL) != 0);
+                         (flags & Q4_FLAG_PDL) != 0, (flags & Q4_FLAG_TC_SKINNY) != 0);
     GemvParams p = {};
     p.x = static_cast<const uint16_t *>(x);
     p.w = codes;

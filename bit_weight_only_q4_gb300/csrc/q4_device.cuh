@@ -250,6 +250,21 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigne
     return false;
 }
 
+// The same wait for a whole (converged) warp: lane 0 polls and the other lanes
+// wait at the warp barrier, which orders their later reads after lane 0's
+// acquire.  A waiting warp then keeps one poll in the shared-memory pipe instead
+// of 32 -- with two dozen warps waiting at once the per-lane polls slowed the
+// copies and everything else that shares the pipe.
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, unsigned *err)
+{
+    int ok = 1;
+    if ((threadIdx.x & 31) == 0)
+        ok = mbar_wait(bar, parity, err) ? 1 : 0;
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    __syncwarp();
+    return ok != 0;
+}
+
 // One contiguous global -> shared copy on the TMA engine; completion is counted
 // in bytes on the mbarrier.  dst, src 16-byte aligned; bytes a multiple of 16.
 __device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void *src, uint32_t bytes,

@@ -103,7 +103,8 @@ bool tc_eligible(int kind, int M, int N, int K);
 size_t tc_workspace_bytes(int M, int N, int K, int sms);
 q4_status tc_launch(int kind, const void *x, const uint8_t *codes, const void *scale,
                     const void *minv, const float *gscale, void *y, int M, int N, int K,
-                    void *ws, size_t ws_bytes, cudaStream_t stream, bool pdl);
+                    void *ws, size_t ws_bytes, cudaStream_t stream, bool pdl,
+                    bool skinny);
 
 // Device address of the library's error-flag word on the current device.
 unsigned *device_error_flags();

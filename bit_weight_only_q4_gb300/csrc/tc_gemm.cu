@@ -76,6 +76,7 @@ extern "C" int q4_tc_trace_copy(unsigned long long *host, int n)
 #endif
 
 struct TcParams {
+    const uint16_t *x;         // bf16 [M, K] (skinny kernel; the ring kernel uses a tensor map)
     const uint8_t *codes;      // [N, K/2]
     const void *scale;         // int4: fp16 [N, K/128]; NVFP4: e4m3 [N, K/16]
     const uint16_t *minv;      // int4: fp16 [N, K/128]
@@ -147,6 +148,22 @@ __device__ __forceinline__ void mma_f16(uint32_t tmem_d, uint64_t a, uint64_t b,
                  : "memory");
 }
 
+// The same with both descriptors passed as 32-bit halves, so that the issuing
+// loop only steps the start-address fields (low halves: +2 per 32 bytes).  One
+// thread issues every MMA of a CTA; rebuilding two 64-bit descriptors per MMA
+// made that thread, not the tensor core, the limit.
+__device__ __forceinline__ void mma_f16_2(uint32_t tmem_d, uint32_t a_lo, uint32_t a_hi, uint32_t b_lo,
+                                          uint32_t b_hi, uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile("{\n\t.reg .b64 ad, bd;\n\t.reg .pred p;\n\t"
+                 "setp.ne.u32 p, %6, 0;\n\t"
+                 "mov.b64 ad, {%1, %2};\n\t"
+                 "mov.b64 bd, {%3, %4};\n\t"
+                 "tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %5, p;\n\t}"
+                 ::"r"(tmem_d), "r"(a_lo), "r"(a_hi), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate)
+                 : "memory");
+}
+
 __device__ __forceinline__ void mma_commit(uint32_t bar)
 {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
@@ -188,6 +205,101 @@ __device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b)
 __device__ __forceinline__ uint32_t f16x2_splat(uint32_t h16)
 {
     return (h16 & 0xffffu) | (h16 << 16);
+}
+
+// Epilogue of both tensor-core kernels, run by the 16 worker warps (w = 0..15)
+// once the final MMA commit has been seen (ok): read the accumulator back from
+// TMEM (warp w reads lane quadrant (w + 2) % 4, a quarter of its columns),
+// release warp 1 to free TMEM after the last read, then store bf16 y -- or, under
+// split-K, fp32 partials that the last CTA of the tile to arrive sums in k order.
+template <int LAYOUT>
+__device__ __forceinline__ void tc_epilogue(const TcParams &p, uint32_t tmem_base, bool ok, int w,
+                                            int lane, int n0, int m0, int tile, int ks,
+                                            unsigned *last_flag)
+{
+    const int TN = p.TN;
+    const int quad = (w + 2) & 3;            // TMEM lane quadrant of this warp
+    const int grp = w >> 2;                  // column share of the quadrant
+    const int r = quad * 32 + lane;          // TMEM lane = weight row within the tile
+    const int n = n0 + r;
+    const bool nok = n < p.N;
+    float gsc = 1.f;
+    if constexpr (LAYOUT == 1)
+        gsc = __ldg(p.gscale);
+    const int ncb = (TN + 16 * TC_GROUPS - 1) / (16 * TC_GROUPS);   // same for every worker
+    for (int it = 0; it < ncb; ++it) {
+        const int cb = grp * 16 + it * 16 * TC_GROUPS;
+        uint32_t v[16];
+        if (cb < TN)
+            tmem_ld16(tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)cb, v);
+        if (it == ncb - 1) {
+            // last TMEM read done: let warp 1 free the accumulator now
+            tc_fence_before();
+            asm volatile("bar.arrive 3, %0;" ::"r"((TC_WORKERS + 1) * 32) : "memory");
+        }
+        if (!ok || cb >= TN)
+            continue;
+        if (p.KS == 1) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const int m = m0 + cb + j;
+                if (nok && m < p.M)
+                    p.y[(int64_t)m * p.N + n] = f32_to_bf16_bits(__uint_as_float(v[j]) * gsc);
+            }
+        } else {
+            float *dst = p.ws + ((size_t)(tile * p.KS + ks) * TN + cb) * TC_ROWS + r;
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+                dst[(size_t)j * TC_ROWS] = __uint_as_float(v[j]);
+        }
+    }
+    if (p.KS > 1) {
+        // split-K: the last CTA of this tile to arrive sums the partials (every
+        // worker reaches both barriers, whatever happened before)
+        __threadfence();
+        asm volatile("bar.sync 2, %0;" ::"r"(TC_WORKERS * 32) : "memory");
+        if (w == 0 && lane == 0)
+            *last_flag = (ok && atomicAdd(&p.tickets[tile], 1u) == (unsigned)(p.KS - 1)) ? 1u : 0u;
+        asm volatile("bar.sync 2, %0;" ::"r"(TC_WORKERS * 32) : "memory");
+        if (*last_flag) {
+            __threadfence();
+            // Each thread sums groups of four rows of one token column: all KS
+            // partials of a group are loaded (16 bytes each) before the adds,
+            // which run in k order, so the result does not depend on timing.
+            const size_t kstride4 = (size_t)TN * TC_ROWS / 4;
+            const float4 *part = reinterpret_cast<const float4 *>(
+                p.ws + (size_t)tile * p.KS * TN * TC_ROWS);
+            for (int g4 = w * 32 + lane; g4 < TN * (TC_ROWS / 4); g4 += TC_WORKERS * 32) {
+                const int c = g4 / (TC_ROWS / 4), q = g4 % (TC_ROWS / 4);
+                float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int k0 = 0; k0 < p.KS; k0 += 8) {
+                    float4 v[8];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        if (k0 + j < p.KS)
+                            v[j] = __ldcg(part + (k0 + j) * kstride4 + (size_t)c * (TC_ROWS / 4) + q);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        if (k0 + j < p.KS) {
+                            sum.x += v[j].x; sum.y += v[j].y;
+                            sum.z += v[j].z; sum.w += v[j].w;
+                        }
+                }
+                const int m = m0 + c;
+                const int nb = n0 + 4 * q;
+                if (m < p.M) {
+                    uint16_t *yr = p.y + (int64_t)m * p.N;
+                    const float o[4] = {sum.x, sum.y, sum.z, sum.w};
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        if (nb + i < p.N)
+                            yr[nb + i] = f32_to_bf16_bits(o[i] * gsc);
+                }
+            }
+            if (w == 0 && lane == 0)
+                p.tickets[tile] = 0u;
+        }
+    }
 }
 
 // ------------------------------------------------------------------ kernel
@@ -301,12 +413,19 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
                 const int kc = c0 + u * SC;
                 const int nv = (c1 - kc) < SC ? (c1 - kc) : SC;
                 const uint32_t st = smem_u32(smem + (size_t)s * stage_bytes);
-                for (int c = 0; c < nv; ++c) {
+                const uint64_t ad = smem_desc_sw128(st);
+                const uint64_t bd = smem_desc_sw128(st + TcStage<SC>::A);
+                const uint32_t alo = (uint32_t)ad, ahi = (uint32_t)(ad >> 32);
+                const uint32_t blo = (uint32_t)bd, bhi = (uint32_t)(bd >> 32);
+#pragma unroll
+                for (int c = 0; c < SC; ++c) {
+                    if (c >= nv)
+                        break;
 #pragma unroll
                     for (int kk = 0; kk < TC_KC / 16; ++kk)
-                        mma_f16(tmem_base, smem_desc_sw128(st + c * 16384 + kk * 32),
-                                smem_desc_sw128(st + TcStage<SC>::A + c * x_stride + kk * 32), idesc,
-                                (u > 0 || c > 0 || kk > 0) ? 1u : 0u);
+                        mma_f16_2(tmem_base, alo + (uint32_t)c * 1024u + 2u * kk, ahi,
+                                  blo + (uint32_t)c * (x_stride >> 4) + 2u * kk, bhi, idesc,
+                                  (u > 0 || c > 0 || kk > 0) ? 1u : 0u);
                 }
                 mma_commit(smem_u32(&bars[2 * NS + s]));
                 TC_TRACE(40 + u);
@@ -335,8 +454,6 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
         constexpr int STEPS = SC * G;
         constexpr int SA = 4;                    // stages of scales loaded ahead
         const int w = warp - 2;                  // 0..15
-        const int grp = w >> 2;                  // epilogue: column share of the quadrant
-        const int quad = warp & 3;               // TMEM lane quadrant of this warp
         const int gi = w / WG;                   // worker group
         const int wg = w % WG;                   // warp within the group
         const int wt = wg * 32 + lane;           // thread within the group
@@ -386,7 +503,7 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
             const int nv = (c1 - kc) < SC ? (c1 - kc) : SC;
             unsigned char *st = smem + (size_t)s * stage_bytes;
             TC_CLK(t0);
-            if (!mbar_wait(smem_u32(&bars[s]), use & 1, p.err))
+            if (!mbar_wait_warp(smem_u32(&bars[s]), use & 1, p.err))
                 break;
             TC_CLK(t1);
             TC_PHASE(56, t0, t1);
@@ -477,94 +594,518 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
             atomicOr(p.err, kErrFp16Range);
 
         // ------------------------------------------------------------ epilogue
-        const int r = quad * 32 + lane;          // TMEM lane = weight row within the tile
-        const int n = n0 + r;
-        const bool nok = n < p.N;
-        const bool ok = nsup > 0 && mbar_wait(smem_u32(&bars[3 * NS]), 0, p.err);
+        const bool ok = nsup > 0 && mbar_wait_warp(smem_u32(&bars[3 * NS]), 0, p.err);
         tc_fence_after();
         if (warp == 2 && lane == 0) TC_TRACE(2);
-        float gsc = 1.f;
-        if constexpr (LAYOUT == 1)
-            gsc = __ldg(p.gscale);
-        const int tile = tile_n * p.tiles_m + tile_m;
-        const int ncb = (TN + 16 * TC_GROUPS - 1) / (16 * TC_GROUPS);   // same for every worker
-        for (int it = 0; it < ncb; ++it) {
-            const int cb = grp * 16 + it * 16 * TC_GROUPS;
-            uint32_t v[16];
-            if (cb < TN)
-                tmem_ld16(tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)cb, v);
-            if (it == ncb - 1) {
-                // last TMEM read done: let warp 1 free the accumulator now
-                tc_fence_before();
-                asm volatile("bar.arrive 3, %0;" ::"r"((TC_WORKERS + 1) * 32) : "memory");
+        __shared__ unsigned last_flag;
+        tc_epilogue<LAYOUT>(p, tmem_base, ok, w, lane, n0, m0, tile_n * p.tiles_m + tile_m, ks,
+                            &last_flag);
+    }
+
+    __syncthreads();
+    if (threadIdx.x == 0) TC_TRACE(3);
+}
+
+// ------------------------------------------------------------ skinny kernel
+// Batched decode (tiles of at most 64 tokens) reads few bytes of x per weight.
+// The ring kernel above stages x, codes and A together through shared memory
+// and issues every copy from one thread; for small tiles it is bound by that
+// issue rate.  This kernel is built around three measured limits instead:
+//   * copies issued by one thread do not overlap much; spread over several
+//     warps they reach ~150 GB/s per SM from L2 and the SM's share of HBM.  So
+//     the codes of the CTA's whole K range are requested at once (16 KB boxes)
+//     before the dependency wait -- weights do not depend on the previous
+//     kernel -- and eight x warps each request every eighth step of x after it;
+//   * shared-memory bandwidth: the dequantised A tiles never touch shared
+//     memory -- each worker writes its row of fp16 weights into tensor memory
+//     (tcgen05.st) and the MMA reads A from there, through a ring of six
+//     two-chunk slots;
+//   * the split-K CTAs of one weight tile form a thread-block cluster: each dumps
+//     its fp32 accumulator into its own shared memory, and after a cluster
+//     barrier each sums 1/KS of the tile over the KS dumps (read through
+//     distributed shared memory) in k order -- deterministic, no workspace.
+__device__ __forceinline__ float4 ld_cluster_f4(uint32_t local_addr, uint32_t rank)
+{
+    uint32_t ra;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(local_addr), "r"(rank));
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(ra)
+                 : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void cluster_sync_all()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Scale loads straight into 32-bit registers (no widening instruction that
+// would wait for the load).
+__device__ __forceinline__ uint32_t ld_nc_u8_r32(const void *p)
+{
+    uint32_t r;
+    asm volatile("ld.global.nc.u8 %0, [%1];" : "=r"(r) : "l"(p));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t ld_nc_u16_r32(const void *p)
+{
+    uint32_t r;
+    asm volatile("ld.global.nc.u16 %0, [%1];" : "=r"(r) : "l"(p));
+    return r;
+}
+
+// 16 codes (one row, 16 consecutive columns) -> 16 fp16 weights: int4
+// w = c * s + min (one fused multiply-add, one rounding); NVFP4 w = E2M1 * e4m3,
+// exact in fp16 (the global scale is applied in the epilogue).
+template <int LAYOUT>
+__device__ __forceinline__ void tc_decode16(uint2 cw, uint32_t sc, uint32_t (&o)[8])
+{
+    const uint32_t words[2] = {cw.x, cw.y};
+    if constexpr (LAYOUT == 0) {
+        const uint32_t s2 = f16x2_splat(sc & 0xffffu);
+        const uint32_t m2 = f16x2_splat(sc >> 16);
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+#pragma unroll
+            for (int b = 0; b < 4; ++b) {
+                // byte b -> (1024 + c_lo, 1024 + 16 c_hi) -> (c_lo, c_hi)
+                const uint32_t t = prmt(words[j], 0u, (uint32_t)(b | (4 << 4) | (b << 8) | (4 << 12)));
+                uint32_t v2;
+                asm("lop3.b32 %0, %1, 0x00F0000F, 0x64006400, 0xEA;" : "=r"(v2) : "r"(t));
+                v2 = hfma2(v2, 0x2C003C00u, 0xD400E400u);   // * (1, 1/16) + (-1024, -64)
+                o[4 * j + b] = hfma2(v2, s2, m2);
             }
-            if (!ok || cb >= TN)
-                continue;
-            if (p.KS == 1) {
+    } else {
+        const uint32_t sg = f16x2_splat(e4m3x2_to_f16x2(sc & 0xffu) & 0xffffu);
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const int m = m0 + cb + j;
-                    if (nok && m < p.M)
-                        p.y[(int64_t)m * p.N + n] = f32_to_bf16_bits(__uint_as_float(v[j]) * gsc);
+        for (int j = 0; j < 2; ++j) {
+            uint32_t h[4];
+            e2m1x8_to_f16x2x4(words[j], h);
+#pragma unroll
+            for (int b = 0; b < 4; ++b)
+                o[4 * j + b] = hmul2(h[b], sg);
+        }
+    }
+}
+
+constexpr int SK_XWARPS = 8;                          // x loading / conversion warps
+constexpr int SK_THREADS = TC_THREADS + SK_XWARPS * 32;
+constexpr int SK_NA = 6;                              // TMEM A slots of two chunks
+constexpr int SK_TMEM_COLS = 512;                     // accumulator (<= 64) + A slots
+
+// tcgen05.mma with the A operand in tensor memory: row i of A in lane i, its K
+// values packed two per 32-bit column.
+__device__ __forceinline__ void mma_f16_tmem_a(uint32_t tmem_d, uint32_t tmem_a, uint64_t b,
+                                               uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "setp.ne.u32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+                 ::"r"(tmem_d), "r"(tmem_a), "l"(b), "r"(idesc), "r"(accumulate)
+                 : "memory");
+}
+
+// The same with the B descriptor passed as two 32-bit halves: the issuing loop
+// then steps the start-address field (low half) by 2 per 32 bytes instead of
+// rebuilding a 64-bit descriptor per MMA (one thread issues every MMA, so its
+// instruction count per MMA is on the critical path).
+__device__ __forceinline__ void mma_f16_tmem_a2(uint32_t tmem_d, uint32_t tmem_a, uint32_t b_lo,
+                                                uint32_t b_hi, uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile("{\n\t.reg .b64 bd;\n\t.reg .pred p;\n\t"
+                 "setp.ne.u32 p, %5, 0;\n\t"
+                 "mov.b64 bd, {%2, %3};\n\t"
+                 "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], bd, %4, p;\n\t}"
+                 ::"r"(tmem_d), "r"(tmem_a), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate)
+                 : "memory");
+}
+
+// A warp writes 16 consecutive 32-bit columns of its 32 TMEM lanes (one row each).
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16])
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+                 "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};"
+                 ::"r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]),
+                   "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]),
+                   "r"(v[13]), "r"(v[14]), "r"(v[15])
+                 : "memory");
+}
+
+// Shared-memory layout of the skinny kernel (offsets from the 1024-aligned base):
+// [x tiles: nch x TN x 128 B][code boxes: ceil(nch / 4) x 128 rows x 128 B][barriers],
+// both in the 128-byte swizzle (16-byte unit u of row r stored at u ^ (r % 8)).
+// After the final MMA the split-K dump of the accumulator (TN x 128 fp32) reuses
+// the start.
+struct SkLayout {
+    int nch, nstep, nbox;
+    uint32_t x_bytes, codes_off, bars_off;
+    __host__ __device__ SkLayout(int TN, int nch_)
+    {
+        nch = nch_;
+        nstep = (nch + 1) / 2;                          // steps of two chunks
+        nbox = (nch + 3) / 4;                           // code boxes of four chunks
+        x_bytes = (uint32_t)TN * 128;
+        codes_off = (uint32_t)nch * x_bytes;
+        const uint32_t data = codes_off + (uint32_t)nbox * 16384u;
+        const uint32_t dump = (uint32_t)TN * TC_ROWS * 4;
+        bars_off = ((data > dump ? data : dump) + 7u) & ~7u;
+    }
+    // barriers: cfull[nbox], xfull[nstep], xready[nstep], afull, aempty, done
+    __host__ __device__ uint32_t bytes() const
+    {
+        return bars_off + (uint32_t)(nbox + 2 * nstep + 2 * SK_NA + 1) * 8 + 16;
+    }
+};
+
+template <int LAYOUT>
+__global__ void __launch_bounds__(SK_THREADS, 1)
+q4_tc_skinny_kernel(const __grid_constant__ CUtensorMap xmap,
+                    const __grid_constant__ CUtensorMap wmap, TcParams p)
+{
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    unsigned char *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    const int TN = p.TN;
+    const int tile = blockIdx.x / p.KS;
+    const int ks = blockIdx.x - tile * p.KS;            // rank within the cluster
+    const int n0 = tile * TC_ROWS;
+    const int c0 = (int)((int64_t)ks * p.chunks / p.KS);
+    const SkLayout L(TN, (int)((int64_t)(ks + 1) * p.chunks / p.KS) - c0);
+    const int nch = L.nch, nstep = L.nstep, nbox = L.nbox;
+    const uint32_t x_bytes = L.x_bytes;
+    unsigned char *xs = smem;
+    unsigned char *cs = smem + L.codes_off;
+    uint64_t *cfull = reinterpret_cast<uint64_t *>(smem + L.bars_off);   // per code box
+    uint64_t *xfull = cfull + nbox;
+    uint64_t *xready = xfull + nstep;
+    uint64_t *afull = xready + nstep;
+    uint64_t *aempty = afull + SK_NA;
+    uint64_t *done = aempty + SK_NA;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(done + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        TC_TRACE(0);
+        for (int i = 0; i < nbox; ++i)
+            mbar_init(smem_u32(&cfull[i]), 1);
+        for (int st = 0; st < nstep; ++st) {
+            mbar_init(smem_u32(&xfull[st]), 1);
+            mbar_init(smem_u32(&xready[st]), SK_XWARPS);
+        }
+        for (int i = 0; i < SK_NA; ++i) {
+            mbar_init(smem_u32(&afull[i]), TC_WORKERS);
+            mbar_init(smem_u32(&aempty[i]), 1);
+        }
+        mbar_init(smem_u32(done), 1);
+        mbar_init_fence();
+        // The codes of the whole K range, requested at once and before the
+        // dependency wait (weights do not depend on the previous kernel): boxes
+        // of four chunks, 128 rows x 128 bytes, rows beyond N zero-filled.
+        for (int b = 0; b < nbox; ++b) {
+            mbar_arrive_expect_tx(smem_u32(&cfull[b]), 16384u);
+            tma_load_2d(smem_u32(cs + (size_t)b * 16384), &wmap, (c0 + 4 * b) * (TC_KC / 2), n0,
+                        smem_u32(&cfull[b]));
+        }
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                     ::"r"(smem_u32(tmem_slot)), "r"(SK_TMEM_COLS) : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    if (threadIdx.x == 0) TC_TRACE(1);
+    float gsc = 1.f;                                    // read before the dependency wait:
+    if constexpr (LAYOUT == 1)                          // the global scale is a weight
+        gsc = __ldg(p.gscale);
+
+    if (warp == 0) {
+        // ---------------------------------------------- launch the next kernel early
+        pdl_launch_dependents();
+    } else if (warp == 1) {
+        // ------------------------------------------------------------- MMA issue
+        // accumulator in TMEM columns 0 .. TN-1; A slot i in columns 64 + 64 i
+        // (chunk h of the step at + 32 h, k-step kk at + 8 kk)
+        if (lane == 0) {
+            const uint32_t idesc = idesc_f16(TN);
+            int sl = 0;
+            uint32_t ph = 0;
+            for (int s = 0; s < nstep; ++s) {
+                if (!mbar_wait(smem_u32(&afull[sl]), ph, p.err))
+                    break;
+                if (s < 16) TC_TRACE(24 + s);
+                if (!mbar_wait(smem_u32(&xready[s]), 0, p.err))
+                    break;
+                if (s < 16) TC_TRACE(8 + s);
+                tc_fence_after();
+                const uint32_t a = tmem_base + 64u + 64u * (uint32_t)sl;
+                const uint64_t bd = smem_desc_sw128(smem_u32(xs + (size_t)(2 * s) * x_bytes));
+                const uint32_t blo = (uint32_t)bd, bhi = (uint32_t)(bd >> 32);
+#pragma unroll
+                for (int kk = 0; kk < TC_KC / 16; ++kk)        // chunk 2s: +32 bytes per k-step
+                    mma_f16_tmem_a2(tmem_base, a + 8u * kk, blo + 2u * kk, bhi, idesc,
+                                    (s > 0 || kk > 0) ? 1u : 0u);
+                if (nch - 2 * s >= 2)                         // chunk 2s + 1: one x chunk on
+#pragma unroll
+                    for (int kk = 0; kk < TC_KC / 16; ++kk)
+                        mma_f16_tmem_a2(tmem_base, a + 32u + 8u * kk,
+                                        blo + (x_bytes >> 4) + 2u * kk, bhi, idesc, 1u);
+                mma_commit(smem_u32(&aempty[sl]));
+                if (s < 16) TC_TRACE(40 + s);
+                if (++sl == SK_NA) {
+                    sl = 0;
+                    ph ^= 1u;
                 }
-            } else {
-                float *dst = p.ws + ((size_t)(tile * p.KS + ks) * TN + cb) * TC_ROWS + r;
+            }
+            mma_commit(smem_u32(done));
+        }
+        // free the accumulator as soon as every worker has read it back
+        __syncwarp();
+        asm volatile("bar.sync 3, %0;" ::"r"((TC_WORKERS + 1) * 32) : "memory");
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;"
+                     ::"r"(tmem_base), "r"(SK_TMEM_COLS) : "memory");
+    } else if (warp >= 2 + TC_WORKERS) {
+        // ------------------------------------------------------ x load + convert
+        // x comes from the previous kernel, so these warps wait for it.  Lane 0 of
+        // x warp i then requests the steps i, i + 8, ...: one tensor copy per x
+        // chunk (TN token rows x 128 bytes, 128-byte swizzle, rows beyond M zero)
+        // -- spread over eight issuing warps, the copies overlap instead of queuing
+        // behind one thread.  All eight warps convert each step bf16 -> fp16 in
+        // place once it lands.  A value outside the fp16 range sets
+        // Q4_DEVERR_FP16_RANGE.
+        const int xw = warp - (2 + TC_WORKERS);
+        const int xt = xw * 32 + lane;
+        pdl_wait();
+        if (lane == 0)
+            for (int st = xw; st < nstep; st += SK_XWARPS) {
+                const int nv = nch - 2 * st < 2 ? 1 : 2;
+                mbar_arrive_expect_tx(smem_u32(&xfull[st]), (uint32_t)nv * x_bytes);
+                for (int h = 0; h < nv; ++h)
+                    tma_load_2d(smem_u32(xs + (size_t)(2 * st + h) * x_bytes), &xmap,
+                                (c0 + 2 * st + h) * TC_KC, 0, smem_u32(&xfull[st]));
+            }
+        if (xt == 0) TC_TRACE(4);
+        bool range_bad = false;
+        for (int st = 0; st < nstep; ++st) {
+            if (!mbar_wait_warp(smem_u32(&xfull[st]), 0, p.err))
+                break;
+            if (xt == 0 && st == 0) TC_TRACE(6);
+            if (xt == 0 && st == nstep - 1) TC_TRACE(61);
+            const int nvec = (nch - 2 * st < 2 ? 1 : 2) * TN * 8;
+            uint4 *xv = reinterpret_cast<uint4 *>(xs + (size_t)(2 * st) * x_bytes);
+            for (int v = xt; v < nvec; v += SK_XWARPS * 32) {
+                const uint4 e4 = xv[v];
+                const uint32_t ev[4] = {e4.x, e4.y, e4.z, e4.w};
+                uint32_t o[4];
+                float mx = 0.f;
 #pragma unroll
-                for (int j = 0; j < 16; ++j)
-                    dst[(size_t)j * TC_ROWS] = __uint_as_float(v[j]);
+                for (int q = 0; q < 4; ++q) {
+                    const float lo = bf16_bits_to_f32(ev[q] & 0xffffu);
+                    const float hi = bf16_bits_to_f32(ev[q] >> 16);
+                    mx = fmaxf(mx, fmaxf(fabsf(lo), fabsf(hi)));
+                    __half2 hh = __floats2half2_rn(lo, hi);
+                    o[q] = *reinterpret_cast<uint32_t *>(&hh);
+                }
+                if (mx >= 65520.f && mx <= 3.4e38f)
+                    range_bad = true;
+                xv[v] = make_uint4(o[0], o[1], o[2], o[3]);
+            }
+            fence_proxy_async();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(smem_u32(&xready[st]));
+            if (xt == 0 && st == 0) TC_TRACE(7);
+        }
+        if (range_bad && p.err)
+            atomicOr(p.err, kErrFp16Range);
+        // every copy this warp requested has landed before the CTA can exit
+        if (lane == 0)
+            for (int st = xw; st < nstep; st += SK_XWARPS)
+                mbar_wait(smem_u32(&xfull[st]), 0, p.err);
+    } else {
+        // ------------------------------------------------------------- workers
+        // A step is two chunks (128 columns).  Warp w may write only TMEM lane
+        // quadrant w % 4, so it owns rows 32 (w % 4) + lane; the four warps of a
+        // quadrant split the step's columns: g = (w - 2) / 4 takes columns
+        // 32 g .. + 31 (chunk g / 2, half g % 2).  A thread reads 16 bytes of its
+        // row's codes, dequantises 32 weights and writes them as 16 packed columns
+        // of its lane.
+        const int w = warp - 2;                  // 0..15
+        const int quad = warp & 3;
+        const int g = w >> 2;
+        const int h = g >> 1;
+        const int half = g & 1;
+        const int row = quad * 32 + lane;
+        const bool rok = n0 + row < p.N;
+        const int64_t n = n0 + row;
+        const uint32_t t_lane = (uint32_t)(quad * 32) << 16;
+        // int4: scale | min << 16 of the thread's group; NVFP4: the e4m3 scales of
+        // its two 16-column groups (low byte first)
+        auto load_scale = [&](int s) -> uint32_t {
+            const int j = 2 * s + h;
+            if (!rok || j >= nch)
+                return 0u;
+            const int kc = c0 + j;
+            if constexpr (LAYOUT == 0) {
+                const int64_t gi = n * (p.K / 128) + kc / 2;
+                return ld_nc_u16_r32(static_cast<const uint16_t *>(p.scale) + gi) |
+                       (ld_nc_u16_r32(p.minv + gi) << 16);
+            } else {
+                return ld_nc_u16_r32(static_cast<const uint8_t *>(p.scale) + n * (p.K / 16) + kc * 4 +
+                                     2 * half);
+            }
+        };
+        int sl = 0;                              // A slot of the step
+        uint32_t ph = 0;                         // parity of the slot's current use
+        TC_PHASE_DECL;
+        // one step; false when a wait timed out
+        auto step = [&](int s, uint32_t sc) -> bool {
+            TC_CLK(t0);
+            if (s >= SK_NA && !mbar_wait_warp(smem_u32(&aempty[sl]), ph ^ 1u, p.err))
+                return false;
+            TC_CLK(t1);
+            TC_PHASE(56, t0, t1);
+            if ((s & 1) == 0 && !mbar_wait_warp(smem_u32(&cfull[s >> 1]), 0, p.err))
+                return false;
+            tc_fence_after();
+            TC_CLK(t2);
+            TC_PHASE(57, t1, t2);
+            if (2 * s + h < nch) {
+                // unit 4 (s % 2) + g of the row in the box, stored at unit ^ (row % 8)
+                const uint4 cw = *reinterpret_cast<const uint4 *>(
+                    cs + (size_t)(s >> 1) * 16384 + row * 128 + (((4 * (s & 1) + g) ^ (row & 7)) << 4));
+                uint32_t lo[8], hi[8];
+                tc_decode16<LAYOUT>(make_uint2(cw.x, cw.y), sc, lo);
+                tc_decode16<LAYOUT>(make_uint2(cw.z, cw.w), LAYOUT == 0 ? sc : (sc >> 8), hi);
+                const uint32_t v[16] = {lo[0], lo[1], lo[2], lo[3], lo[4], lo[5], lo[6], lo[7],
+                                        hi[0], hi[1], hi[2], hi[3], hi[4], hi[5], hi[6], hi[7]};
+                tmem_st16(tmem_base + t_lane + 64u + 64u * (uint32_t)sl + 32u * h + 16u * half, v);
+            }
+            TC_CLK(t3);
+            TC_PHASE(58, t2, t3);
+            asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(smem_u32(&afull[sl]));
+            if (++sl == SK_NA) {
+                sl = 0;
+                ph ^= 1u;
+            }
+            TC_CLK(t4);
+            TC_PHASE(59, t3, t4);
+            return true;
+        };
+        // Scales run eight steps ahead in two register sets that take turns, each
+        // refilled right after its value is used: no register moves, so no wait on
+        // a load that is still in flight.
+        uint32_t sa[4], sb[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            sa[i] = load_scale(i);
+            sb[i] = load_scale(4 + i);
+        }
+        bool alive = true;
+        for (int g8 = 0; g8 < nstep && alive; g8 += 8) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                if (alive && g8 + i < nstep)
+                    alive = step(g8 + i, sa[i]);
+                sa[i] = load_scale(g8 + 8 + i);
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                if (alive && g8 + 4 + i < nstep)
+                    alive = step(g8 + 4 + i, sb[i]);
+                sb[i] = load_scale(g8 + 12 + i);
             }
         }
-        if (p.KS > 1) {
-            // split-K: the last CTA of this tile to arrive sums the partials (every
-            // worker reaches both barriers, whatever happened before)
-            __threadfence();
-            asm volatile("bar.sync 2, %0;" ::"r"(TC_WORKERS * 32) : "memory");
-            __shared__ unsigned last_flag;
-            if (w == 0 && lane == 0)
-                last_flag = (ok && atomicAdd(&p.tickets[tile], 1u) == (unsigned)(p.KS - 1)) ? 1u : 0u;
-            asm volatile("bar.sync 2, %0;" ::"r"(TC_WORKERS * 32) : "memory");
-            if (last_flag) {
-                __threadfence();
-                // Each thread sums groups of four rows of one token column: all KS
-                // partials of a group are loaded (16 bytes each) before the adds,
-                // which run in k order, so the result does not depend on timing.
-                const size_t kstride4 = (size_t)TN * TC_ROWS / 4;
-                const float4 *part = reinterpret_cast<const float4 *>(
-                    p.ws + (size_t)tile * p.KS * TN * TC_ROWS);
-                for (int g4 = w * 32 + lane; g4 < TN * (TC_ROWS / 4); g4 += TC_WORKERS * 32) {
-                    const int c = g4 / (TC_ROWS / 4), q = g4 % (TC_ROWS / 4);
-                    float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
-                    for (int k0 = 0; k0 < p.KS; k0 += 8) {
-                        float4 v[8];
+        TC_PHASE_STORE();
+        // every code copy has landed before the CTA can exit (the steps wait for
+        // them; this covers a step loop that stopped early)
+        if (warp == 2 && lane == 0)
+            for (int b = 0; b < nbox; ++b)
+                mbar_wait(smem_u32(&cfull[b]), 0, p.err);
+
+        // ------------------------------------------------------------ epilogue
+        // warp w reads TMEM lane quadrant (w + 2) % 4, columns 16 (w / 4) .. + 15
+        const bool ok = mbar_wait_warp(smem_u32(done), 0, p.err);
+        tc_fence_after();
+        if (warp == 2 && lane == 0) TC_TRACE(2);
+        const int cb = g * 16;
+        const int r = row;
+        uint32_t v[16];
+        if (cb < TN)
+            tmem_ld16(tmem_base + t_lane + (uint32_t)cb, v);
+        tc_fence_before();
+        asm volatile("bar.arrive 3, %0;" ::"r"((TC_WORKERS + 1) * 32) : "memory");
+        if (ok && cb < TN) {
+            if (p.KS == 1) {
+                if (n0 + r < p.N)
 #pragma unroll
-                        for (int j = 0; j < 8; ++j)
-                            if (k0 + j < p.KS)
-                                v[j] = __ldcg(part + (k0 + j) * kstride4 + (size_t)c * (TC_ROWS / 4) + q);
+                    for (int j = 0; j < 16; ++j)
+                        if (cb + j < p.M)
+                            p.y[(int64_t)(cb + j) * p.N + n0 + r] =
+                                f32_to_bf16_bits(__uint_as_float(v[j]) * gsc);
+            } else {
+                // x and codes are idle once the final commit has been seen
+                float *dump = reinterpret_cast<float *>(smem);
 #pragma unroll
-                        for (int j = 0; j < 8; ++j)
-                            if (k0 + j < p.KS) {
-                                sum.x += v[j].x; sum.y += v[j].y;
-                                sum.z += v[j].z; sum.w += v[j].w;
-                            }
-                    }
-                    const int m = m0 + c;
-                    const int nb = n0 + 4 * q;
-                    if (m < p.M) {
-                        uint16_t *yr = p.y + (int64_t)m * p.N;
-                        const float o[4] = {sum.x, sum.y, sum.z, sum.w};
-#pragma unroll
-                        for (int i = 0; i < 4; ++i)
-                            if (nb + i < p.N)
-                                yr[nb + i] = f32_to_bf16_bits(o[i] * gsc);
-                    }
-                }
-                if (w == 0 && lane == 0)
-                    p.tickets[tile] = 0u;
+                for (int j = 0; j < 16; ++j)
+                    dump[(cb + j) * TC_ROWS + r] = __uint_as_float(v[j]);
             }
         }
     }
 
-    __syncthreads();
+    if (p.KS > 1) {
+        // Sum this CTA's share of the tile over the KS accumulators of the cluster.
+        __syncwarp();
+        cluster_sync_all();                      // every dump of the cluster is written
+        if (threadIdx.x == 0) TC_TRACE(5);
+        const int e4 = TN * (TC_ROWS / 4);       // float4 groups of the tile
+        const int g0 = (int)((int64_t)ks * e4 / p.KS);
+        const int g1 = (int)((int64_t)(ks + 1) * e4 / p.KS);
+        const uint32_t base = smem_u32(smem);
+        for (int g = g0 + (int)threadIdx.x; g < g1; g += SK_THREADS) {
+            float4 part[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                if (k < p.KS)
+                    part[k] = ld_cluster_f4(base + (uint32_t)g * 16u, (uint32_t)k);
+            float4 sum = part[0];
+#pragma unroll
+            for (int k = 1; k < 8; ++k)
+                if (k < p.KS) {
+                    sum.x += part[k].x; sum.y += part[k].y;
+                    sum.z += part[k].z; sum.w += part[k].w;
+                }
+            const int m = g / (TC_ROWS / 4);
+            const int nb = n0 + 4 * (g % (TC_ROWS / 4));
+            if (m < p.M) {
+                uint16_t *yr = p.y + (int64_t)m * p.N + nb;
+                const uint16_t o[4] = {f32_to_bf16_bits(sum.x * gsc), f32_to_bf16_bits(sum.y * gsc),
+                                       f32_to_bf16_bits(sum.z * gsc), f32_to_bf16_bits(sum.w * gsc)};
+                if (nb + 3 < p.N && (reinterpret_cast<uintptr_t>(yr) & 7u) == 0) {
+                    *reinterpret_cast<uint2 *>(yr) =
+                        make_uint2(o[0] | ((uint32_t)o[1] << 16), o[2] | ((uint32_t)o[3] << 16));
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        if (nb + i < p.N)
+                            yr[i] = o[i];
+                }
+            }
+        }
+        cluster_sync_all();                      // no CTA leaves while its dump is read
+    }
     if (threadIdx.x == 0) TC_TRACE(3);
 }
 
@@ -683,6 +1224,99 @@ size_t tc_workspace_bytes(int M, int N, int K, int sms)
     return tc_xf16_bytes(M, K) + tc_split_bytes(M, N, K, sms);
 }
 
+// Skinny plan: tiles of at most 64 tokens whose K range, split into at most
+// eight parts (one cluster of at most eight CTAs per weight tile), keeps all its
+// codes and x chunks resident in shared memory (the A tiles live in TMEM).
+struct TcSkinnyPlan {
+    int ks = 0, ncmax = 0;
+    size_t smem = 0;
+};
+
+static size_t tc_skinny_smem(int TN, int nch)
+{
+    return 1024 /* alignment of the base */ + SkLayout(TN, nch).bytes();
+}
+
+static bool tc_skinny_plan(const DeviceInfo &dev, int M, int N, int K, TcSkinnyPlan &sp)
+{
+    const int TN = tc_tn(M);
+    if (TN > 64 || K % TC_KC)
+        return false;
+    const int chunks = K / TC_KC;
+    const int64_t tiles = (N + TC_ROWS - 1) / TC_ROWS;
+    // the smallest split that fits, then more CTAs -- they pull more bandwidth --
+    // while the grid stays one wave and every CTA keeps at least four chunks
+    for (int ks = 1; ks <= 8 && ks <= chunks; ++ks) {
+        if (tc_skinny_smem(TN, (chunks + ks - 1) / ks) > dev.smem_optin)
+            continue;
+        while (ks < 8 && tiles * (ks + 1) <= dev.sms && chunks / (ks + 1) >= 4)
+            ++ks;
+        sp.ks = ks;
+        sp.ncmax = (chunks + ks - 1) / ks;
+        sp.smem = tc_skinny_smem(TN, sp.ncmax);
+        return true;
+    }
+    return false;
+}
+
+// Whether a cluster of ks CTAs of this size can be resident at all (cached).
+static bool tc_cluster_fits(const void *k, int device, int ks, size_t smem)
+{
+    struct Entry {
+        const void *k;
+        int device, ks;
+        size_t smem;
+        bool ok;
+    };
+    static std::mutex mu;
+    static Entry cache[64];
+    static int used = 0;
+    std::lock_guard<std::mutex> g(mu);
+    for (int i = 0; i < used; ++i)
+        if (cache[i].k == k && cache[i].device == device && cache[i].ks == ks && cache[i].smem == smem)
+            return cache[i].ok;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)ks);
+    cfg.blockDim = dim3(SK_THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute a[1];
+    a[0].id = cudaLaunchAttributeClusterDimension;
+    a[0].val.clusterDim.x = (unsigned)ks;
+    a[0].val.clusterDim.y = 1;
+    a[0].val.clusterDim.z = 1;
+    cfg.attrs = a;
+    cfg.numAttrs = 1;
+    int n = 0;
+    const bool ok = cudaOccupancyMaxActiveClusters(&n, k, &cfg) == cudaSuccess && n > 0;
+    cudaGetLastError();
+    if (used < 64)
+        cache[used++] = {k, device, ks, smem, ok};
+    return ok;
+}
+
+static CUresult tc_encode_maps(EncodeTiledFn enc, CUtensorMap &xmap, CUtensorMap &wmap,
+                               const void *xsrc, bool x_f16, const uint8_t *codes, int M, int N,
+                               int K, int TN, int code_box_bytes, bool code_swizzle)
+{
+    cuuint64_t xd[2] = {(cuuint64_t)K, (cuuint64_t)M};
+    cuuint64_t xstr[1] = {(cuuint64_t)K * 2};
+    cuuint32_t xbox[2] = {TC_KC, (cuuint32_t)TN};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(&xmap, x_f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                     2, const_cast<void *>(xsrc), xd, xstr, xbox, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return r;
+    cuuint64_t wd[2] = {(cuuint64_t)K / 2, (cuuint64_t)N};
+    cuuint64_t wstr[1] = {(cuuint64_t)K / 2};
+    cuuint32_t wbox[2] = {(cuuint32_t)code_box_bytes, TC_ROWS};
+    return enc(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(codes), wd, wstr, wbox,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               code_swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
 template <int LAYOUT>
 static const void *tc_select_layout(int sc, int groups)
 {
@@ -702,7 +1336,8 @@ static const void *tc_select(int kind, int sc, int groups)
 
 q4_status tc_launch(int kind, const void *x, const uint8_t *codes, const void *scale,
                     const void *minv, const float *gscale, void *y, int M, int N, int K,
-                    void *ws, size_t ws_bytes, cudaStream_t stream, bool pdl)
+                    void *ws, size_t ws_bytes, cudaStream_t stream, bool pdl,
+                    bool skinny)
 {
     DeviceInfo dev;
     q4_status s = current_device(dev);
@@ -733,6 +1368,53 @@ q4_status tc_launch(int kind, const void *x, const uint8_t *codes, const void *s
     while (cols < p.TN)
         cols *= 2;
     p.tmem_cols = cols;
+    TcSkinnyPlan sp;
+    if (skinny && tc_skinny_plan(dev, M, N, K, sp)) {
+        const void *k = kind == W_INT4 ? reinterpret_cast<const void *>(&q4_tc_skinny_kernel<0>)
+                                       : reinterpret_cast<const void *>(&q4_tc_skinny_kernel<1>);
+        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)sp.smem);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "cudaFuncSetAttribute(skinny tensor-core kernel)");
+        if (sp.ks == 1 || tc_cluster_fits(k, dev.device, sp.ks, sp.smem)) {
+            p.KS = sp.ks;
+            p.ns = SK_NA;
+            p.tmem_cols = SK_TMEM_COLS;
+            p.x_f16 = 0;
+            p.x = static_cast<const uint16_t *>(x);
+            CUtensorMap xmap, wmap;
+            const CUresult r = tc_encode_maps(enc, xmap, wmap, x, false, codes, M, N, K, p.TN,
+                                              2 * TC_KC, true);
+            if (r != CUDA_SUCCESS)
+                return fail(Q4_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3((unsigned)(((N + TC_ROWS - 1) / TC_ROWS) * sp.ks));
+            cfg.blockDim = dim3(SK_THREADS);
+            cfg.dynamicSmemBytes = sp.smem;
+            cfg.stream = stream;
+            cudaLaunchAttribute a[2];
+            unsigned na = 0;
+            if (pdl) {
+                a[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+                a[na].val.programmaticStreamSerializationAllowed = 1;
+                ++na;
+            }
+            if (sp.ks > 1) {
+                a[na].id = cudaLaunchAttributeClusterDimension;
+                a[na].val.clusterDim.x = (unsigned)sp.ks;
+                a[na].val.clusterDim.y = 1;
+                a[na].val.clusterDim.z = 1;
+                ++na;
+            }
+            cfg.attrs = na ? a : nullptr;
+            cfg.numAttrs = na;
+            void *args[] = {&xmap, &wmap, &p};
+            e = cudaLaunchKernelExC(&cfg, k, args);
+            if (e != cudaSuccess)
+                return cuda_fail(e, "launch of the skinny tensor-core kernel");
+            return Q4_OK;
+        }
+    }
     const size_t need = tc_workspace_bytes(M, N, K, dev.sms);
     if (need > ws_bytes)
         return fail(Q4_ERR_WORKSPACE, "tensor-core path needs %zu bytes of workspace", need);
@@ -799,30 +1481,10 @@ q4_status tc_launch(int kind, const void *x, const uint8_t *codes, const void *s
 
     CUtensorMap xmap, wmap;
     {
-        cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
-        cuuint64_t strides[1] = {(cuuint64_t)K * 2};
-        cuuint32_t box[2] = {TC_KC, (cuuint32_t)p.TN};
-        cuuint32_t estr[2] = {1, 1};
-        CUresult r = enc(&xmap, p.x_f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
-                                        : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
-                         2, const_cast<void *>(xsrc), dims,
-                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        const CUresult r = tc_encode_maps(enc, xmap, wmap, xsrc, p.x_f16 != 0, codes, M, N, K, p.TN,
+                                          sc * TC_KC / 2, false);
         if (r != CUDA_SUCCESS)
-            return fail(Q4_ERR_CUDA, "cuTensorMapEncodeTiled(x) failed (%d)", (int)r);
-    }
-    {
-        cuuint64_t dims[2] = {(cuuint64_t)K / 2, (cuuint64_t)N};
-        cuuint64_t strides[1] = {(cuuint64_t)K / 2};
-        cuuint32_t box[2] = {(cuuint32_t)(sc * TC_KC / 2), TC_ROWS};   // SC chunks of codes
-        cuuint32_t estr[2] = {1, 1};
-        CUresult r = enc(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(codes),
-                         dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                         CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-        if (r != CUDA_SUCCESS)
-            return fail(Q4_ERR_CUDA, "cuTensorMapEncodeTiled(codes) failed (%d)", (int)r);
+            return fail(Q4_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
     }
     // two worker groups, two stages dequantised at once (measured: prefill
     // GEMMs 5-22% faster than one group of 16 warps; batched decode unchanged)

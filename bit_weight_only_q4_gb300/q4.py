@@ -22,6 +22,7 @@ LAYOUT_NVFP4 = 1
 FLAG_PDL = 0x1
 FLAG_FORCE_CUDA_CORE = 0x2
 FLAG_FORCE_TENSOR_CORE = 0x4
+FLAG_TC_SKINNY = 0x8
 
 STATUS = {0: "Q4_OK", 1: "Q4_ERR_NULL", 2: "Q4_ERR_SHAPE", 3: "Q4_ERR_ALIGN",
           4: "Q4_ERR_WORKSPACE", 5: "Q4_ERR_ARG", 6: "Q4_ERR_CUDA", 7: "Q4_ERR_DEVICE"}

@@ -61,10 +61,15 @@ typedef enum {
  *     by the immediately preceding kernel.  Activations, outputs and workspace
  *     are touched only after the previous kernel has completed.
  *   Q4_FLAG_FORCE_CUDA_CORE / Q4_FLAG_FORCE_TENSOR_CORE: override the choice of
- *     kernel by M (testing and benchmarking only). */
+ *     kernel by M (testing and benchmarking only).
+ *   Q4_FLAG_TC_SKINNY: on the tensor-core path, run tiles of at most 64 tokens
+ *     on the skinny kernel (whole K range resident, A operand in tensor memory,
+ *     cluster split-K) instead of the staged-ring kernel.  Experimental: on
+ *     GB300 it is slower than the default at the sizes measured. */
 #define Q4_FLAG_PDL 0x1u
 #define Q4_FLAG_FORCE_CUDA_CORE 0x2u
 #define Q4_FLAG_FORCE_TENSOR_CORE 0x4u
+#define Q4_FLAG_TC_SKINNY 0x8u
 
 int q4_abi_version(void);
 const char *q4_status_string(q4_status s);

@@ -49,19 +49,25 @@ def _mat(layout, rng, N, K):
     return synth.int4_matrix(rng, N, K) if layout == "int4" else synth.nvfp4_matrix(rng, N, K)
 
 
+@pytest.mark.parametrize("skinny", [False, True])
 @pytest.mark.parametrize("layout", ["int4", "nvfp4"])
 @pytest.mark.parametrize("M,N,K", [(16, 128, 128), (1, 128, 128), (5, 200, 256), (48, 1000, 640),
                                    (64, 384, 1024), (200, 130, 2048), (300, 256, 384),
-                                   (17, 8192, 128), (48, 96, 8192)])
-def test_forced_tensor_core_shapes(q4, oracle_mod, layout, M, N, K):
+                                   (17, 8192, 128), (48, 96, 8192), (8, 512, 2048),
+                                   (33, 2049, 8192), (64, 2048, 8192), (16, 16384, 2048)])
+def test_forced_tensor_core_shapes(q4, oracle_mod, layout, M, N, K, skinny):
+    """The staged-ring kernel on every shape; with the skinny flag, tiles of up to
+    64 tokens take the skinny kernel (cluster split-K up to eight CTAs)."""
     if layout == "int4" and K % 128:
         pytest.skip("int4 needs K % 128")
+    if skinny and M > 64:
+        pytest.skip("tiles of more than 64 tokens always take the ring kernel")
     rng = synth.rng_for(300, M, N, K)
     w = _mat(layout, rng, N, K)
     x = synth.activations(rng, M, K)
-    y = _run(q4, layout, x, w, q4.FLAG_FORCE_TENSOR_CORE)
+    y = _run(q4, layout, x, w, q4.FLAG_FORCE_TENSOR_CORE | (q4.FLAG_TC_SKINNY if skinny else 0))
     yo, ao = _oracle(oracle_mod, layout, x, w)
-    P.check(y, yo, ao, f"tc {layout} M={M} N={N} K={K}")
+    P.check(y, yo, ao, f"tc {layout} M={M} N={N} K={K} skinny={skinny}")
 
 
 @pytest.mark.parametrize("layout", ["int4", "nvfp4"])
@@ -89,13 +95,28 @@ def test_prefill_2048_tokens_sampled_rows(q4, oracle_mod, layout, shape_index):
             f"prefill {layout} shape {shape_index}")
 
 
-def test_tensor_core_is_deterministic(q4):
+@pytest.mark.parametrize("skinny", [False, True])
+def test_tensor_core_is_deterministic(q4, skinny):
+    """Split-K sums run in k order in both kernels: repeated calls are bit-identical."""
     rng = synth.rng_for(303)
     w = synth.nvfp4_matrix(rng, 2048, 8192)
     x = synth.activations(rng, 48, 8192)
-    y1 = _run(q4, "nvfp4", x, w, 0)
-    y2 = _run(q4, "nvfp4", x, w, 0)
-    assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))
+    flags = q4.FLAG_TC_SKINNY if skinny else 0
+    y1 = _run(q4, "nvfp4", x, w, flags)
+    for _ in range(3):
+        y2 = _run(q4, "nvfp4", x, w, flags)
+        assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))
+
+
+@pytest.mark.parametrize("layout", ["int4", "nvfp4"])
+def test_skinny_and_ring_kernels_agree(q4, layout):
+    """The two tensor-core kernels differ only in the order of the split-K sums."""
+    rng = synth.rng_for(305)
+    w = _mat(layout, rng, 2048, 8192)
+    x = synth.activations(rng, 40, 8192)
+    a = _run(q4, layout, x, w, q4.FLAG_TC_SKINNY).float()
+    b = _run(q4, layout, x, w, 0).float()
+    assert float((a - b).norm() / b.norm()) < 1e-3
 
 
 def test_fp16_range_flag(q4):
@@ -114,7 +135,6 @@ def test_fp16_range_flag(q4):
         q4.set_launch_flags(0)
     torch.cuda.synchronize()
     assert q4.device_error_flags() & 0x2
-    y = q4.q4_linear_int4g128(P.bf16_dev(x), *P.int4_dev(w), ) if False else None
     q4.set_launch_flags(q4.FLAG_FORCE_CUDA_CORE)
     try:
         y = q4.q4_linear_int4g128(P.bf16_dev(x), *P.int4_dev(w))
