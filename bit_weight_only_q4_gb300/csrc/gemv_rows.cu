@@ -168,11 +168,17 @@ __device__ __forceinline__ void rows_dot(const uint4 qv, uint32_t swr,
             out[m] = t * cd[m].x;
         }
     } else {
-        float Ta[MT], Tb[MT];
+        // NVFP4: each 16-column group (two words) is summed in fp16 -- eight exact
+        // products (E2M1 x prescaled x, at most 10 significant bits) per half, one
+        // rounding per add, magnitude below 2^16 by the prescale -- then the two
+        // halves go to fp32 and meet the group scale.  Packed fp16 FMAs take one
+        // instruction per two weights where fp32 accumulation of fp16 products
+        // takes two per weight.
+        uint32_t Ha[MT], Hb[MT];
 #pragma unroll
         for (int m = 0; m < MT; ++m) {
-            Ta[m] = 0.f;
-            Tb[m] = 0.f;
+            Ha[m] = 0u;
+            Hb[m] = 0u;
         }
 #pragma unroll
         for (int jj = 0; jj < 4; ++jj) {
@@ -183,9 +189,9 @@ __device__ __forceinline__ void rows_dot(const uint4 qv, uint32_t swr,
 #pragma unroll
                 for (int m = 0; m < MT; ++m) {
                     if (jj < 2)
-                        Ta[m] = fma2_f16(Ta[m], hh[q], xr[m][4 * jj + q]);
+                        Ha[m] = hfma2_rn(hh[q], xr[m][4 * jj + q], Ha[m]);
                     else
-                        Tb[m] = fma2_f16(Tb[m], hh[q], xr[m][4 * jj + q]);
+                        Hb[m] = hfma2_rn(hh[q], xr[m][4 * jj + q], Hb[m]);
                 }
             }
         }
@@ -193,8 +199,11 @@ __device__ __forceinline__ void rows_dot(const uint4 qv, uint32_t swr,
         const float sa = f16lo_to_f32(s2);
         const float sb = f16hi_to_f32(s2);
 #pragma unroll
-        for (int m = 0; m < MT; ++m)
-            out[m] = fmaf(Ta[m], sa, Tb[m] * sb) * cd[m].x;
+        for (int m = 0; m < MT; ++m) {
+            const float ta = f16lo_to_f32(Ha[m]) + f16hi_to_f32(Ha[m]);
+            const float tb = f16lo_to_f32(Hb[m]) + f16hi_to_f32(Hb[m]);
+            out[m] = fmaf(ta, sa, tb * sb) * cd[m].x;
+        }
     }
 }
 

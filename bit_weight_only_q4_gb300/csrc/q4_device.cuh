@@ -120,6 +120,14 @@ __device__ __forceinline__ float fma2_f16(float acc, uint32_t a, uint32_t b)
     return acc;
 }
 
+// Packed fp16 fused multiply-add: c + a * b per half, one rounding each.
+__device__ __forceinline__ uint32_t hfma2_rn(uint32_t a, uint32_t b, uint32_t c)
+{
+    uint32_t r;
+    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(c));
+    return r;
+}
+
 // ------------------------------------------------------ NVFP4 decoding
 // One byte of two E2M1 codes (low nibble = even column) -> f16x2 (exact).
 __device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte_lo8)
