@@ -295,6 +295,33 @@ q4_rows_kernel(GemvParams p)
     const int64_t colbyte = (WK == W_BF16) ? (int64_t)col0 * 2
                             : (WK == W_INT8) ? (int64_t)col0 : (int64_t)(col0 / 2);
 
+    // Ring rows are requested strictly in order (jr = 0, 1, 2, ...).  The linear
+    // layers map logical row n to physical row n, so their weight and scale
+    // pointers simply advance by G rows per request (two 64-bit adds) instead of
+    // being recomputed from the row index; the head keeps the row mapping.
+    constexpr bool kStep = WK != W_BF16;
+    const uint8_t *wnext = p.w;                   // weights of the next ring row
+    const uint8_t *snext = nullptr;               // its scale bytes (int4: scale, min)
+    int64_t wstep = 0, sstep = 0, mdiff = 0;
+    if constexpr (kStep) {
+        const int64_t prow = (int64_t)p.row_begin + n0 + g + G * REG;
+        wnext = p.w + prow * p.w_row_bytes + colbyte;
+        wstep = (int64_t)G * p.w_row_bytes;
+        if constexpr (WK == W_INT4) {
+            const int64_t gi = prow * (p.K >> 7) + (col0 >> 7);
+            snext = reinterpret_cast<const uint8_t *>(static_cast<const uint16_t *>(p.scale) + gi);
+            mdiff = reinterpret_cast<const uint8_t *>(p.minv) -
+                    reinterpret_cast<const uint8_t *>(p.scale);
+            sstep = (int64_t)G * (p.K >> 7) * 2;
+        } else if constexpr (WK == W_NVFP4_A16) {
+            snext = static_cast<const uint8_t *>(p.scale) + prow * (p.K >> 4) + (col0 >> 4);
+            sstep = (int64_t)G * (p.K >> 4);
+        } else {
+            snext = reinterpret_cast<const uint8_t *>(static_cast<const uint16_t *>(p.scale) + prow);
+            sstep = (int64_t)G * 2;
+        }
+    }
+
     // Request ring row jr (row j = REG + jr of this warp) into ring slot `slot`
     // (one commit group per call, empty past the last row, so wait_group counts
     // stay uniform).
@@ -304,11 +331,23 @@ q4_rows_kernel(GemvParams p)
         if (jr < my_ring) {
             const uint8_t *src = p.w;
             if (colok) {
-                const int64_t prow = rows_phys(p, n0 + g + G * (REG + jr));
-                src = p.w + prow * p.w_row_bytes + colbyte;
-                sv = rows_scale_global<WK>(p, prow, col0);
+                if constexpr (kStep) {
+                    src = wnext;
+                    if constexpr (WK == W_INT4)
+                        sv = ld_nc_u16(snext) | (ld_nc_u16(snext + mdiff) << 16);
+                    else
+                        sv = ld_nc_u16(snext);
+                } else {
+                    const int64_t prow = rows_phys(p, n0 + g + G * (REG + jr));
+                    src = p.w + prow * p.w_row_bytes + colbyte;
+                    sv = rows_scale_global<WK>(p, prow, col0);
+                }
             }
             cp_async_16(ring + (uint32_t)slot * (RK_THREADS * 16), src, colok ? 16u : 0u);
+            if constexpr (kStep) {
+                wnext += wstep;
+                snext += sstep;
+            }
         }
         sw[slot] = sv;
         cp_async_commit();
