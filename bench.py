@@ -38,7 +38,7 @@ METRIC = "4-bit decode GEMV µs/call & effective weight GB/s (% of GB300 HBM pea
 # valid only for the kernel sources it was taken on (see _kernel_sha).
 TRAFFIC = {
     # workload key: (bytes per launch, _kernel_sha() when captured)
-    "nvfp4_gemv": (18916352, "57230a01d6632c75587dbd2900a7711fb40f7787a56cdb41b3762b82ef2eb6fc"),
+    "nvfp4_gemv": (18909184, "9a158f314761df1d5490918e3e11ca7253018bd81728892b21d2f35985c13440"),
 }
 
 
@@ -602,7 +602,9 @@ def run_gpu(args, world, rank, local):
             "higher_is_better": True,
             "scaling": "weak",
             "vs_baseline": None,
-            "dtype": "f32",
+            # NVFP4 whole-row GEMV: fp16 partial sums per 16-column group, fp32 across
+            # groups; the other layouts accumulate in fp32
+            "dtype": "f16/f32" if wl.layout == "nvfp4" else "f32",
             "data": "synthetic (seeded PCG64; shapes and distributions of the workload)",
             "config": {
                 "workload": wl.desc,
