@@ -273,6 +273,13 @@ __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, un
     return ok != 0;
 }
 
+// Order this thread's earlier generic-proxy shared-memory accesses before later
+// async-proxy ones (TMA copies, tensor-core operand reads).
+__device__ __forceinline__ void fence_proxy_async()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // One contiguous global -> shared copy on the TMA engine; completion is counted
 // in bytes on the mbarrier.  dst, src 16-byte aligned; bytes a multiple of 16.
 __device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void *src, uint32_t bytes,
