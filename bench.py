@@ -12,7 +12,10 @@ stream with a barrier + synchronize on both sides; the max over ranks is taken.
 `value` is the effective weight bandwidth (algorithmic bytes / time per call).
 The `e2e` key repeats the measurement through the same public call with the
 activations copied in from pinned host memory and the result copied back every
-step.  `--impl reference` times the CPU oracle on the host cores instead.
+step (copies on their own streams, device x and y double-buffered, so one step's
+copies overlap the neighbouring steps' kernels; the host results are checked
+against the device results).  `--impl reference` times the CPU oracle on the
+host cores instead.
 """
 from __future__ import annotations
 
@@ -552,27 +555,68 @@ def run_gpu(args, world, rank, local):
     ms = max_over_ranks(ms, world)
     clocks = clk.summary()
 
-    # end to end through the public call: pinned host x in, y back, every step
+    # End to end through the public call: every step copies its x in from pinned
+    # host memory and its y back out to pinned host memory.  The copies run on
+    # their own streams with double-buffered device x and y, so that step i + 1's
+    # input copy and step i's output copy overlap step i's kernel, as in a
+    # serving loop; every copy still happens inside the timed region.
+    NBUF = 2
     xh = torch.empty_like(wl.x, device="cpu").pin_memory()
     xh.copy_(wl.x.cpu())
-    yh = torch.empty((wl.M, wl.N), dtype=torch.bfloat16).pin_memory()
-    xd = torch.empty_like(wl.x)
+    yh = [torch.empty((wl.M, wl.N), dtype=torch.bfloat16).pin_memory() for _ in range(NBUF)]
+    xd = [torch.empty_like(wl.x) for _ in range(NBUF)]
+    yd = [torch.empty_like(wl.y) for _ in range(NBUF)]
+    s_in = torch.cuda.Stream(device)
+    s_out = torch.cuda.Stream(device)
+    k_ev = [torch.cuda.Event() for _ in range(NBUF)]     # kernel of the buffer's last step
+    x_ev = [torch.cuda.Event() for _ in range(NBUF)]     # input copy landed
+    o_ev = [torch.cuda.Event() for _ in range(NBUF)]     # output copy done
 
-    def e2e_step(i):
-        xd.copy_(xh, non_blocking=True)
-        wl.call(i, x=xd)
-        yh.copy_(wl.y, non_blocking=True)
+    def e2e_steps(n):
+        cur = torch.cuda.current_stream()
+        s_in.wait_stream(cur)                             # fork (joins a graph capture)
+        s_out.wait_stream(cur)
+        for i in range(n):
+            b = i % NBUF
+            if i >= NBUF:
+                s_in.wait_event(k_ev[b])                  # step i - 2's kernel read xd[b]
+            with torch.cuda.stream(s_in):
+                xd[b].copy_(xh, non_blocking=True)
+                x_ev[b].record(s_in)
+            cur.wait_event(x_ev[b])
+            if i >= NBUF:
+                cur.wait_event(o_ev[b])                   # step i - 2's output copy read yd[b]
+            wl.call(i, x=xd[b], y=yd[b])
+            k_ev[b].record(cur)
+            s_out.wait_event(k_ev[b])
+            with torch.cuda.stream(s_out):
+                yh[b].copy_(yd[b], non_blocking=True)
+                o_ev[b].record(s_out)
+        cur.wait_stream(s_in)                             # join before the graph ends
+        cur.wait_stream(s_out)
+
+    def e2e_graph(n):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(g, stream=stream):
+                e2e_steps(n)
+        return g
 
     with torch.cuda.stream(stream):
-        for i in range(3):
-            e2e_step(i)
+        e2e_steps(3)
     torch.cuda.synchronize()
     Ke = max(R, min(K, 20000))
-    ge = _capture(torch, e2e_step, R, stream)
-    ge_tail = _capture(torch, e2e_step, Ke % R, stream) if Ke % R else None
+    ge = e2e_graph(R)
+    ge_tail = e2e_graph(Ke % R) if Ke % R else None
+    _time_graphs(torch, stream, [(ge, 2)], world)
     e2e_ms = _time_graphs(torch, stream, [(ge, Ke // R)] + ([(ge_tail, 1)] if ge_tail else []),
                           world)
     e2e_ms = max_over_ranks(e2e_ms, world)
+    # each host buffer holds the result of the last step that used it
+    torch.cuda.synchronize()
+    for b in range(NBUF):
+        if not torch.equal(yh[b].view(torch.int16), yd[b].cpu().view(torch.int16)):
+            raise SystemExit("end-to-end output copy does not match the device result")
 
     us_per_call = ms * 1e3 / K
     gbs = wl.bytes_per_call / (us_per_call * 1e-6) / 1e9
