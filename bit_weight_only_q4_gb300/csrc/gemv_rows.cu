@@ -92,10 +92,11 @@ __device__ __forceinline__ void rows_load_x(const uint16_t *xs, const float *cf,
     }
 }
 
-// One lane's share of one row: 16 weight bytes (w4) and its scale word (int4:
-// fp16 scale | fp16 min << 16; NVFP4: two e4m3 group scales) against MT tokens.
+// One lane's share of one row: 16 weight bytes (w4) and its scale words (int4:
+// fp16 scale in swr, fp16 min in swm; NVFP4: two e4m3 group scales in swr; int8:
+// the fp16 row scale) against MT tokens.
 template <int WK, int MT, int XV>
-__device__ __forceinline__ void rows_dot(const uint4 qv, uint32_t swr,
+__device__ __forceinline__ void rows_dot(const uint4 qv, uint32_t swr, uint32_t swm,
                                          const uint32_t (&xr)[MT][XV], const float4 (&cd)[MT],
                                          float *out)
 {
@@ -133,39 +134,43 @@ __device__ __forceinline__ void rows_dot(const uint4 qv, uint32_t swr,
         for (int m = 0; m < MT; ++m)
             out[m] = fmaf(-1152.f, cd[m].y, A[m]) * cd[m].x * sc;
     } else if constexpr (WK == W_INT4) {
-        float A1[MT], A2[MT];
+        // fp16 sums of (c - 8) x' (c - 8 in -8 .. 7, exact; symmetric codes keep
+        // the sums from cancelling against the min term): eight products per half
+        // in each of two accumulators, one rounding per add, below 8 * 8 * 2^9 by
+        // the prescale; then sum_k (c s + m) x' = s C + (m + 8 s) X in fp32.
+        uint32_t H1[MT], H2[MT];
 #pragma unroll
         for (int m = 0; m < MT; ++m) {
-            A1[m] = 0.f;
-            A2[m] = 0.f;
+            H1[m] = 0u;
+            H2[m] = 0u;
         }
 #pragma unroll
         for (int jj = 0; jj < 4; ++jj) {
             const uint32_t w8 = w4[jj] >> 8;
-            const uint32_t pa = int4_pair_f16_biased<0x000F000Fu>(w4[jj]);  // cols 0, 4
-            const uint32_t pb = int4_pair_f16_biased<0x00F000F0u>(w4[jj]);  // cols 1, 5
-            const uint32_t pc = int4_pair_f16_biased<0x000F000Fu>(w8);      // cols 2, 6
-            const uint32_t pd = int4_pair_f16_biased<0x00F000F0u>(w8);      // cols 3, 7
+            // magic pairs (1024 + c) and (1024 + 16 c) -> (c - 8), exactly
+            const uint32_t pa = hadd2_rn(int4_pair_f16_biased<0x000F000Fu>(w4[jj]), 0xE408E408u); // cols 0, 4
+            const uint32_t pb = hfma2_rn(int4_pair_f16_biased<0x00F000F0u>(w4[jj]), 0x2C002C00u,
+                                         0xD480D480u);                                           // cols 1, 5
+            const uint32_t pc = hadd2_rn(int4_pair_f16_biased<0x000F000Fu>(w8), 0xE408E408u);     // cols 2, 6
+            const uint32_t pd = hfma2_rn(int4_pair_f16_biased<0x00F000F0u>(w8), 0x2C002C00u,
+                                         0xD480D480u);                                           // cols 3, 7
 #pragma unroll
             for (int m = 0; m < MT; ++m) {
-                A1[m] = fma2_f16(A1[m], pa, xr[m][4 * jj + 0]);
-                A2[m] = fma2_f16(A2[m], pb, xr[m][4 * jj + 1]);
-                A1[m] = fma2_f16(A1[m], pc, xr[m][4 * jj + 2]);
-                A2[m] = fma2_f16(A2[m], pd, xr[m][4 * jj + 3]);
+                uint32_t &H = jj < 2 ? H1[m] : H2[m];
+                H = hfma2_rn(pa, xr[m][4 * jj + 0], H);
+                H = hfma2_rn(pb, xr[m][4 * jj + 1], H);
+                H = hfma2_rn(pc, xr[m][4 * jj + 2], H);
+                H = hfma2_rn(pd, xr[m][4 * jj + 3], H);
             }
         }
         const float sc = f16lo_to_f32(swr);
-        const float mn = f16hi_to_f32(swr);
-        const float c1 = fmaf(-1024.f, sc, mn);
-        const float c2 = fmaf(-64.f, sc, mn);
-        const float s16 = sc * 0.0625f;
+        const float mn = f16lo_to_f32(swm);
+        const float m8 = fmaf(8.f, sc, mn);
 #pragma unroll
         for (int m = 0; m < MT; ++m) {
-            float t = sc * A1[m];
-            t = fmaf(s16, A2[m], t);
-            t = fmaf(c1, cd[m].y, t);
-            t = fmaf(c2, cd[m].z, t);
-            out[m] = t * cd[m].x;
+            const float C = (f16lo_to_f32(H1[m]) + f16hi_to_f32(H1[m])) +
+                            (f16lo_to_f32(H2[m]) + f16hi_to_f32(H2[m]));
+            out[m] = fmaf(sc, C, m8 * (cd[m].y + cd[m].z)) * cd[m].x;
         }
     } else {
         // NVFP4: each 16-column group (two words) is summed in fp16 -- eight exact
@@ -248,8 +253,7 @@ template <int WK>
 __device__ __forceinline__ uint32_t rows_scale_global(const GemvParams &p, int64_t prow, int col0)
 {
     if constexpr (WK == W_INT4) {
-        const int64_t gi = prow * (p.K / 128) + col0 / 128;
-        return ld_nc_u16(static_cast<const uint16_t *>(p.scale) + gi) | (ld_nc_u16(p.minv + gi) << 16);
+        return ld_nc_u16(static_cast<const uint16_t *>(p.scale) + prow * (p.K / 128) + col0 / 128);
     } else if constexpr (WK == W_NVFP4_A16) {
         return ld_nc_u16(static_cast<const uint8_t *>(p.scale) + prow * (p.K / 16) + col0 / 16);
     } else if constexpr (WK == W_INT8) {
@@ -258,6 +262,17 @@ __device__ __forceinline__ uint32_t rows_scale_global(const GemvParams &p, int64
     } else {
         return 0u;
     }
+}
+
+// int4: the min word of physical row prow for the lane (loaded apart from the
+// scale and combined only where it is used).
+template <int WK>
+__device__ __forceinline__ uint32_t rows_min_global(const GemvParams &p, int64_t prow, int col0)
+{
+    if constexpr (WK == W_INT4)
+        return ld_nc_u16(p.minv + prow * (p.K / 128) + col0 / 128);
+    else
+        return 0u;
 }
 
 // ------------------------------------------------------------ cp.async ring
@@ -325,22 +340,22 @@ q4_rows_kernel(GemvParams p)
     // Request ring row jr (row j = REG + jr of this warp) into ring slot `slot`
     // (one commit group per call, empty past the last row, so wait_group counts
     // stay uniform).
-    uint32_t sw[NSLOT];
+    uint32_t sw[NSLOT], swm[NSLOT];
     auto issue = [&](int jr, int slot) {
-        uint32_t sv = 0u;
+        uint32_t sv = 0u, mv = 0u;
         if (jr < my_ring) {
             const uint8_t *src = p.w;
             if (colok) {
                 if constexpr (kStep) {
                     src = wnext;
+                    sv = ld_nc_u16(snext);
                     if constexpr (WK == W_INT4)
-                        sv = ld_nc_u16(snext) | (ld_nc_u16(snext + mdiff) << 16);
-                    else
-                        sv = ld_nc_u16(snext);
+                        mv = ld_nc_u16(snext + mdiff);
                 } else {
                     const int64_t prow = rows_phys(p, n0 + g + G * (REG + jr));
                     src = p.w + prow * p.w_row_bytes + colbyte;
                     sv = rows_scale_global<WK>(p, prow, col0);
+                    mv = rows_min_global<WK>(p, prow, col0);
                 }
             }
             cp_async_16(ring + (uint32_t)slot * (RK_THREADS * 16), src, colok ? 16u : 0u);
@@ -350,21 +365,24 @@ q4_rows_kernel(GemvParams p)
             }
         }
         sw[slot] = sv;
+        swm[slot] = mv;
         cp_async_commit();
     };
 
     // the first REG rows of the warp: 128-bit loads straight into registers
     constexpr int NREG = REG > 0 ? REG : 1;
     uint4 q[NREG];
-    uint32_t sq[NREG];
+    uint32_t sq[NREG], sqm[NREG];
 #pragma unroll
     for (int r = 0; r < NREG; ++r) {
         q[r] = make_uint4(0u, 0u, 0u, 0u);
         sq[r] = 0u;
+        sqm[r] = 0u;
         if (r < REG && r < my_rows && colok) {
             const int64_t prow = rows_phys(p, n0 + g + G * r);
             q[r] = ld_stream_v4(p.w + prow * p.w_row_bytes + colbyte);
             sq[r] = rows_scale_global<WK>(p, prow, col0);
+            sqm[r] = rows_min_global<WK>(p, prow, col0);
         }
     }
 #pragma unroll
@@ -387,7 +405,7 @@ q4_rows_kernel(GemvParams p)
         float part[RB * MT];
 #pragma unroll
         for (int r = 0; r < RB; ++r)
-            rows_dot<WK, MT, XV>(q[r], sq[r], xr, cd, part + r * MT);
+            rows_dot<WK, MT, XV>(q[r], sq[r], sqm[r], xr, cd, part + r * MT);
         rows_park<RB, MT, S>(part, lane, ks, g, G, my_rows, red);
     }
 
@@ -401,7 +419,7 @@ q4_rows_kernel(GemvParams p)
             float part[RB * MT];
 #pragma unroll
             for (int r = 0; r < RB; ++r)
-                rows_dot<WK, MT, XV>(ring_ld[(h * RB + r) * RK_THREADS], sw[h * RB + r], xr, cd,
+                rows_dot<WK, MT, XV>(ring_ld[(h * RB + r) * RK_THREADS], sw[h * RB + r], swm[h * RB + r], xr, cd,
                                      part + r * MT);
             // the slots' contents are in registers now: refill them NB * RB rows ahead
 #pragma unroll

@@ -52,17 +52,19 @@ __device__ __forceinline__ void cp_async_wait()
     asm volatile("cp.async.wait_group %0;" :: "n"(N) : "memory");
 }
 
+// 8- and 16-bit loads straight into 32-bit registers (zero-extended), so no
+// widening instruction waits for the load right after it is issued.
 __device__ __forceinline__ uint32_t ld_nc_u16(const void *p)
 {
-    unsigned short r;
-    asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(r) : "l"(p));
+    uint32_t r;
+    asm volatile("ld.global.nc.u16 %0, [%1];" : "=r"(r) : "l"(p));
     return r;
 }
 
 __device__ __forceinline__ uint32_t ld_nc_u8(const void *p)
 {
-    unsigned short r;
-    asm volatile("ld.global.nc.u8 %0, [%1];" : "=h"(r) : "l"(p));
+    uint32_t r;
+    asm volatile("ld.global.nc.u8 %0, [%1];" : "=r"(r) : "l"(p));
     return r;
 }
 
@@ -118,6 +120,14 @@ __device__ __forceinline__ float fma2_f16(float acc, uint32_t a, uint32_t b)
         : "+f"(acc)
         : "r"(a), "r"(b));
     return acc;
+}
+
+// Packed fp16 add: a + b per half, one rounding each.
+__device__ __forceinline__ uint32_t hadd2_rn(uint32_t a, uint32_t b)
+{
+    uint32_t r;
+    asm("add.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
 }
 
 // Packed fp16 fused multiply-add: c + a * b per half, one rounding each.

@@ -116,10 +116,11 @@ __device__ void stage_x(const GemvParams &p, int Kpad, uint16_t *xs, float *cf, 
                 else
                     frexpf(amax, &ex);
             }
-            // chunk maximum in [2^14, 2^15); NVFP4 in [2^9, 2^10), so that a
-            // half-group sum of eight products (|E2M1| <= 6) stays below 2^16
-            // when the whole-row kernel accumulates it in fp16
-            int pw = (WK == W_NVFP4_A16 ? 10 : 15) - ex;
+            // chunk maximum in [2^14, 2^15); NVFP4 in [2^9, 2^10) and int4 in
+            // [2^8, 2^9), so that a sum of eight products (|E2M1| <= 6,
+            // |c - 8| <= 8) stays below 2^16 when the whole-row kernel
+            // accumulates it in fp16
+            int pw = (WK == W_NVFP4_A16 ? 10 : (WK == W_INT4 ? 9 : 15)) - ex;
             pw = pw > 100 ? 100 : (pw < -100 ? -100 : pw);
             const float up = pow2f(pw);
             float xq[8];
