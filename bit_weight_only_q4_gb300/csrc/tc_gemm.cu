@@ -463,127 +463,138 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
             rowk[k] = (128 / WG) * wg + RPS * k + lane / L;
             rok[k] = n0 + rowk[k] < p.N;
         }
-        auto load_scale = [&](int u, int k) -> uint32_t {
+        // Group scales (int4: fp16 scale and min, loaded apart and combined only
+        // where used; NVFP4: the e4m3 byte) run SA stages ahead in SA register
+        // sets, each refilled right after its stage: no register moves, so no
+        // wait on a load still in flight.
+        auto load_scale = [&](int u, int k, const void *base) -> uint32_t {
             const int kc = c0 + u * SC + c;
-            if (!rok[k] || kc >= c1)
+            if (u >= nsup || !rok[k] || kc >= c1)
                 return 0u;
             const int64_t n = n0 + rowk[k];
-            if constexpr (LAYOUT == 0) {
-                const int64_t gi = n * (p.K / 128) + (kc * TC_KC) / 128;
-                return ld_nc_u16(static_cast<const uint16_t *>(p.scale) + gi) |
-                       (ld_nc_u16(p.minv + gi) << 16);
-            } else {
-                return ld_nc_u8(static_cast<const uint8_t *>(p.scale) + n * (p.K / 16) + kc * 4 + qd);
-            }
+            if constexpr (LAYOUT == 0)
+                return ld_nc_u16(static_cast<const uint16_t *>(base) + n * (p.K / 128) + (kc * TC_KC) / 128);
+            else
+                return ld_nc_u8(static_cast<const uint8_t *>(base) + n * (p.K / 16) + kc * 4 + qd);
         };
-        uint32_t scq[SA][STEPS];
+        uint32_t scq[SA][STEPS], mnq[SA][STEPS];
 #pragma unroll
         for (int j = 0; j < SA; ++j)
 #pragma unroll
-            for (int k = 0; k < STEPS; ++k)
-                scq[j][k] = gi + j * G < nsup ? load_scale(gi + j * G, k) : 0u;
+            for (int k = 0; k < STEPS; ++k) {
+                scq[j][k] = load_scale(gi + j * G, k, p.scale);
+                mnq[j][k] = LAYOUT == 0 ? load_scale(gi + j * G, k, p.minv) : 0u;
+            }
         bool range_bad = false;
         TC_PHASE_DECL;
-        for (int u = gi; u < nsup; u += G) {
-            const int s = u % NS, use = u / NS;
-            uint32_t sc[STEPS];
-#pragma unroll
-            for (int k = 0; k < STEPS; ++k) {
-                sc[k] = scq[0][k];
-#pragma unroll
-                for (int j = 0; j + 1 < SA; ++j)
-                    scq[j][k] = scq[j + 1][k];
-                scq[SA - 1][k] = u + SA * G < nsup ? load_scale(u + SA * G, k) : 0u;
-            }
-            const int kc = c0 + u * SC;
-            const int nv = (c1 - kc) < SC ? (c1 - kc) : SC;
-            unsigned char *st = smem + (size_t)s * stage_bytes;
-            TC_CLK(t0);
-            if (!mbar_wait_warp(smem_u32(&bars[s]), use & 1, p.err))
-                break;
-            TC_CLK(t1);
-            TC_PHASE(56, t0, t1);
-            // x sub-tiles: bf16 -> fp16 in place (element-wise, swizzle-agnostic).
-            // Only tiles of at most 64 tokens are converted here (larger M arrive
-            // in fp16), so a thread has at most SC * G 16-byte vectors: the loop is
-            // unrolled and interleaves with the code loads below.
-            if (!p.x_f16) {
-                const int per = TN * 8;                  // vectors per sub-tile
-#pragma unroll
-                for (int j = 0; j < SC * G; ++j) {
-                    const int v = wt + j * WG * 32;
-                    if (v < nv * per) {
-                        const int sub = (v >= per) + (v >= 2 * per) + (v >= 3 * per);
-                        uint4 *xv = reinterpret_cast<uint4 *>(st + TcStage<SC>::A + sub * x_stride) +
-                                    (v - sub * per);
-                        const uint4 t = *xv;
-                        const uint32_t e[4] = {t.x, t.y, t.z, t.w};
+        // one stage; false when a wait timed out
+        auto stage = [&](int u, const uint32_t (&scs)[STEPS], const uint32_t (&mns)[STEPS]) -> bool {
+                const int s = u % NS, use = u / NS;
+                const int kc = c0 + u * SC;
+                const int nv = (c1 - kc) < SC ? (c1 - kc) : SC;
+                unsigned char *st = smem + (size_t)s * stage_bytes;
+                TC_CLK(t0);
+                if (!mbar_wait_warp(smem_u32(&bars[s]), use & 1, p.err))
+                    return false;
+                TC_CLK(t1);
+                TC_PHASE(56, t0, t1);
+                // x sub-tiles: bf16 -> fp16 in place (element-wise, swizzle-agnostic).
+                // Only tiles of at most 64 tokens are converted here (larger M arrive
+                // in fp16), so a thread has at most SC * G 16-byte vectors: the loop is
+                // unrolled and interleaves with the code loads below.
+                if (!p.x_f16) {
+                    const int per = TN * 8;                  // vectors per sub-tile
+    #pragma unroll
+                    for (int j = 0; j < SC * G; ++j) {
+                        const int v = wt + j * WG * 32;
+                        if (v < nv * per) {
+                            const int sub = (v >= per) + (v >= 2 * per) + (v >= 3 * per);
+                            uint4 *xv = reinterpret_cast<uint4 *>(st + TcStage<SC>::A + sub * x_stride) +
+                                        (v - sub * per);
+                            const uint4 t = *xv;
+                            const uint32_t e[4] = {t.x, t.y, t.z, t.w};
+                            uint32_t o[4];
+                            float mx = 0.f;
+    #pragma unroll
+                            for (int q = 0; q < 4; ++q) {
+                                const float lo = bf16_bits_to_f32(e[q] & 0xffffu);
+                                const float hi = bf16_bits_to_f32(e[q] >> 16);
+                                mx = fmaxf(mx, fmaxf(fabsf(lo), fabsf(hi)));
+                                __half2 h = __floats2half2_rn(lo, hi);
+                                o[q] = *reinterpret_cast<uint32_t *>(&h);
+                            }
+                            if (mx >= 65520.f && mx <= 3.4e38f)
+                                range_bad = true;
+                            *xv = make_uint4(o[0], o[1], o[2], o[3]);
+                        }
+                    }
+                }
+                TC_CLK(t2);
+                TC_PHASE(57, t1, t2);
+                const unsigned char *codes = st + TcStage<SC>::A + SC * x_stride;
+    #pragma unroll
+                for (int k = 0; k < STEPS; ++k) {
+                    const int rd = rowk[k];
+                    const uint2 cw = *reinterpret_cast<const uint2 *>(codes + rd * (SC * 32) + cl * 8);
+                    const uint32_t words[2] = {cw.x, cw.y};
+                    unsigned char *arow = st + c * 16384 + rd * 128;
+                    uint32_t sg = 0u;
+                    if constexpr (LAYOUT == 1)
+                        sg = f16x2_splat(e4m3x2_to_f16x2(scs[k] & 0xffu) & 0xffffu);
+    #pragma unroll
+                    for (int j = 0; j < 2; ++j) {           // 8 K columns per 16-byte chunk
                         uint32_t o[4];
-                        float mx = 0.f;
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            const float lo = bf16_bits_to_f32(e[q] & 0xffffu);
-                            const float hi = bf16_bits_to_f32(e[q] >> 16);
-                            mx = fmaxf(mx, fmaxf(fabsf(lo), fabsf(hi)));
-                            __half2 h = __floats2half2_rn(lo, hi);
-                            o[q] = *reinterpret_cast<uint32_t *>(&h);
+                        if constexpr (LAYOUT == 0) {
+                            const uint32_t s2 = f16x2_splat(scs[k]);
+                            const uint32_t m2 = f16x2_splat(mns[k]);
+    #pragma unroll
+                            for (int b = 0; b < 4; ++b) {
+                                // byte b -> (1024 + c_lo, 1024 + 16 c_hi) -> (c_lo, c_hi)
+                                const uint32_t t = prmt(words[j], 0u, (uint32_t)(b | (4 << 4) | (b << 8) | (4 << 12)));
+                                uint32_t v2;
+                                asm("lop3.b32 %0, %1, 0x00F0000F, 0x64006400, 0xEA;" : "=r"(v2) : "r"(t));
+                                v2 = hfma2(v2, 0x2C003C00u, 0xD400E400u);   // * (1, 1/16) + (-1024, -64)
+                                o[b] = hfma2(v2, s2, m2);                   // c * s + min, one rounding
+                            }
+                        } else {
+                            uint32_t h[4];
+                            e2m1x8_to_f16x2x4(words[j], h);
+    #pragma unroll
+                            for (int b = 0; b < 4; ++b)
+                                o[b] = hmul2(h[b], sg);                    // exact in fp16
                         }
-                        if (mx >= 65520.f && mx <= 3.4e38f)
-                            range_bad = true;
-                        *xv = make_uint4(o[0], o[1], o[2], o[3]);
+                        const int seg = 2 * qd + j;
+                        *reinterpret_cast<uint4 *>(arow + ((seg ^ (rd & 7)) << 4)) =
+                            make_uint4(o[0], o[1], o[2], o[3]);
                     }
                 }
-            }
-            TC_CLK(t2);
-            TC_PHASE(57, t1, t2);
-            const unsigned char *codes = st + TcStage<SC>::A + SC * x_stride;
+                TC_CLK(t3);
+                TC_PHASE(58, t2, t3);
+                fence_proxy_async();
+                TC_CLK(t4);
+                TC_PHASE(59, t3, t4);
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(smem_u32(&bars[NS + s]));
+                TC_CLK(t5);
+                TC_PHASE(60, t4, t5);
+                if (warp == 2 && lane == 0) TC_TRACE(24 + u);
+            return true;
+        };
+        bool alive = true;
+        for (int u0 = gi; u0 < nsup && alive; u0 += SA * G) {
 #pragma unroll
-            for (int k = 0; k < STEPS; ++k) {
-                const int rd = rowk[k];
-                const uint2 cw = *reinterpret_cast<const uint2 *>(codes + rd * (SC * 32) + cl * 8);
-                const uint32_t words[2] = {cw.x, cw.y};
-                unsigned char *arow = st + c * 16384 + rd * 128;
-                uint32_t sg = 0u;
-                if constexpr (LAYOUT == 1)
-                    sg = f16x2_splat(e4m3x2_to_f16x2(sc[k] & 0xffu) & 0xffffu);
+            for (int j = 0; j < SA; ++j) {
+                const int u = u0 + j * G;
+                if (alive && u < nsup)
+                    alive = stage(u, scq[j], mnq[j]);
 #pragma unroll
-                for (int j = 0; j < 2; ++j) {           // 8 K columns per 16-byte chunk
-                    uint32_t o[4];
-                    if constexpr (LAYOUT == 0) {
-                        const uint32_t s2 = f16x2_splat(sc[k] & 0xffffu);
-                        const uint32_t m2 = f16x2_splat(sc[k] >> 16);
-#pragma unroll
-                        for (int b = 0; b < 4; ++b) {
-                            // byte b -> (1024 + c_lo, 1024 + 16 c_hi) -> (c_lo, c_hi)
-                            const uint32_t t = prmt(words[j], 0u, (uint32_t)(b | (4 << 4) | (b << 8) | (4 << 12)));
-                            uint32_t v2;
-                            asm("lop3.b32 %0, %1, 0x00F0000F, 0x64006400, 0xEA;" : "=r"(v2) : "r"(t));
-                            v2 = hfma2(v2, 0x2C003C00u, 0xD400E400u);   // * (1, 1/16) + (-1024, -64)
-                            o[b] = hfma2(v2, s2, m2);                   // c * s + min, one rounding
-                        }
-                    } else {
-                        uint32_t h[4];
-                        e2m1x8_to_f16x2x4(words[j], h);
-#pragma unroll
-                        for (int b = 0; b < 4; ++b)
-                            o[b] = hmul2(h[b], sg);                    // exact in fp16
-                    }
-                    const int seg = 2 * qd + j;
-                    *reinterpret_cast<uint4 *>(arow + ((seg ^ (rd & 7)) << 4)) =
-                        make_uint4(o[0], o[1], o[2], o[3]);
+                for (int k = 0; k < STEPS; ++k) {
+                    scq[j][k] = load_scale(u + SA * G, k, p.scale);
+                    if constexpr (LAYOUT == 0)
+                        mnq[j][k] = load_scale(u + SA * G, k, p.minv);
                 }
             }
-            TC_CLK(t3);
-            TC_PHASE(58, t2, t3);
-            fence_proxy_async();
-            TC_CLK(t4);
-            TC_PHASE(59, t3, t4);
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(smem_u32(&bars[NS + s]));
-            TC_CLK(t5);
-            TC_PHASE(60, t4, t5);
-            if (warp == 2 && lane == 0) TC_TRACE(24 + u);
         }
         TC_PHASE_STORE();
         if (range_bad && p.err)
