@@ -45,11 +45,15 @@ constexpr int TC_WORKERS = 4 * TC_GROUPS;   // dequant / epilogue warps
 constexpr int TC_THREADS = (2 + TC_WORKERS) * 32;
 constexpr unsigned kErrFp16Range = 2u;
 
-// Per-CTA timestamps (globaltimer ns) for builds with -DQ4_TRACE: slots 0..7
-// start, TMEM ready, final commit seen by the epilogue, end; 8+i producer issued
-// chunk i, 24+i workers (warp 2) finished chunk i, 40+i MMA issued chunk i;
-// 56..61 warp 2's clock cycles summed over its chunks: data waits, x conversion,
-// dequant, proxy fence, warp sync + arrive.
+// Per-CTA timestamps (globaltimer ns) for builds with -DQ4_TRACE.  Ring kernel:
+// slots 0..3 start, TMEM ready, final commit seen by the epilogue, end; 8+i
+// producer issued stage i, 24+i workers (warp 2) finished stage i, 40+i MMA issued
+// stage i; 56..60 warp 2's clock cycles summed over its stages: data waits, x
+// conversion, dequant, proxy fence, warp sync + arrive.  Skinny kernel: 0, 1, 2,
+// 3 as above, 4 / 6 / 7 / 61 x warps issued their copies / saw step 0 land / had
+// step 0 ready / saw the last step land, 5 past the first cluster barrier; 24+s
+// and 8+s the MMA thread past the A-full and x-ready waits of step s, 40+s its
+// MMAs issued; 56..59 warp 2's cycles in the step's waits and stores.
 #ifdef Q4_TRACE
 __device__ unsigned long long g_q4_tc_trace[8 * 1024 * 64];   // 8 most recent calls
 __device__ __forceinline__ unsigned long long tc_now()
@@ -76,7 +80,6 @@ extern "C" int q4_tc_trace_copy(unsigned long long *host, int n)
 #endif
 
 struct TcParams {
-    const uint16_t *x;         // bf16 [M, K] (skinny kernel; the ring kernel uses a tensor map)
     const uint8_t *codes;      // [N, K/2]
     const void *scale;         // int4: fp16 [N, K/128]; NVFP4: e4m3 [N, K/16]
     const uint16_t *minv;      // int4: fp16 [N, K/128]
@@ -134,20 +137,10 @@ __device__ __forceinline__ uint32_t idesc_f16(int n)
          | ((uint32_t)(TC_ROWS >> 4) << 24);   // M / 16
 }
 
-__device__ __forceinline__ void mma_f16(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t idesc,
-                                        uint32_t accumulate)
-{
-    asm volatile("{\n\t.reg .pred p;\n\t"
-                 "setp.ne.u32 p, %4, 0;\n\t"
-                 "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
-                 ::"r"(tmem_d), "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
-                 : "memory");
-}
-
-// The same with both descriptors passed as 32-bit halves, so that the issuing
-// loop only steps the start-address fields (low halves: +2 per 32 bytes).  One
-// thread issues every MMA of a CTA; rebuilding two 64-bit descriptors per MMA
-// made that thread, not the tensor core, the limit.
+// tcgen05.mma kind::f16 (M = 128) with both descriptors passed as 32-bit halves,
+// so that the issuing loop only steps the start-address fields (low halves: +2 per
+// 32 bytes).  One thread issues every MMA of a CTA; rebuilding two 64-bit
+// descriptors per MMA costs that thread more than the MMA costs the tensor core.
 __device__ __forceinline__ void mma_f16_2(uint32_t tmem_d, uint32_t a_lo, uint32_t a_hi, uint32_t b_lo,
                                           uint32_t b_hi, uint32_t idesc, uint32_t accumulate)
 {
@@ -649,22 +642,6 @@ __device__ __forceinline__ void cluster_sync_all()
                  "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-// Scale loads straight into 32-bit registers (no widening instruction that
-// would wait for the load).
-__device__ __forceinline__ uint32_t ld_nc_u8_r32(const void *p)
-{
-    uint32_t r;
-    asm volatile("ld.global.nc.u8 %0, [%1];" : "=r"(r) : "l"(p));
-    return r;
-}
-
-__device__ __forceinline__ uint32_t ld_nc_u16_r32(const void *p)
-{
-    uint32_t r;
-    asm volatile("ld.global.nc.u16 %0, [%1];" : "=r"(r) : "l"(p));
-    return r;
-}
-
 // 16 codes (one row, 16 consecutive columns) -> 16 fp16 weights: int4
 // w = c * s + min (one fused multiply-add, one rounding); NVFP4 w = E2M1 * e4m3,
 // exact in fp16 (the global scale is applied in the epilogue).
@@ -704,22 +681,10 @@ constexpr int SK_THREADS = TC_THREADS + SK_XWARPS * 32;
 constexpr int SK_NA = 6;                              // TMEM A slots of two chunks
 constexpr int SK_TMEM_COLS = 512;                     // accumulator (<= 64) + A slots
 
-// tcgen05.mma with the A operand in tensor memory: row i of A in lane i, its K
-// values packed two per 32-bit column.
-__device__ __forceinline__ void mma_f16_tmem_a(uint32_t tmem_d, uint32_t tmem_a, uint64_t b,
-                                               uint32_t idesc, uint32_t accumulate)
-{
-    asm volatile("{\n\t.reg .pred p;\n\t"
-                 "setp.ne.u32 p, %4, 0;\n\t"
-                 "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
-                 ::"r"(tmem_d), "r"(tmem_a), "l"(b), "r"(idesc), "r"(accumulate)
-                 : "memory");
-}
-
-// The same with the B descriptor passed as two 32-bit halves: the issuing loop
-// then steps the start-address field (low half) by 2 per 32 bytes instead of
-// rebuilding a 64-bit descriptor per MMA (one thread issues every MMA, so its
-// instruction count per MMA is on the critical path).
+// tcgen05.mma with the A operand in tensor memory (row i of A in lane i, its K
+// values packed two per 32-bit column) and the B descriptor passed as two 32-bit
+// halves, so that the issuing loop steps the start-address field (low half) by 2
+// per 32 bytes instead of rebuilding a 64-bit descriptor per MMA.
 __device__ __forceinline__ void mma_f16_tmem_a2(uint32_t tmem_d, uint32_t tmem_a, uint32_t b_lo,
                                                 uint32_t b_hi, uint32_t idesc, uint32_t accumulate)
 {
@@ -963,10 +928,10 @@ q4_tc_skinny_kernel(const __grid_constant__ CUtensorMap xmap,
             const int kc = c0 + j;
             if constexpr (LAYOUT == 0) {
                 const int64_t gi = n * (p.K / 128) + kc / 2;
-                return ld_nc_u16_r32(static_cast<const uint16_t *>(p.scale) + gi) |
-                       (ld_nc_u16_r32(p.minv + gi) << 16);
+                return ld_nc_u16(static_cast<const uint16_t *>(p.scale) + gi) |
+                       (ld_nc_u16(p.minv + gi) << 16);
             } else {
-                return ld_nc_u16_r32(static_cast<const uint8_t *>(p.scale) + n * (p.K / 16) + kc * 4 +
+                return ld_nc_u16(static_cast<const uint8_t *>(p.scale) + n * (p.K / 16) + kc * 4 +
                                      2 * half);
             }
         };
@@ -1388,7 +1353,6 @@ q4_status tc_launch(int kind, const void *x, const uint8_t *codes, const void *s
             p.ns = SK_NA;
             p.tmem_cols = SK_TMEM_COLS;
             p.x_f16 = 0;
-            p.x = static_cast<const uint16_t *>(x);
             CUtensorMap xmap, wmap;
             const CUresult r = tc_encode_maps(enc, xmap, wmap, x, false, codes, M, N, K, p.TN,
                                               2 * TC_KC, true);
