@@ -35,6 +35,9 @@ struct GemvParams {
     int row_begin, n_rows, extra_row;
     // whole-row kernels: CTA b owns rows_q (+1 when b < rows_r) rows
     int rows_q, rows_r;
+    // whole-row kernels, one token: nanoseconds to hold the prologue's ring
+    // requests back (0: issue at once)
+    unsigned ring_defer_ns;
     // bulk-copy path only
     int64_t T;                // stages = row blocks * S
     int grid;                 // CTAs
