@@ -41,7 +41,7 @@ METRIC = "4-bit decode GEMV µs/call & effective weight GB/s (% of GB300 HBM pea
 # valid only for the kernel sources it was taken on (see _kernel_sha).
 TRAFFIC = {
     # workload key: (bytes per launch, _kernel_sha() when captured)
-    "nvfp4_gemv": (18909184, "70b07e957d6004a89a5208646aadca73b42fcdeb0e4853aac9e978b60881367d"),
+    "nvfp4_gemv": (18909440, "2b145ea31d864149c9eade65bb298fcc31bff4edc24232aa8c78985c69b44a16"),
 }
 
 

@@ -134,43 +134,35 @@ __device__ __forceinline__ void rows_dot(const uint4 qv, uint32_t swr, uint32_t 
         for (int m = 0; m < MT; ++m)
             out[m] = fmaf(-1152.f, cd[m].y, A[m]) * cd[m].x * sc;
     } else if constexpr (WK == W_INT4) {
-        // fp16 sums of (c - 8) x' (c - 8 in -8 .. 7, exact; symmetric codes keep
-        // the sums from cancelling against the min term): eight products per half
-        // in each of two accumulators, one rounding per add, below 8 * 8 * 2^9 by
-        // the prescale; then sum_k (c s + m) x' = s C + (m + 8 s) X in fp32.
-        uint32_t H1[MT], H2[MT];
+        // Exact integer sums: x' is int16 (the int16 staging path, |x'| < 2^15)
+        // and the codes become bytes -- w & 0x0F0F0F0F holds the even
+        // columns' codes, (w >> 4) & 0x0F0F0F0F the odd columns' -- so each
+        // dp2a adds two exact products to an int32.  Over the lane's 32
+        // columns |C| <= 32 * 15 * 32767 < 2^24, so C converts to fp32
+        // exactly; then sum_k (c s + m) x' = s C + m X in fp32, with X the
+        // chunk's sum of x' from staging.
+        int A[MT];
 #pragma unroll
-        for (int m = 0; m < MT; ++m) {
-            H1[m] = 0u;
-            H2[m] = 0u;
-        }
+        for (int m = 0; m < MT; ++m)
+            A[m] = 0;
 #pragma unroll
         for (int jj = 0; jj < 4; ++jj) {
-            const uint32_t w8 = w4[jj] >> 8;
-            // magic pairs (1024 + c) and (1024 + 16 c) -> (c - 8), exactly
-            const uint32_t pa = hadd2_rn(int4_pair_f16_biased<0x000F000Fu>(w4[jj]), 0xE408E408u); // cols 0, 4
-            const uint32_t pb = hfma2_rn(int4_pair_f16_biased<0x00F000F0u>(w4[jj]), 0x2C002C00u,
-                                         0xD480D480u);                                           // cols 1, 5
-            const uint32_t pc = hadd2_rn(int4_pair_f16_biased<0x000F000Fu>(w8), 0xE408E408u);     // cols 2, 6
-            const uint32_t pd = hfma2_rn(int4_pair_f16_biased<0x00F000F0u>(w8), 0x2C002C00u,
-                                         0xD480D480u);                                           // cols 3, 7
+            const uint32_t ce = w4[jj] & 0x0F0F0F0Fu;          // c of columns 0, 2, 4, 6
+            const uint32_t co = (w4[jj] >> 4) & 0x0F0F0F0Fu;   // c of columns 1, 3, 5, 7
 #pragma unroll
             for (int m = 0; m < MT; ++m) {
-                uint32_t &H = jj < 2 ? H1[m] : H2[m];
-                H = hfma2_rn(pa, xr[m][4 * jj + 0], H);
-                H = hfma2_rn(pb, xr[m][4 * jj + 1], H);
-                H = hfma2_rn(pc, xr[m][4 * jj + 2], H);
-                H = hfma2_rn(pd, xr[m][4 * jj + 3], H);
+                A[m] = dp2a_lo_su(xr[m][4 * jj + 0], ce, A[m]);
+                A[m] = dp2a_hi_su(xr[m][4 * jj + 1], ce, A[m]);
+                A[m] = dp2a_lo_su(xr[m][4 * jj + 2], co, A[m]);
+                A[m] = dp2a_hi_su(xr[m][4 * jj + 3], co, A[m]);
             }
         }
         const float sc = f16lo_to_f32(swr);
         const float mn = f16lo_to_f32(swm);
-        const float m8 = fmaf(8.f, sc, mn);
 #pragma unroll
         for (int m = 0; m < MT; ++m) {
-            const float C = (f16lo_to_f32(H1[m]) + f16hi_to_f32(H1[m])) +
-                            (f16lo_to_f32(H2[m]) + f16hi_to_f32(H2[m]));
-            out[m] = fmaf(sc, C, m8 * (cd[m].y + cd[m].z)) * cd[m].x;
+            const float C = (float)A[m];
+            out[m] = fmaf(sc, C, mn * cd[m].y) * cd[m].x;
         }
     } else {
         // NVFP4: each 16-column group (two words) is summed in fp16 -- eight exact
@@ -395,11 +387,11 @@ q4_rows_kernel(GemvParams p)
         gsc = __ldg(p.gscale);
     pdl_launch_dependents();
     pdl_wait();                                   // x comes from the previous kernel
-    stage_x<WK, MT>(p, Kpad, xs, cf, (int)threadIdx.x, RK_THREADS);
+    stage_x<WK, MT, WK == W_INT4>(p, Kpad, xs, cf, (int)threadIdx.x, RK_THREADS);
     __syncthreads();
 
     uint32_t xr[MT][XV];
-    float4 cd[MT];           // int4: (2^-p, X1, X2, -); NVFP4: (2^-p * g, ...)
+    float4 cd[MT];           // int4: (2^-p, X, -, -); NVFP4: (2^-p * g, ...)
     rows_load_x<WK, MT, XV>(xs, cf, Kpad, ks, lane, col0, gsc, xr, cd);
 
     if constexpr (REG > 0) {

@@ -178,6 +178,22 @@ __device__ __forceinline__ uint32_t int4_pair_f16_biased(uint32_t v)
     return r;  // (v & MASK) | 0x64006400
 }
 
+// Integer dot products: c + a.lo16 * b.byte(0|2) + a.hi16 * b.byte(1|3), with a's
+// halves signed 16-bit and b's bytes unsigned (.lo takes bytes 0, 1; .hi 2, 3).
+__device__ __forceinline__ int dp2a_lo_su(uint32_t a, uint32_t b, int c)
+{
+    int d;
+    asm("dp2a.lo.s32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+__device__ __forceinline__ int dp2a_hi_su(uint32_t a, uint32_t b, int c)
+{
+    int d;
+    asm("dp2a.hi.s32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
 // Two float8_e4m3fn bytes (low 16 bits) -> f16x2 (exact: e4m3 fits in fp16).
 __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_bytes)
 {

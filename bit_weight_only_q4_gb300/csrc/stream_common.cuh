@@ -15,7 +15,9 @@
 //     ("magic number" decode); per chunk the two partial sums
 //       A1 = sum_{even k} (1024 + c) x'   and   A2 = sum_{odd k} (1024 + 16 c) x'
 //     give  sum_k (c s + m) x' = s A1 + (s/16) A2 + (m - 1024 s) X1 + (m - 64 s) X2
-//     with X1, X2 the sums of x' over the chunk's even and odd columns.
+//     with X1, X2 the sums of x' over the chunk's even and odd columns (the
+//     split-K and bulk-copy kernels; the whole-row kernel stages int4 x as
+//     int16 and sums c x' exactly with integer dot products, see stage_x).
 #pragma once
 
 #include "q4_device.cuh"
@@ -28,8 +30,8 @@ struct Kind {
     // columns held by one lane's 16 weight bytes
     static constexpr int COLS = (WK == W_BF16) ? 8 : ((WK == W_INT8) ? 16 : 32);
     static constexpr int KSTEP = 32 * COLS;
-    // floats of per-chunk data in shared memory: int4 (2^-p, X1, X2, 0),
-    // NVFP4 (2^-p), bf16 none
+    // floats of per-chunk data in shared memory: int4 (2^-p, X1, X2, 0), or
+    // (2^-p, X, 0, 0) with int16 staging; NVFP4 (2^-p), bf16 none
     // INT8: (2^-p, sum of x' over the chunk's first 16 columns, over its last 16, 0)
     static constexpr int CH = (WK == W_INT4 || WK == W_INT8) ? 4 : ((WK == W_BF16) ? 0 : 1);
 };
@@ -73,10 +75,16 @@ __device__ __forceinline__ float pow2f(int e)  // 2^e for -126 <= e <= 127
     return __uint_as_float((uint32_t)(e + 127) << 23);
 }
 
-template <int WK, int MT>
+// XI16 (int4 whole-row kernel): x' is an int16 fixed-point value instead, chunk
+// maximum in [2^14, 2^15), stored as signed 16-bit pairs in the order the integer
+// dot products take them -- (x0, x2), (x4, x6), (x1, x3), (x5, x7) for each 8
+// columns -- with chunk data (2^-p, sum of x', -, -); a chunk holding a
+// non-finite value gets a NaN sum, so its rows come out NaN.
+template <int WK, int MT, bool XI16 = false>
 __device__ void stage_x(const GemvParams &p, int Kpad, uint16_t *xs, float *cf, int tid,
                         int nthreads)
 {
+    static_assert(!XI16 || WK == W_INT4, "int16 staging is for int4 weights");
     constexpr int CH = Kind<WK>::CH;
     const int blocks_per_row = Kpad / 8;
     const int total = MT * blocks_per_row;
@@ -118,53 +126,81 @@ __device__ void stage_x(const GemvParams &p, int Kpad, uint16_t *xs, float *cf, 
             }
             // chunk maximum in [2^14, 2^15); NVFP4 in [2^9, 2^10) and int4 in
             // [2^8, 2^9), so that a sum of eight products (|E2M1| <= 6,
-            // |c - 8| <= 8) stays below 2^16 when the whole-row kernel
-            // accumulates it in fp16
-            int pw = (WK == W_NVFP4_A16 ? 10 : (WK == W_INT4 ? 9 : 15)) - ex;
+            // |c - 8| <= 8) stays below 2^16 when a kernel accumulates it in
+            // fp16; int16 staging in [2^14, 2^15)
+            int pw = (XI16 ? 15 : (WK == W_NVFP4_A16 ? 10 : (WK == W_INT4 ? 9 : 15))) - ex;
             pw = pw > 100 ? 100 : (pw < -100 ? -100 : pw);
             const float up = pow2f(pw);
-            float xq[8];
-            uint32_t h[4];
+            if constexpr (XI16) {
+                // x * 2^p is exact in fp32 and below 2^15 in magnitude; rounding
+                // to the nearest integer is exact for values within 2^7 of the
+                // chunk maximum (BF16 has 8 significant bits)
+                int xi[8];
+                bool bad = false;
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                __half2 hh;
-                if constexpr (WK == W_INT4)   // pairs (x'[t], x'[t+4])
-                    hh = __floats2half2_rn(f[i] * up, f[i + 4] * up);
-                else                          // natural order
-                    hh = __floats2half2_rn(f[2 * i] * up, f[2 * i + 1] * up);
-                h[i] = *reinterpret_cast<uint32_t *>(&hh);
-                xq[2 * i] = __low2float(hh);
-                xq[2 * i + 1] = __high2float(hh);
-            }
-            if (active)
-                reinterpret_cast<uint4 *>(xs + (size_t)m * Kpad)[xs_vec_index_kind<WK>(k0)] =
-                    make_uint4(h[0], h[1], h[2], h[3]);
-            if constexpr (WK == W_INT4) {
-                // h[i] holds columns (i, i+4): even columns are i = 0, 2
-                float s_even = (xq[0] + xq[1]) + (xq[4] + xq[5]);
-                float s_odd = (xq[2] + xq[3]) + (xq[6] + xq[7]);
-                s_even += __shfl_xor_sync(0xffffffffu, s_even, 1);
-                s_even += __shfl_xor_sync(0xffffffffu, s_even, 2);
-                s_odd += __shfl_xor_sync(0xffffffffu, s_odd, 1);
-                s_odd += __shfl_xor_sync(0xffffffffu, s_odd, 2);
+                for (int i = 0; i < 8; ++i) {
+                    bad |= !(fabsf(f[i]) <= 3.402823466e38f);
+                    xi[i] = __float2int_rn(f[i] * up);
+                }
+                auto pack = [](int lo, int hi) {
+                    return ((uint32_t)lo & 0xffffu) | ((uint32_t)hi << 16);
+                };
+                if (active)
+                    reinterpret_cast<uint4 *>(xs + (size_t)m * Kpad)[xs_vec_index_kind<WK>(k0)] =
+                        make_uint4(pack(xi[0], xi[2]), pack(xi[4], xi[6]), pack(xi[1], xi[3]),
+                                   pack(xi[5], xi[7]));
+                float sx = (float)(((xi[0] + xi[1]) + (xi[2] + xi[3])) + ((xi[4] + xi[5]) + (xi[6] + xi[7])));
+                if (bad)
+                    sx = __int_as_float(0x7fc00000);
+                sx += __shfl_xor_sync(0xffffffffu, sx, 1);
+                sx += __shfl_xor_sync(0xffffffffu, sx, 2);
                 if (active && (k0 % 32) == 0)
                     reinterpret_cast<float4 *>(cf)[(size_t)m * (Kpad / 32) + k0 / 32] =
-                        make_float4(pow2f(-pw), s_even, s_odd, 0.f);
-            } else if constexpr (WK == W_INT8) {
-                // sums of x' over the chunk's first and last 16 columns (the two
-                // lanes of the chunk): blocks t = 0, 1 and t = 2, 3
-                float sh = 0.f;
-#pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    sh += xq[i];
-                sh += __shfl_xor_sync(0xffffffffu, sh, 1);
-                const float other = __shfl_xor_sync(0xffffffffu, sh, 2);
-                if (active && (k0 % 32) == 0)
-                    reinterpret_cast<float4 *>(cf)[(size_t)m * (Kpad / 32) + k0 / 32] =
-                        make_float4(pow2f(-pw), sh, other, 0.f);
+                        make_float4(pow2f(-pw), sx, 0.f, 0.f);
             } else {
-                if (active && (k0 % 32) == 0)
-                    cf[(size_t)m * (Kpad / 32) + k0 / 32] = pow2f(-pw);
+                float xq[8];
+                uint32_t h[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    __half2 hh;
+                    if constexpr (WK == W_INT4)   // pairs (x'[t], x'[t+4])
+                        hh = __floats2half2_rn(f[i] * up, f[i + 4] * up);
+                    else                          // natural order
+                        hh = __floats2half2_rn(f[2 * i] * up, f[2 * i + 1] * up);
+                    h[i] = *reinterpret_cast<uint32_t *>(&hh);
+                    xq[2 * i] = __low2float(hh);
+                    xq[2 * i + 1] = __high2float(hh);
+                }
+                if (active)
+                    reinterpret_cast<uint4 *>(xs + (size_t)m * Kpad)[xs_vec_index_kind<WK>(k0)] =
+                        make_uint4(h[0], h[1], h[2], h[3]);
+                if constexpr (WK == W_INT4) {
+                    // h[i] holds columns (i, i+4): even columns are i = 0, 2
+                    float s_even = (xq[0] + xq[1]) + (xq[4] + xq[5]);
+                    float s_odd = (xq[2] + xq[3]) + (xq[6] + xq[7]);
+                    s_even += __shfl_xor_sync(0xffffffffu, s_even, 1);
+                    s_even += __shfl_xor_sync(0xffffffffu, s_even, 2);
+                    s_odd += __shfl_xor_sync(0xffffffffu, s_odd, 1);
+                    s_odd += __shfl_xor_sync(0xffffffffu, s_odd, 2);
+                    if (active && (k0 % 32) == 0)
+                        reinterpret_cast<float4 *>(cf)[(size_t)m * (Kpad / 32) + k0 / 32] =
+                            make_float4(pow2f(-pw), s_even, s_odd, 0.f);
+                } else if constexpr (WK == W_INT8) {
+                    // sums of x' over the chunk's first and last 16 columns (the two
+                    // lanes of the chunk): blocks t = 0, 1 and t = 2, 3
+                    float sh = 0.f;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        sh += xq[i];
+                    sh += __shfl_xor_sync(0xffffffffu, sh, 1);
+                    const float other = __shfl_xor_sync(0xffffffffu, sh, 2);
+                    if (active && (k0 % 32) == 0)
+                        reinterpret_cast<float4 *>(cf)[(size_t)m * (Kpad / 32) + k0 / 32] =
+                            make_float4(pow2f(-pw), sh, other, 0.f);
+                } else {
+                    if (active && (k0 % 32) == 0)
+                        cf[(size_t)m * (Kpad / 32) + k0 / 32] = pow2f(-pw);
+                }
             }
             (void)CH;
         }

@@ -1,10 +1,11 @@
-"""Worst cases of the fp16 partial sums in the whole-row GEMV.
+"""Worst cases of the partial sums in the whole-row GEMV.
 
 Every x value of a 32-column chunk sits at the top of the prescale range
 (|x| = 1.9921875, the largest bf16 below 2) and every code is at the extreme of
-one sign, so each eight-product half-group sum reaches its largest magnitude:
-NVFP4 8 * 6 * 1020 = 48,960 and int4 8 * 8 * 510 = 32,640, both below the fp16
-maximum of 65,504.  Outputs must be finite and within the stated tolerance of the
+one sign.  NVFP4 sums each eight-product half-group in fp16, which then reaches
+8 * 6 * 1020 = 48,960, below the fp16 maximum of 65,504; int4 sums c * x' in
+int32 with x' in int16, which then reaches 32 * 15 * 32,640 per lane, below 2^24
+(exact in fp32).  Outputs must be finite and within the stated tolerance of the
 fp64 oracle, for one and four tokens and for K = 2048 and 8192."""
 from __future__ import annotations
 
