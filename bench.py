@@ -35,6 +35,8 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "4-bit decode GEMV µs/call & effective weight GB/s (% of GB300 HBM peak)"
+# GB300 HBM3e nominal bandwidth; fractions are reported against it beside the measured peak
+HBM_NOMINAL_GBS = 8000.0
 
 # DRAM traffic of one launch of the decode GEMV kernel on a workload, from the ncu
 # capture summarised in profiles/ (dram__bytes_read.sum + dram__bytes_write.sum),
@@ -330,6 +332,7 @@ def run_decode_step(args, device):
     gbs = wbytes / (ms * 1e-3) / 1e9
     return {"workload": c["name"], "ms_per_step": round(ms, 4), "weight_bytes": wbytes,
             "value": round(gbs, 1), "unit": "GB/s", "hbm_frac": round(gbs / peak, 4),
+            "hbm_frac_nominal": round(gbs / HBM_NOMINAL_GBS, 4),
             "steps_per_s": round(1e3 / ms, 1), "launches_per_step": launches,
             "fused_projections": fuse, "pdl": not args.no_pdl}
 
@@ -368,6 +371,7 @@ def run_batched(args, device):
         gbs = wb / (ms * 1e-3) / 1e9
         out["sweep"].append({"M": M, "us_per_step": round(ms * 1e3, 3), "weight_GBps": round(gbs, 1),
                              "hbm_frac": round(gbs / peak, 4),
+                             "hbm_frac_nominal": round(gbs / HBM_NOMINAL_GBS, 4),
                              "tflops": round(flops / (ms * 1e-3) / 1e12, 2)})
     return out
 
@@ -450,7 +454,8 @@ def run_quantize(args, device):
             nbytes = 2 * N * K + layout.weight_bytes(lay, N, K)
             gbs = nbytes / (ms * 1e-3) / 1e9
             res["runs"].append({"layout": lay, "N": N, "K": K, "us": round(ms * 1e3, 2),
-                                "GBps": round(gbs, 1), "hbm_frac": round(gbs / peak, 4)})
+                                "GBps": round(gbs, 1), "hbm_frac": round(gbs / peak, 4),
+                                "hbm_frac_nominal": round(gbs / HBM_NOMINAL_GBS, 4)})
     return res
 
 
@@ -639,6 +644,7 @@ def run_gpu(args, world, rank, local):
             "unit": "GB/s",
             "us_per_call": round(us_per_call, 4),
             "hbm_frac": round(gbs / peak, 4),
+            "hbm_frac_nominal": round(gbs / HBM_NOMINAL_GBS, 4),
             "n_gpus": world,
             "steps": K,
             "warmup": W,
