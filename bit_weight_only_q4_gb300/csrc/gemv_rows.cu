@@ -492,7 +492,10 @@ q4_status rows_plan(const DeviceInfo &dev, int kind, int M, int N, int K, RowsPl
     const int kstep = rows_kstep(kind);
     const int ch = (kind == W_INT4 || kind == W_INT8) ? 4 : (kind == W_BF16 ? 0 : 1);
     plan.S = (K + kstep - 1) / kstep;
-    plan.mt = M >= 4 ? 4 : (M >= 2 ? 2 : 1);
+    // one launch per 1, 2 or 4 tokens; three tokens take the 4-token kernel once
+    // (weights read once: 17.7 against 20.6 us per NVFP4 batched-decode step as
+    // a 2-token plus a 1-token launch)
+    plan.mt = M >= 3 ? 4 : (M >= 2 ? 2 : 1);
     if (plan.S > 8)
         plan.mt = 1;                 // 16 k-steps need the 16-warp one-token CTA
     plan.rb = plan.mt == 4 ? 2 : 4;
