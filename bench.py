@@ -43,7 +43,7 @@ HBM_NOMINAL_GBS = 8000.0
 # valid only for the kernel sources it was taken on (see _kernel_sha).
 TRAFFIC = {
     # workload key: (bytes per launch, _kernel_sha() when captured)
-    "nvfp4_gemv": (18909440, "2b145ea31d864149c9eade65bb298fcc31bff4edc24232aa8c78985c69b44a16"),
+    "nvfp4_gemv": (18909696, "01679d37bf9ba940bad72912410666bbb61219e6e8173f33854acf787cfbb8c4"),
 }
 
 

@@ -1,6 +1,7 @@
-// Pieces shared by the two CUDA-core weight-streaming kernels (register path in
-// gemv.cu, bulk-copy path in gemv_bulk.cu): the unit geometry, the staging of x
-// in shared memory and the in-register decode + dot product of one unit.
+// Pieces shared by the CUDA-core weight-streaming kernels (whole-row kernel in
+// gemv_rows.cu, register path in gemv.cu, bulk-copy path in gemv_bulk.cu): the
+// unit geometry, the staging of x in shared memory and the in-register decode +
+// dot product of one unit.
 //
 // Arithmetic (both 4-bit layouts): x is staged as fp16 values x' = x * 2^p with
 // one power-of-two p per 32-column chunk, chosen so the chunk's largest |x'| lies
