@@ -544,16 +544,16 @@ q4_status rows_launch(const RowsPlan &plan, GemvParams p, int M, cudaStream_t st
     p.grid = plan.grid;
     p.rows_q = p.N / plan.grid;
     p.rows_r = p.N % plan.grid;
-    // A chained one-token call of a 4-bit layout whose warps own more rows than
-    // their registers and ring request before the wait (the rest are requested
-    // while the call computes) holds its ring requests back by 300 ns: the
-    // register rows go out at once, and the ring burst no longer lands on the
-    // running call's x staging and refills.  Measured on NVFP4 16384 x 2048:
-    // 4.80 against 5.19 us per chained call; int4 at that shape 6.27 against
-    // 6.29; shapes whose rows all fit the pre-wait requests lose 3-14% with any
-    // delay and keep none.
+    // A chained one-token NVFP4 call whose warps own more rows than their
+    // registers and ring request before the wait (the rest are requested while
+    // the call computes) holds its ring requests back by 300 ns: the register
+    // rows go out at once, and the ring burst no longer lands on the running
+    // call's x staging and refills.  Measured on 16384 x 2048: 4.80 against
+    // 5.19 us per chained call.  int4 at that shape is 1.3-1.8% faster without
+    // it (4.83 against 4.89-4.92 us), and shapes whose rows all fit the
+    // pre-wait requests lose 3-14% with any delay; neither uses it.
     p.ring_defer_ns = 0;
-    if (pdl && plan.mt == 1 && (plan.kind == W_NVFP4_A16 || plan.kind == W_INT4)) {
+    if (pdl && plan.mt == 1 && plan.kind == W_NVFP4_A16) {
         const int G = rows_warps(plan) / plan.S;
         const int64_t per_warp = ((int64_t)(p.rows_q + (p.rows_r ? 1 : 0)) + G - 1) / G;
         if (per_warp > (int64_t)plan.rb * (1 + plan.nb))
