@@ -43,7 +43,7 @@ HBM_NOMINAL_GBS = 8000.0
 # valid only for the kernel sources it was taken on (see _kernel_sha).
 TRAFFIC = {
     # workload key: (bytes per launch, _kernel_sha() when captured)
-    "nvfp4_gemv": (18909696, "01679d37bf9ba940bad72912410666bbb61219e6e8173f33854acf787cfbb8c4"),
+    "nvfp4_gemv": (18909696, "626568acef56ef9115b723634b4612cfd8ace1802f241bbb525766e307460d18"),
 }
 
 
