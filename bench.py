@@ -98,6 +98,13 @@ def _kernel_sha() -> str:
     return h.hexdigest()
 
 
+def traffic_for(workload: str):
+    """DRAM bytes per launch recorded for `workload` from an ncu capture, or None
+    when nothing was recorded or the kernel sources changed since the capture."""
+    t = TRAFFIC.get(workload)
+    return t[0] if t and t[1] == _kernel_sha() else None
+
+
 class ClockSampler:
     """nvidia-smi samples of SM clock and throttle reasons during a region."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -628,10 +635,7 @@ def run_gpu(args, world, rank, local):
     e2e_us = e2e_ms * 1e3 / Ke
     e2e_gbs = wl.bytes_per_call / (e2e_us * 1e-6) / 1e9
     peak, peak_src = _peaks()
-    traffic = None
-    t = TRAFFIC.get(args.workload)
-    if t and t[1] == _kernel_sha():
-        traffic = t[0]
+    traffic = traffic_for(args.workload)
 
     cpu_baseline = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -60,3 +60,22 @@ def test_reference_arm_prints_one_json_line():
     assert d["impl"] == "reference" and d["unit"] == "GB/s" and d["value"] > 0
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
     assert d["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_traffic_figure_only_for_the_sources_it_was_captured_on(monkeypatch):
+    sys.path.insert(0, ROOT)
+    import bench
+    sha = bench._kernel_sha()
+    assert len(sha) == 64
+    monkeypatch.setattr(bench, "TRAFFIC", {"w": (123, sha), "old": (456, "0" * 64)})
+    assert bench.traffic_for("w") == 123
+    assert bench.traffic_for("old") is None          # kernel changed since the capture
+    assert bench.traffic_for("missing") is None
+
+
+def test_kernel_hash_covers_the_gemv_sources():
+    sys.path.insert(0, ROOT)
+    import bench
+    for rel in bench.KERNEL_SOURCES:
+        assert os.path.exists(os.path.join(ROOT, rel)), rel
+    assert any(rel.endswith("gemv_rows.cu") for rel in bench.KERNEL_SOURCES)
