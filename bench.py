@@ -203,7 +203,7 @@ class Workload:
             self.desc = c["name"]
             base = P.int4_dev(w)
         else:
-            raise ValueError(f"workload {name} is not a bench line of this build")
+            raise ValueError(f"workload {name} has no GEMV bench line")
         self.x_host_bits = x
         self.x = P.bf16_dev(x).to(device)
         self.bytes_per_call = layout.linear_bytes(self.layout, self.M, self.N, self.K)
