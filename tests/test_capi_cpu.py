@@ -131,3 +131,4 @@ def test_layout_byte_accounting():
     assert layout.weight_bytes("int4", 2048, 2048) == 2048 * 1024 + 4 * 2048 * 16
     assert layout.linear_bytes("int4", 1, 2048, 2048) == 2236416
     assert layout.linear_bytes("nvfp4", 1, 16384, 2048) == 18911236
+

@@ -315,6 +315,10 @@ def test_int4_layout_bytes_reproduce_checkpoint_size():
     body = nums["model_params"] - emb
     total = body * int4_bytes_per_weight() + emb * 1 + V * 2 + head_rows * H * 2
     assert abs(total / 1e9 - nums["int4_checkpoint_gb"]) < 0.01
+    # fp32 scale and min, groups of 64, or no scale and min at all miss the file size
+    for alt in (0.5 + 2 * 4 / 128, 0.5 + 2 * 2 / 64, 0.5):
+        alt_total = body * alt + emb * 1 + V * 2 + head_rows * H * 2
+        assert abs(alt_total / 1e9 - nums["int4_checkpoint_gb"]) > 0.05, alt
     assert nums["codebook_head_rows"] == 2048 + 1
     assert int4_bytes_per_weight() == 0.5 + 2 * 2 / nums["group_size_int4"]
 
