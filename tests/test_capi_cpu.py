@@ -125,6 +125,36 @@ def test_dequant_arguments_are_rejected_before_launch(lib):
     assert lib.q4_dequant_nvfp4_f32(FAKE, FAKE, FAKE, FAKE + 4, 4, 32, None) == 3
 
 
+
+def test_int8_embedding_quantiser_and_noalloc_arguments_are_rejected_before_launch(lib):
+    """Every other entry point validates pointers, shapes and alignment on the
+    host and launches nothing on failure (status 1 NULL, 2 shape, 3 alignment)."""
+    # q4_linear_int8(x, qweight, scale, y, M, N, K, stream): K % 16, K >= 16
+    i8 = lambda x=FAKE, w=FAKE, s=FAKE, y=FAKE, M=1, N=64, K=128: \
+        lib.q4_linear_int8(x, w, s, y, M, N, K, None)
+    assert i8(s=None) == 1 and i8(x=None) == 1 and i8(y=None) == 1
+    assert i8(K=24) == 2 and i8(K=8) == 2 and i8(M=0) == 2 and i8(N=0) == 2
+    assert i8(x=FAKE + 8) == 3 and i8(w=FAKE + 4) == 3 and i8(s=FAKE + 1) == 3
+    assert i8(K=16384) == 2                               # beyond the whole-row kernel
+    # q4_embedding_int8(ids, qweight, scale, out, M, V, H, stream): H % 16
+    emb = lambda ids=FAKE, w=FAKE, s=FAKE, o=FAKE, M=1, V=100, H=2048: \
+        lib.q4_embedding_int8(ids, w, s, o, M, V, H, None)
+    assert emb(ids=None) == 1 and emb(o=None) == 1
+    assert emb(M=0) == 2 and emb(V=0) == 2 and emb(H=24) == 2
+    assert emb(ids=FAKE + 2) == 3 and emb(w=FAKE + 8) == 3 and emb(o=FAKE + 8) == 3
+    # quantisers: int4 needs K % 128, NVFP4 K % 16
+    qi = lambda w=FAKE, q=FAKE, s=FAKE, m=FAKE, N=4, K=256: \
+        lib.q4_quantize_int4g128(w, q, s, m, N, K, None)
+    assert qi(m=None) == 1 and qi(K=200) == 2 and qi(N=0) == 2 and qi(w=FAKE + 4) == 3
+    qn = lambda w=FAKE, c=FAKE, s=FAKE, g=FAKE, N=4, K=256: \
+        lib.q4_quantize_nvfp4(w, c, s, g, N, K, None)
+    assert qn(g=None) == 1 and qn(K=24) == 2 and qn(w=FAKE + 8) == 3 and qn(g=FAKE + 2) == 3
+    # the allocation-free int4 entry: same checks as the workspace form
+    na = lambda x=FAKE, w=FAKE, s=FAKE, m=FAKE, y=FAKE, M=1, N=64, K=2048: \
+        lib.q4_linear_int4g128_noalloc(x, w, s, m, y, M, N, K, None)
+    assert na(y=None) == 1 and na(K=100) == 2 and na(M=0) == 2 and na(x=FAKE + 8) == 3
+    assert lib.q4_last_error_string() != b""
+
 def test_layout_byte_accounting():
     assert layout.int4_bytes_per_weight() == 0.53125
     assert layout.nvfp4_bytes_per_weight() == 0.5625
