@@ -24,8 +24,12 @@
  *     scales uint8 [N, K/16] (one per 16 columns), one fp32 global scale per
  *     matrix which multiplies: w[n,k] = E2M1(code) * e4m3(scale[n,k/16]) * g.
  *     Activations stay BF16 (there is no activation scale).
- * Activations x and outputs y are bf16; accumulation is fp32 and the output is
- * rounded to bf16 (round to nearest even).
+ * Activations x and outputs y are bf16; the output is rounded to bf16 (round to
+ * nearest even) from an fp32 row sum.  Below five tokens that sum is built from
+ * exact int32 dot products (int4, x scaled to int16 per 32 columns) or from fp16
+ * partial sums of at most eight products per half group (NVFP4); from five tokens
+ * on, the tensor cores multiply fp16 operands (x, and the int4 weights rounded once
+ * to fp16) into fp32 accumulators.
  */
 #ifndef Q4_GB300_H
 #define Q4_GB300_H
