@@ -2,14 +2,16 @@
 
 Default workload: NVFP4 weight-only GEMV at batch 1, K=2048 -> N=16384 (seeded
 synthetic weights: E2M1 codes uniform over 16 values, e4m3 group-16 scales from
-U[0.25, 4], global scale 1e-2; x ~ N(0,1) in bf16).  One step is one call of the
-whole path (E2M1/e4m3 decode, dot products, split-K fixup, bf16 store).
+U[0.25, 4], global scale 1e-2; x ~ N(0,1) in bf16).  Each call runs the whole
+path (E2M1/e4m3 decode, dot products, bf16 store).
 
 Timing: the calls rotate over enough copies of the weights to cover 4x the L2
-cache, so every call streams its weights from HBM.  W warm-up steps, then K timed
-steps, replayed from CUDA graphs and bracketed by CUDA events on the launching
-stream with a barrier + synchronize on both sides; the max over ranks is taken.
-`value` is the effective weight bandwidth (algorithmic bytes / time per call).
+cache, so every call streams its weights from HBM.  One step is about 8,192
+chained calls: whole passes over that ring of copies, replayed from one CUDA
+graph of one pass.  W warm-up steps replay the same graph, then K timed steps
+are bracketed by CUDA events on the launching stream with a barrier +
+synchronize on both sides; the max over ranks is taken.  `value` is the
+effective weight bandwidth (algorithmic bytes / time per call).
 The `e2e` key repeats the measurement through the same public call with the
 activations copied in from pinned host memory and the result copied back every
 step (copies on their own streams, device x and y double-buffered, so one step's
@@ -37,6 +39,10 @@ if ROOT not in sys.path:
 METRIC = "4-bit decode GEMV µs/call & effective weight GB/s (% of GB300 HBM peak)"
 # GB300 HBM3e nominal bandwidth; fractions are reported against it beside the measured peak
 HBM_NOMINAL_GBS = 8000.0
+# Chained calls per bench step (rounded up to whole passes over the weight ring):
+# a step lasts tens of milliseconds, so a 20-step timed region spans several
+# clock samples and the per-call time is a steady-state figure.
+CALLS_PER_STEP = 8192
 
 # DRAM traffic of one launch of the decode GEMV kernel on a workload, from the ncu
 # capture summarised in profiles/ (dram__bytes_read.sum + dram__bytes_write.sum),
@@ -170,10 +176,9 @@ class Workload:
     """Seeded inputs on the device, a ring of weight copies and one call per step."""
 
     def __init__(self, name: str, device):
-        import numpy as np
         import torch
         from bit_weight_only_q4_gb300 import layout, q4, synth
-        from tests import parity as P
+        from bit_weight_only_q4_gb300 import upload as P
         self.name = name
         self.torch = torch
         self.q4 = q4
@@ -193,8 +198,7 @@ class Workload:
             self.M, self.N, self.K = c["M"], c["N"], c["K"]
             self.layout = "int8"
             self.desc = c["name"]
-            base = (torch.from_numpy(w.qweight),
-                    torch.from_numpy(w.scale.view(np.int16)).view(torch.float16))
+            base = P.int8_dev(w)
         elif name == "int4_gemv":
             c = synth.INT4_GEMV_2048
             x, w = synth.int4_gemv_2048()
@@ -277,7 +281,7 @@ def run_decode_step(args, device):
     Replayed from one CUDA graph; 1.007 GB of weights per step."""
     import torch
     from bit_weight_only_q4_gb300 import layout, q4, synth
-    from tests import parity as P
+    from bit_weight_only_q4_gb300 import upload as P
     c = synth.DECODE_STACK_28
     H, F = c["hidden"], c["ffn"]
     fuse = not getattr(args, "no_fuse", False)
@@ -334,7 +338,7 @@ def run_decode_step(args, device):
         launches = len(synth.DECODE_LAYER_PROJS) * c["layers"] + 1
 
     stream = torch.cuda.Stream(device)
-    ms = _graph_time(torch, stream, step, 1, args.steps)
+    ms = _graph_time(torch, stream, step, 1, max(args.steps, 200))
     peak, _ = _peaks()
     gbs = wbytes / (ms * 1e-3) / 1e9
     return {"workload": c["name"], "ms_per_step": round(ms, 4), "weight_bytes": wbytes,
@@ -349,7 +353,7 @@ def run_batched(args, device):
     per step, weights rotating over >= 4x L2; swept over M."""
     import torch
     from bit_weight_only_q4_gb300 import layout, q4, synth
-    from tests import parity as P
+    from bit_weight_only_q4_gb300 import upload as P
     c = synth.NVFP4_BATCHED_48
     l2 = torch.cuda.get_device_properties(device).L2_cache_size
     out = {"workload": c["name"], "sweep": []}
@@ -372,7 +376,7 @@ def run_batched(args, device):
                 q4.q4_linear_nvfp4(xd, *ring[i % len(ring)], y=y, workspace=wsb)
 
         stream = torch.cuda.Stream(device)
-        ms = _graph_time(torch, stream, fn, R, max(3, args.steps // R)) / R
+        ms = _graph_time(torch, stream, fn, R, max(20, args.steps // R)) / R
         wb = sum(layout.weight_bytes("nvfp4", N, K) for N, K in c["shapes"])
         flops = sum(2 * M * N * K for N, K in c["shapes"])
         gbs = wb / (ms * 1e-3) / 1e9
@@ -388,7 +392,7 @@ def run_prefill(args, device):
     K=8192 -> N=2048 (68.7 GFLOP each), tcgen05 path."""
     import torch
     from bit_weight_only_q4_gb300 import q4, synth
-    from tests import parity as P
+    from bit_weight_only_q4_gb300 import upload as P
     c = synth.PREFILL_2048
     res = {"workload": c["name"], "gemms": []}
     bf16_peak = _bf16_peak()
@@ -406,7 +410,7 @@ def run_prefill(args, device):
                 wsb = q4.alloc_workspace(q4.LAYOUT_NVFP4, c["M"], N, K, device)
                 fn = lambda i, xd=xd, wd=wd, y=y, wsb=wsb: q4.q4_linear_nvfp4(xd, *wd, y=y, workspace=wsb)
             stream = torch.cuda.Stream(device)
-            ms = _graph_time(torch, stream, fn, 10, max(3, args.steps // 10)) / 10
+            ms = _graph_time(torch, stream, fn, 10, max(20, args.steps // 10)) / 10
             tf = 2 * c["M"] * N * K / (ms * 1e-3) / 1e12
             res["gemms"].append({"layout": lay, "N": N, "K": K, "us": round(ms * 1e3, 2),
                                  "tflops": round(tf, 1), "tensor_frac": round(tf / bf16_peak, 4)})
@@ -431,7 +435,7 @@ def run_embedding(args, device):
         out = torch.empty((M, H), dtype=torch.bfloat16, device=device)
         fn = lambda i, ids=ids, out=out: q4.q4_embedding_int8(ids, q, sc, out=out)
         stream = torch.cuda.Stream(device)
-        ms = _graph_time(torch, stream, fn, 50, max(3, args.steps // 50)) / 50
+        ms = _graph_time(torch, stream, fn, 50, max(20, args.steps // 50)) / 50
         nbytes = M * (H + 2 + 2 * H + 4)
         res["runs"].append({"M": M, "us_per_call": round(ms * 1e3, 3),
                             "GBps": round(nbytes / (ms * 1e-3) / 1e9, 1)})
@@ -457,7 +461,7 @@ def run_quantize(args, device):
             else:
                 fn = lambda i, w=w: q4.q4_quantize_nvfp4(w)
             stream = torch.cuda.Stream(device)
-            ms = _graph_time(torch, stream, fn, 5, max(3, args.steps // 5)) / 5
+            ms = _graph_time(torch, stream, fn, 5, max(20, args.steps // 5)) / 5
             nbytes = 2 * N * K + layout.weight_bytes(lay, N, K)
             gbs = nbytes / (ms * 1e-3) / 1e9
             res["runs"].append({"layout": lay, "N": N, "K": K, "us": round(ms * 1e3, 2),
@@ -499,7 +503,7 @@ def run_profile(args, local):
     import torch
     from bit_weight_only_q4_gb300 import build as libbuild
     from bit_weight_only_q4_gb300 import q4, synth
-    from tests import parity as P
+    from bit_weight_only_q4_gb300 import upload as P
     torch.cuda.set_device(local)
     device = torch.device("cuda", local)
     libbuild.build()
@@ -545,25 +549,25 @@ def run_gpu(args, world, rank, local):
     stream = torch.cuda.Stream(device)
     R = wl.copies
     K, W = args.steps, args.warmup
+    # One step = P passes over the R-copy weight ring (R * P chained calls, about
+    # CALLS_PER_STEP), replayed from one graph of R calls.  Warm-up replays that
+    # same graph, so the timed region never holds a first replay.
+    P_ring = max(1, math.ceil(CALLS_PER_STEP / R))
+    calls_per_step = R * P_ring
 
-    # warm-up (also the first, uncaptured calls: plans and attributes cached)
     with torch.cuda.stream(stream):
-        for i in range(max(W, 1)):
+        for i in range(R):                 # first, uncaptured calls: plans and attributes cached
             wl.call(i)
     torch.cuda.synchronize()
     g_ring = _capture(torch, wl.call, R, stream)
-    g_tail = _capture(torch, wl.call, K % R, stream) if K % R else None
-    g_warm = _capture(torch, wl.call, W % R, stream) if W % R else None
-    warm = [(g_ring, W // R)] + ([(g_warm, 1)] if g_warm else [])
-    timed = [(g_ring, K // R)] + ([(g_tail, 1)] if g_tail else [])
-    _time_graphs(torch, stream, warm, world)
+    _time_graphs(torch, stream, [(g_ring, W * P_ring)], world)
 
     props = torch.cuda.get_device_properties(device)
     gpu_id = str(getattr(props, "uuid", local))
     if gpu_id and not gpu_id.startswith("GPU-") and "-" in gpu_id:
         gpu_id = "GPU-" + gpu_id
     with ClockSampler(gpu_id) as clk:
-        ms = _time_graphs(torch, stream, timed, world)
+        ms = _time_graphs(torch, stream, [(g_ring, K * P_ring)], world)
     ms = max_over_ranks(ms, world)
     clocks = clk.summary()
 
@@ -617,12 +621,9 @@ def run_gpu(args, world, rank, local):
     with torch.cuda.stream(stream):
         e2e_steps(3)
     torch.cuda.synchronize()
-    Ke = max(R, min(K, 20000))
     ge = e2e_graph(R)
-    ge_tail = e2e_graph(Ke % R) if Ke % R else None
-    _time_graphs(torch, stream, [(ge, 2)], world)
-    e2e_ms = _time_graphs(torch, stream, [(ge, Ke // R)] + ([(ge_tail, 1)] if ge_tail else []),
-                          world)
+    _time_graphs(torch, stream, [(ge, W * P_ring)], world)
+    e2e_ms = _time_graphs(torch, stream, [(ge, K * P_ring)], world)
     e2e_ms = max_over_ranks(e2e_ms, world)
     # each host buffer holds the result of the last step that used it
     torch.cuda.synchronize()
@@ -630,9 +631,9 @@ def run_gpu(args, world, rank, local):
         if not torch.equal(yh[b].view(torch.int16), yd[b].cpu().view(torch.int16)):
             raise SystemExit("end-to-end output copy does not match the device result")
 
-    us_per_call = ms * 1e3 / K
+    us_per_call = ms * 1e3 / (K * calls_per_step)
     gbs = wl.bytes_per_call / (us_per_call * 1e-6) / 1e9
-    e2e_us = e2e_ms * 1e3 / Ke
+    e2e_us = e2e_ms * 1e3 / (K * calls_per_step)
     e2e_gbs = wl.bytes_per_call / (e2e_us * 1e-6) / 1e9
     peak, peak_src = _peaks()
     traffic = traffic_for(args.workload)
@@ -666,7 +667,10 @@ def run_gpu(args, world, rank, local):
                 "algorithmic_bytes_per_call": wl.bytes_per_call,
                 "l2": f"weights rotate over {wl.copies} copies "
                       f"({wl.ring_bytes / 1e6:.0f} MB, >= 4x the {wl.l2 / 1e6:.0f} MB L2)",
-                "graph": "CUDA graph replay, one call per step",
+                "calls_per_step": calls_per_step,
+                "step": f"{calls_per_step} chained calls: {P_ring} passes over the "
+                        f"{R}-copy weight ring, replayed from one CUDA graph of {R} calls "
+                        f"(warm-up replays the same graph)",
                 "pdl": not args.no_pdl,
                 "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
             },
@@ -684,11 +688,11 @@ def run_gpu(args, world, rank, local):
                 "value": round(e2e_gbs * world, 2),
                 "unit": "GB/s",
                 "us_per_call": round(e2e_us, 4),
-                "h2d_bytes_per_step": int(wl.x.numel() * 2),
-                "d2h_bytes_per_step": int(wl.M * wl.N * 2),
-                "steps": Ke,
+                "h2d_bytes_per_step": int(wl.x.numel() * 2) * calls_per_step,
+                "d2h_bytes_per_step": int(wl.M * wl.N * 2) * calls_per_step,
+                "steps": K,
             },
-            "gpu_launches": K * wl.kernel_launches_per_step,
+            "gpu_launches": K * calls_per_step * wl.kernel_launches_per_step,
             "clocks": clocks,
             "cpu_baseline": cpu_baseline,
         }
@@ -755,10 +759,13 @@ def run_reference(args, world, rank):
     line = {
         "metric": METRIC, "impl": "reference", "value": cb["value"], "unit": "GB/s",
         "us_per_call": cb["us_per_call"], "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": cb["us_per_call"] / 1e3,
+        "warmup": args.warmup, "ms_per_step": cb["us_per_call"] * CALLS_PER_STEP / 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded PCG64)",
-        "config": {"workload": wl_desc},
+        "config": {"workload": wl_desc, "calls_per_step": CALLS_PER_STEP,
+                   "step": "each timed step runs the oracle once on a sample of rows; "
+                           "ms_per_step is the per-call time scaled to a step of "
+                           f"{CALLS_PER_STEP} calls"},
         "cpu_baseline": cb,
         "e2e": {"value": cb["value"], "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
@@ -769,8 +776,8 @@ def run_reference(args, world, rank):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200000)
-    ap.add_argument("--warmup", type=int, default=2000)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", choices=("nvfp4_gemv", "int4_gemv", "int8_gemv", "decode_step", "batched", "quantize", "embedding",
                                            "prefill"), default="nvfp4_gemv",

@@ -38,22 +38,18 @@ def _newest_header() -> float:
     return max((os.path.getmtime(h) for h in hdrs), default=0.0)
 
 
-def build(verbose: bool = False, jobs: int | None = None, defines: tuple[str, ...] = (),
-          out_dir: str | None = None, src_dir: str | None = None) -> str:
-    """Compile and link the library; ``defines`` (e.g. ``Q4_BULK_RW=2``),
-    ``out_dir`` and ``src_dir`` build a variant elsewhere without touching the
-    default build."""
+def build(verbose: bool = False, jobs: int | None = None) -> str:
+    """Compile and link the library (objects are rebuilt when out of date)."""
     nvcc = _nvcc()
-    csrc = src_dir or CSRC
-    out = out_dir or OUT
-    lib = os.path.join(out, os.path.basename(LIB))
+    csrc = CSRC
+    out = OUT
+    lib = LIB
     os.makedirs(out, exist_ok=True)
     srcs = sorted(glob.glob(os.path.join(csrc, "*.cu")))
     hdr_time = max(_newest_header(), max((os.path.getmtime(h) for h in
                                           glob.glob(os.path.join(csrc, "*.cuh"))), default=0.0))
     flags = ARCH + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
                     "-Xptxas", "-v" if verbose else "-O3", "-I", os.path.join(ROOT, "include")]
-    flags += [f"-D{d}" for d in defines]
 
     def compile_one(src: str) -> str:
         obj = os.path.join(out, os.path.basename(src)[:-3] + ".o")

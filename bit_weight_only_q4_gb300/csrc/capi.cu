@@ -5,11 +5,15 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <cuda.h>
 #include <mutex>
 
 #include "q4_internal.h"
 
 namespace q4 {
+
+// The library's device-side error word (Q4_DEVERR_* bits), one per device.
+__device__ unsigned g_q4_device_error;
 
 static thread_local char g_last_error[512] = "";
 // Smallest M served by the tcgen05 kernel (below it the CUDA-core streaming
@@ -62,6 +66,46 @@ q4_status current_device(DeviceInfo &out)
     return Q4_OK;
 }
 
+typedef CUresult (*CtxGetCurrentFn)(CUcontext *);
+
+void *current_context()
+{
+    static CtxGetCurrentFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<CtxGetCurrentFn>(p);
+    });
+    CUcontext c = nullptr;
+    if (!fn || fn(&c) != CUDA_SUCCESS)
+        return nullptr;
+    return c;
+}
+
+unsigned *device_error_flags()
+{
+    static std::mutex mu;
+    static void *ctx_of[64] = {};
+    static unsigned *addr[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+        return nullptr;
+    void *ctx = current_context();
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[dev] || !ctx || ctx_of[dev] != ctx) {
+        void *a = nullptr;
+        if (cudaGetSymbolAddress(&a, g_q4_device_error) != cudaSuccess)
+            return nullptr;
+        addr[dev] = static_cast<unsigned *>(a);
+        ctx_of[dev] = ctx;
+    }
+    return addr[dev];
+}
+
 static bool aligned(const void *p, size_t a) { return ((uintptr_t)p % a) == 0; }
 
 // Workspace layout: [tickets: u32, padded to 256 B][partials: fp32].
@@ -71,7 +115,7 @@ struct WsLayout {
 
 static size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-// Upper bound over every plan gemv_plan or bulk_plan can choose for this shape
+// Upper bound over every plan gemv_plan can choose for this shape
 // (independent of the device): partial slots for N rows rounded up to a whole
 // stage (64 rows) x k-steps x up to 4 tokens, one counter per row group.
 static WsLayout stream_ws_layout(int kind, int M, int N, int K)
@@ -110,7 +154,7 @@ static q4_status check_common(int M, int N, int K, void *ws, size_t ws_bytes, si
 }
 
 static q4_status run_stream(int kind, GemvParams p, int M, int N, int K, void *ws,
-                            cudaStream_t st, bool bulk_ok)
+                            cudaStream_t st)
 {
     DeviceInfo dev;
     q4_status s = current_device(dev);
@@ -121,24 +165,10 @@ static q4_status run_stream(int kind, GemvParams p, int M, int N, int K, void *w
     unsigned char *wsb = static_cast<unsigned char *>(ws);
     p.N = N;
     p.K = K;
-#ifndef Q4_PREFER_BULK
     if (rows_eligible(kind, K)) {
         RowsPlan plan;
         if ((s = rows_plan(dev, kind, M, N, K, plan)) == Q4_OK)
             return rows_launch(plan, p, M, st, pdl);
-    }
-#endif
-    if (bulk_ok && bulk_eligible(kind, K)) {
-        BulkPlan plan;
-        if ((s = bulk_plan(dev, kind, M, N, K, plan)) != Q4_OK)
-            return s;
-        const bool split = plan.ws_floats > 0;
-        if (split && (ws == nullptr || plan.ws_floats * 4 + L.partial_off > L.total ||
-                      plan.tickets * 4 > L.partial_off))
-            return fail(Q4_ERR_WORKSPACE, "internal: plan exceeds the workspace bound");
-        p.tickets = split ? reinterpret_cast<unsigned *>(wsb + L.tickets_off) : nullptr;
-        p.ws = split ? reinterpret_cast<float *>(wsb + L.partial_off) : nullptr;
-        return bulk_launch(plan, p, M, st, pdl);
     }
     GemvPlan plan;
     if ((s = gemv_plan(dev, kind, M, N, K, plan)) != Q4_OK)
@@ -180,7 +210,7 @@ const char *q4_last_error_string(void) { return g_last_error; }
 q4_status q4_set_launch_flags(unsigned flags)
 {
     const unsigned known =
-        Q4_FLAG_PDL | Q4_FLAG_FORCE_CUDA_CORE | Q4_FLAG_FORCE_TENSOR_CORE | Q4_FLAG_TC_SKINNY;
+        Q4_FLAG_PDL | Q4_FLAG_FORCE_CUDA_CORE | Q4_FLAG_FORCE_TENSOR_CORE;
     if (flags & ~known)
         return fail(Q4_ERR_ARG, "unknown launch flags 0x%x", flags & ~known);
     if ((flags & Q4_FLAG_FORCE_CUDA_CORE) && (flags & Q4_FLAG_FORCE_TENSOR_CORE))
@@ -239,7 +269,16 @@ q4_status q4_linear_int4g128(const void *x, const uint8_t *qweight, const void *
         ((flags & Q4_FLAG_FORCE_TENSOR_CORE) || M >= kTensorCoreMinM))
         return tc_launch(W_INT4, x, qweight, scale, minv, nullptr, y, M, N, K, workspace,
                          workspace_bytes, static_cast<cudaStream_t>(stream),
-                         (flags & Q4_FLAG_PDL) != 0, (flags & Q4_FLAG_TC_SKINNY) != 0);
+                         (flags & Q4_FLAG_PDL) != 0);
+    if (M == 1) {
+        DeviceInfo dev;
+        if ((s = current_device(dev)) != Q4_OK)
+            return s;
+        StagePlan sp;
+        if (stage_plan(dev, W_INT4, M, N, K, x, qweight, scale, minv, y, sp))
+            return stage_launch(sp, x, qweight, scale, minv, nullptr, y, N, K,
+                                static_cast<cudaStream_t>(stream), (flags & Q4_FLAG_PDL) != 0);
+    }
     GemvParams p = {};
     p.x = static_cast<const uint16_t *>(x);
     p.w = qweight;
@@ -251,8 +290,7 @@ q4_status q4_linear_int4g128(const void *x, const uint8_t *qweight, const void *
     p.row_begin = 0;
     p.n_rows = N;
     p.extra_row = -1;
-    const bool bulk_ok = aligned(scale, 16) && aligned(minv, 16);
-    return run_stream(W_INT4, p, M, N, K, workspace, static_cast<cudaStream_t>(stream), bulk_ok);
+    return run_stream(W_INT4, p, M, N, K, workspace, static_cast<cudaStream_t>(stream));
 }
 
 q4_status q4_linear_nvfp4(const void *x, const uint8_t *codes, const uint8_t *scale_e4m3,
@@ -279,7 +317,16 @@ q4_status q4_linear_nvfp4(const void *x, const uint8_t *codes, const uint8_t *sc
         ((flags & Q4_FLAG_FORCE_TENSOR_CORE) || M >= kTensorCoreMinM))
         return tc_launch(W_NVFP4_A16, x, codes, scale_e4m3, nullptr, global_scale, y, M, N, K,
                          workspace, workspace_bytes, static_cast<cudaStream_t>(stream),
-                         (flags & Q4_FLAG_PDL) != 0, (flags & Q4_FLAG_TC_SKINNY) != 0);
+                         (flags & Q4_FLAG_PDL) != 0);
+    if (M == 1 && K % 32 == 0) {
+        DeviceInfo dev;
+        if ((s = current_device(dev)) != Q4_OK)
+            return s;
+        StagePlan sp;
+        if (stage_plan(dev, W_NVFP4_A16, M, N, K, x, codes, scale_e4m3, nullptr, y, sp))
+            return stage_launch(sp, x, codes, scale_e4m3, nullptr, global_scale, y, N, K,
+                                static_cast<cudaStream_t>(stream), (flags & Q4_FLAG_PDL) != 0);
+    }
     GemvParams p = {};
     p.x = static_cast<const uint16_t *>(x);
     p.w = codes;
@@ -292,8 +339,7 @@ q4_status q4_linear_nvfp4(const void *x, const uint8_t *codes, const uint8_t *sc
     p.n_rows = N;
     p.extra_row = -1;
     const int kind = (K % 32 == 0) ? W_NVFP4_A16 : W_NVFP4_A8;
-    const bool bulk_ok = aligned(scale_e4m3, 16);
-    return run_stream(kind, p, M, N, K, workspace, static_cast<cudaStream_t>(stream), bulk_ok);
+    return run_stream(kind, p, M, N, K, workspace, static_cast<cudaStream_t>(stream));
 }
 
 q4_status audio_head_logits_restricted(const void *h, const void *head, int R_total,
@@ -323,7 +369,7 @@ q4_status audio_head_logits_restricted(const void *h, const void *head, int R_to
     p.row_begin = row_begin;
     p.n_rows = n_rows;
     p.extra_row = extra_row;
-    return run_stream(W_BF16, p, M, cols, H, nullptr, static_cast<cudaStream_t>(stream), true);
+    return run_stream(W_BF16, p, M, cols, H, nullptr, static_cast<cudaStream_t>(stream));
 }
 
 q4_status q4_device_error_flags(unsigned *flags, int clear)

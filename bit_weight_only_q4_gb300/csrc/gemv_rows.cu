@@ -31,8 +31,9 @@
 // cp.async ring did not help: 16 warps of cp.async per SM are throttled near
 // 34 GB/s, so fewer requests in flight let the first rows land sooner.)
 //
-// Eligibility: S = ceil(K / kstep) in {1, 2, 4, 8}; 16-byte aligned rows (int4
-// always, NVFP4 K % 32 == 0, bf16 H % 8 == 0).  Other shapes use gemv.cu.
+// Eligibility: S = ceil(K / kstep) rounded up to a power of two, at most 8 (16
+// for int8 at one token); 16-byte aligned rows (int4 always, NVFP4 K % 32 == 0,
+// bf16 H % 8 == 0).  Other shapes use gemv.cu.
 #include "q4_device.cuh"
 #include "q4_internal.h"
 #include "stream_common.cuh"
@@ -472,11 +473,23 @@ static int rows_kstep(int kind)
     return kind == W_BF16 ? 256 : (kind == W_INT8 ? 512 : 1024);
 }
 
-bool rows_eligible(int kind, int K)
+// k-steps of a row: ceil(K / kstep) rounded up to a power of two, so that the
+// warps of a CTA split evenly into row groups (the k-steps past K read nothing
+// and add zeros).
+static int rows_ksteps(int kind, int K)
 {
     const int kstep = rows_kstep(kind);
-    const int S = (K + kstep - 1) / kstep;
-    if (S != 1 && S != 2 && S != 4 && S != 8 && !(kind == W_INT8 && S == 16))
+    const int s = (K + kstep - 1) / kstep;
+    int S = 1;
+    while (S < s)
+        S *= 2;
+    return S;
+}
+
+bool rows_eligible(int kind, int K)
+{
+    const int S = rows_ksteps(kind, K);
+    if (S > 8 && !(kind == W_INT8 && S == 16))
         return false;
     if (kind == W_INT8) return K % 16 == 0;
     if (kind == W_INT4) return K % 128 == 0;
@@ -491,7 +504,7 @@ q4_status rows_plan(const DeviceInfo &dev, int kind, int M, int N, int K, RowsPl
     plan.kind = kind;
     const int kstep = rows_kstep(kind);
     const int ch = (kind == W_INT4 || kind == W_INT8) ? 4 : (kind == W_BF16 ? 0 : 1);
-    plan.S = (K + kstep - 1) / kstep;
+    plan.S = rows_ksteps(kind, K);
     // one launch per 1, 2 or 4 tokens; three tokens take the 4-token kernel once
     // (weights read once: 17.7 against 20.6 us per NVFP4 batched-decode step as
     // a 2-token plus a 1-token launch)

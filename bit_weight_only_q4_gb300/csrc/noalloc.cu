@@ -22,24 +22,30 @@ static __device__ __align__(256) unsigned char g_q4_static_scratch[kStaticScratc
 
 // Device address of the scratch array on the current device.  The host-side
 // name of a __device__ array is only a host stand-in, so the address is looked up
-// once per device (with that device current) and cached.
+// with cudaGetSymbolAddress, with the device current, the first time a device is
+// used, and cached for that device.  The cache also records the driver context
+// the lookup was made in: after a cudaDeviceReset the device gets a new context
+// (and the array a new address), so the lookup is made again there.
 static q4_status static_scratch_address(void **out)
 {
     static std::mutex mu;
     static void *addr[64] = {};
+    static void *ctx_of[64] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess)
         return cuda_fail(e, "cudaGetDevice");
     if (dev < 0 || dev >= 64)
         return fail(Q4_ERR_DEVICE, "device ordinal %d out of range", dev);
+    void *ctx = current_context();
     std::lock_guard<std::mutex> lock(mu);
-    if (!addr[dev]) {
+    if (!addr[dev] || !ctx || ctx_of[dev] != ctx) {
         void *p = nullptr;
         e = cudaGetSymbolAddress(&p, g_q4_static_scratch);
         if (e != cudaSuccess)
             return cuda_fail(e, "cudaGetSymbolAddress(static scratch)");
         addr[dev] = p;
+        ctx_of[dev] = ctx;
     }
     *out = addr[dev];
     return Q4_OK;

@@ -38,12 +38,7 @@ struct GemvParams {
     // whole-row kernels, one token: nanoseconds to hold the prologue's ring
     // requests back (0: issue at once)
     unsigned ring_defer_ns;
-    // bulk-copy path only
-    int64_t T;                // stages = row blocks * S
     int grid;                 // CTAs
-    int nst;                  // shared-memory ring depth
-    int consumers;            // consumer warps per CTA
-    unsigned *err;            // device error flags (bounded waits that timed out)
 };
 
 enum WeightKind { W_INT4 = 0, W_NVFP4_A16 = 1, W_NVFP4_A8 = 2, W_BF16 = 3, W_INT8 = 4 };
@@ -78,20 +73,6 @@ q4_status gemv_plan(const DeviceInfo &dev, int kind, int M, int N, int K, GemvPl
 q4_status gemv_launch(const GemvPlan &plan, GemvParams p, int M, cudaStream_t stream,
                       bool pdl);
 
-// ---- bulk-copy (TMA engine) weight-streaming kernel (gemv_bulk.cu)
-struct BulkPlan {
-    int kind = 0, mt = 1, rpw = 1, nst = 4, consumers = 16;
-    int64_t gran = 1;
-    int grid = 0;
-    size_t smem = 0;
-    int S = 0, G = 0;
-    int64_t B = 0, T = 0;
-    size_t ws_floats = 0, tickets = 0;
-};
-// Whether the bulk path can serve this shape (16-byte aligned row segments).
-bool bulk_eligible(int kind, int K);
-q4_status bulk_plan(const DeviceInfo &dev, int kind, int M, int N, int K, BulkPlan &plan);
-q4_status bulk_launch(const BulkPlan &plan, GemvParams p, int M, cudaStream_t stream, bool pdl);
 // ---- register-prefetch weight-streaming kernel (gemv_rows.cu)
 struct RowsPlan {
     int kind = 0, mt = 1, rb = 4, nb = 2, S = 1, grid = 0;
@@ -101,16 +82,35 @@ bool rows_eligible(int kind, int K);
 q4_status rows_plan(const DeviceInfo &dev, int kind, int M, int N, int K, RowsPlan &plan);
 q4_status rows_launch(const RowsPlan &plan, GemvParams p, int M, cudaStream_t stream, bool pdl);
 
+// ---- one-token GEMV with bulk-copy weight stages (gemv_stage.cu)
+struct StagePlan {
+    int kind = 0, grid = 0, ns = 0, rows_max = 0;
+    size_t smem = 0;
+};
+// Whether the staged kernel serves this call (M == 1, K a multiple of 2048 with
+// K / 2048 in {1, 2, 4, 8}, 16-byte aligned pointers, fits half an SM), and how.
+bool stage_plan(const DeviceInfo &dev, int kind, int M, int N, int K, const void *x,
+                const void *codes, const void *scale, const void *minv, const void *y,
+                StagePlan &plan);
+q4_status stage_launch(const StagePlan &plan, const void *x, const uint8_t *codes,
+                       const void *scale, const void *minv, const float *gscale, void *y, int N,
+                       int K, cudaStream_t stream, bool pdl);
+
 // ---- tcgen05 tensor-core GEMM (tc_gemm.cu)
 bool tc_eligible(int kind, int M, int N, int K);
 size_t tc_workspace_bytes(int M, int N, int K, int sms);
 q4_status tc_launch(int kind, const void *x, const uint8_t *codes, const void *scale,
                     const void *minv, const float *gscale, void *y, int M, int N, int K,
-                    void *ws, size_t ws_bytes, cudaStream_t stream, bool pdl,
-                    bool skinny);
+                    void *ws, size_t ws_bytes, cudaStream_t stream, bool pdl);
 
-// Device address of the library's error-flag word on the current device.
+// Device address of the library's error-flag word in the current context
+// (looked up once per device and context; nullptr if the lookup fails).
 unsigned *device_error_flags();
+
+// The current CUDA driver context (nullptr when none is current or the driver
+// entry point is unavailable); caches of device addresses are keyed on it, so a
+// context created after cudaDeviceReset gets fresh lookups.
+void *current_context();
 
 // ---- test-only dequantisers (dequant.cu)
 q4_status launch_dequant_int4(const uint8_t *q, const uint16_t *s, const uint16_t *m,

@@ -1,7 +1,7 @@
 // Pieces shared by the CUDA-core weight-streaming kernels (whole-row kernel in
-// gemv_rows.cu, register path in gemv.cu, bulk-copy path in gemv_bulk.cu): the
-// unit geometry, the staging of x in shared memory and the in-register decode +
-// dot product of one unit.
+// gemv_rows.cu, split-K register path in gemv.cu): the unit geometry, the
+// staging of x in shared memory and the in-register decode + dot product of one
+// unit.
 //
 // Arithmetic (both 4-bit layouts): x is staged as fp16 values x' = x * 2^p with
 // one power-of-two p per 32-column chunk, chosen so the chunk's largest |x'| lies
@@ -17,7 +17,7 @@
 //       A1 = sum_{even k} (1024 + c) x'   and   A2 = sum_{odd k} (1024 + 16 c) x'
 //     give  sum_k (c s + m) x' = s A1 + (s/16) A2 + (m - 1024 s) X1 + (m - 64 s) X2
 //     with X1, X2 the sums of x' over the chunk's even and odd columns (the
-//     split-K and bulk-copy kernels; the whole-row kernel stages int4 x as
+//     split-K kernel; the whole-row kernel stages int4 x as
 //     int16 and sums c x' exactly with integer dot products, see stage_x).
 #pragma once
 
@@ -130,7 +130,10 @@ __device__ void stage_x(const GemvParams &p, int Kpad, uint16_t *xs, float *cf, 
             // |c - 8| <= 8) stays below 2^16 when a kernel accumulates it in
             // fp16; int16 staging in [2^14, 2^15)
             int pw = (XI16 ? 15 : (WK == W_NVFP4_A16 ? 10 : (WK == W_INT4 ? 9 : 15))) - ex;
-            pw = pw > 100 ? 100 : (pw < -100 ? -100 : pw);
+            // |pw| <= 126 keeps 2^pw and 2^-pw normal fp32 numbers; the top of the
+            // bf16 range (amax < 2^128) needs pw >= 15 - 128 = -113, so no finite
+            // chunk is clamped at the top and every one lands in its target range
+            pw = pw > 126 ? 126 : (pw < -126 ? -126 : pw);
             const float up = pow2f(pw);
             if constexpr (XI16) {
                 // x * 2^p is exact in fp32 and below 2^15 in magnitude; rounding
@@ -204,75 +207,6 @@ __device__ void stage_x(const GemvParams &p, int Kpad, uint16_t *xs, float *cf, 
                 }
             }
             (void)CH;
-        }
-    }
-}
-
-// One lane's slice of x for the bulk kernel, loaded straight from global memory:
-// columns [col0, col0 + COLS) of every token, converted to the decoder's operand
-// format (the same values stage_x writes to shared memory), and its chunk data
-// (int4: 2^-p, X1, X2; NVFP4: 2^-p * g).  A 32-column chunk is exactly one lane's
-// slice, so the prescale needs no communication between lanes.
-template <int WK, int MT, int XV>
-__device__ __forceinline__ void load_x_slice(const GemvParams &p, int col0, float gsc,
-                                             uint32_t (&xr)[MT][XV], float4 (&cd)[MT])
-{
-#pragma unroll
-    for (int m = 0; m < MT; ++m) {
-        const bool ok = m < p.mcount && col0 < p.K;
-        const uint16_t *src = p.x + (int64_t)(p.m0 + m) * p.K + col0;
-        cd[m] = make_float4(1.f, 0.f, 0.f, 0.f);
-        if constexpr (WK == W_BF16) {
-            const uint4 v = ok ? *reinterpret_cast<const uint4 *>(src) : make_uint4(0u, 0u, 0u, 0u);
-            xr[m][0] = v.x; xr[m][1] = v.y; xr[m][2] = v.z; xr[m][3] = v.w;
-        } else {
-            uint32_t e[16];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const uint4 v = ok ? reinterpret_cast<const uint4 *>(src)[i]
-                                   : make_uint4(0u, 0u, 0u, 0u);
-                e[4 * i] = v.x; e[4 * i + 1] = v.y; e[4 * i + 2] = v.z; e[4 * i + 3] = v.w;
-            }
-            float f[32];
-            float amax = 0.f;
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                f[2 * i] = bf16_bits_to_f32(e[i] & 0xffffu);
-                f[2 * i + 1] = bf16_bits_to_f32(e[i] >> 16);
-                amax = fmaxf(amax, fmaxf(fabsf(f[2 * i]), fabsf(f[2 * i + 1])));
-            }
-            int ex = 0;
-            if (amax > 0.f && !isinf(amax)) {
-                const int be = (int)((__float_as_uint(amax) >> 23) & 0xff);
-                if (be > 0)
-                    ex = be - 126;
-                else
-                    frexpf(amax, &ex);
-            }
-            int pw = 15 - ex;
-            pw = pw > 100 ? 100 : (pw < -100 ? -100 : pw);
-            const float up = pow2f(pw);
-            float s_even = 0.f, s_odd = 0.f;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {        // 8-column block i
-#pragma unroll
-                for (int t = 0; t < 4; ++t) {
-                    __half2 hh;
-                    if constexpr (WK == W_INT4)  // pair (col t, col t + 4)
-                        hh = __floats2half2_rn(f[8 * i + t] * up, f[8 * i + t + 4] * up);
-                    else                         // pair (col 2t, col 2t + 1)
-                        hh = __floats2half2_rn(f[8 * i + 2 * t] * up, f[8 * i + 2 * t + 1] * up);
-                    xr[m][4 * i + t] = *reinterpret_cast<uint32_t *>(&hh);
-                    if constexpr (WK == W_INT4) {
-                        const float pr = __low2float(hh) + __high2float(hh);
-                        if (t % 2 == 0)
-                            s_even += pr;
-                        else
-                            s_odd += pr;
-                    }
-                }
-            }
-            cd[m] = make_float4(pow2f(-pw) * (WK == W_INT4 ? 1.f : gsc), s_even, s_odd, 0.f);
         }
     }
 }

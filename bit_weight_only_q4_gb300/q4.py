@@ -22,7 +22,6 @@ LAYOUT_NVFP4 = 1
 FLAG_PDL = 0x1
 FLAG_FORCE_CUDA_CORE = 0x2
 FLAG_FORCE_TENSOR_CORE = 0x4
-FLAG_TC_SKINNY = 0x8
 
 STATUS = {0: "Q4_OK", 1: "Q4_ERR_NULL", 2: "Q4_ERR_SHAPE", 3: "Q4_ERR_ALIGN",
           4: "Q4_ERR_WORKSPACE", 5: "Q4_ERR_ARG", 6: "Q4_ERR_CUDA", 7: "Q4_ERR_DEVICE"}
@@ -132,7 +131,8 @@ def get_launch_flags() -> int:
 
 
 def device_error_flags(clear: bool = True) -> int:
-    """Device error word (bit 0: a bounded in-kernel wait timed out). Synchronises."""
+    """Device error word (bit 0: a bounded in-kernel wait timed out; bit 2: an
+    embedding id out of range). Synchronises."""
     v = ctypes.c_uint(0)
     _check(load().q4_device_error_flags(ctypes.byref(v), 1 if clear else 0))
     return int(v.value)

@@ -28,8 +28,9 @@
  * nearest even) from an fp32 row sum.  Below five tokens that sum is built from
  * exact int32 dot products (int4, x scaled to int16 per 32 columns) or from fp16
  * partial sums of at most eight products per half group (NVFP4); from five tokens
- * on, the tensor cores multiply fp16 operands (x, and the int4 weights rounded once
- * to fp16) into fp32 accumulators.
+ * on, the tensor cores multiply fp16 operands (x scaled per token by a power of
+ * two that keeps every bf16 value in the fp16 range, and the int4 weights rounded
+ * once to fp16) into fp32 accumulators.
  */
 #ifndef Q4_GB300_H
 #define Q4_GB300_H
@@ -65,15 +66,10 @@ typedef enum {
  *     by the immediately preceding kernel.  Activations, outputs and workspace
  *     are touched only after the previous kernel has completed.
  *   Q4_FLAG_FORCE_CUDA_CORE / Q4_FLAG_FORCE_TENSOR_CORE: override the choice of
- *     kernel by M (testing and benchmarking only).
- *   Q4_FLAG_TC_SKINNY: on the tensor-core path, run tiles of at most 64 tokens
- *     on the skinny kernel (whole K range resident, A operand in tensor memory,
- *     cluster split-K) instead of the staged-ring kernel.  Experimental: on
- *     GB300 it is slower than the default at the sizes measured. */
+ *     kernel by M (testing and benchmarking only). */
 #define Q4_FLAG_PDL 0x1u
 #define Q4_FLAG_FORCE_CUDA_CORE 0x2u
 #define Q4_FLAG_FORCE_TENSOR_CORE 0x4u
-#define Q4_FLAG_TC_SKINNY 0x8u
 
 int q4_abi_version(void);
 const char *q4_status_string(q4_status s);
@@ -176,11 +172,6 @@ q4_status audio_head_logits_restricted(const void *h, const void *head, int R_to
  * with clear != 0 the word is reset to zero afterwards.
  */
 #define Q4_DEVERR_TIMEOUT 0x1u
-/* Bit 1: the tensor-core path (M >= 5, K % 64 == 0) met an activation whose
- * magnitude exceeds the fp16 range (65504); it converts x to fp16 internally, so
- * that output is not valid.  Activations inside the range are converted exactly
- * (down to 2^-17; smaller values are rounded to fp16 subnormals). */
-#define Q4_DEVERR_FP16_RANGE 0x2u
 /* Bit 2: q4_embedding_int8 met a token id outside 0 .. V-1 and wrote a row of
  * zeros for it. */
 #define Q4_DEVERR_INDEX 0x4u

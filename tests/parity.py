@@ -17,29 +17,9 @@ ABS_ADD = 1e-3
 FRO_MIN_ELEMS = 1024
 
 
-def bf16_dev(bits: np.ndarray, device="cuda") -> torch.Tensor:
-    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(device)
-
-
-def u8_dev(a: np.ndarray, device="cuda") -> torch.Tensor:
-    return torch.from_numpy(np.ascontiguousarray(a)).to(device)
-
-
-def f16_dev(bits: np.ndarray, device="cuda") -> torch.Tensor:
-    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.float16).to(device)
-
-
-def bf16_bits_host(t: torch.Tensor) -> np.ndarray:
-    return t.detach().contiguous().cpu().view(torch.int16).numpy().view(np.uint16).copy()
-
-
-def int4_dev(w):
-    return u8_dev(w.qweight), f16_dev(w.scale), f16_dev(w.minv)
-
-
-def nvfp4_dev(w):
-    g = torch.tensor([float(w.global_scale)], dtype=torch.float32, device="cuda")
-    return u8_dev(w.codes), u8_dev(w.scale), g
+# device upload helpers live in the package (bench.py uses them too)
+from bit_weight_only_q4_gb300.upload import (bf16_bits_host, bf16_dev, f16_dev, int4_dev,  # noqa: F401
+                                             int8_dev, nvfp4_dev, u8_dev)
 
 
 def check(y_gpu: torch.Tensor, y_ref: np.ndarray, abs_ref: np.ndarray, what: str = "",

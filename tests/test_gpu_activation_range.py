@@ -82,3 +82,39 @@ def test_nonfinite_x_poisons_only_its_token(q4, oracle_mod, layout, bad, M):
         else:
             yo, ao = oracle_mod.linear_nvfp4(x[1:], w.codes, w.scale, w.global_scale, with_abs=True)
         P.check(y[1:], yo, ao, f"{layout} token beside a non-finite one")
+
+
+def _x_extreme(rng: np.random.Generator, M: int, K: int) -> np.ndarray:
+    """N(0,1) bf16 activations with one 32-column chunk of every token moved up by
+    2^120 and another moved down by 2^-120 (exact: only the exponent field
+    changes), so the prescale of x must reach both ends of the bf16 range."""
+    x = synth.activations(rng, M, K)
+    e = (x >> 7) & 0xFF
+    up = slice(160, 192)
+    down = slice(640, 672)
+    eu = e[:, up].astype(np.int32)
+    x[:, up] = np.where(eu > 0, (x[:, up] & 0x807F) | ((eu + 120).astype(np.uint16) << 7), x[:, up])
+    ed = e[:, down].astype(np.int32)
+    x[:, down] = np.where(ed > 121, (x[:, down] & 0x807F) | ((ed - 120).astype(np.uint16) << 7),
+                          x[:, down])
+    return x
+
+
+@pytest.mark.parametrize("layout", ["int4", "nvfp4"])
+@pytest.mark.parametrize("M", [1, 3, 4])
+def test_chunks_near_both_ends_of_the_bf16_range(q4, oracle_mod, layout, M):
+    """A chunk whose largest |x| is about 2^121 (beyond the reach of a +-100
+    prescale) and one about 2^-118: outputs finite and within the oracle's bound."""
+    rng = synth.rng_for(94, M)
+    N, K = 640, 2048
+    x = _x_extreme(rng, M, K)
+    assert np.abs(x.view(np.int16).astype(np.int32) & 0x7F80).max() >= (247 << 7)
+    if layout == "int4":
+        w = synth.int4_matrix(rng, N, K)
+        y = q4.q4_linear_int4g128(P.bf16_dev(x), *P.int4_dev(w))
+        yo, ao = oracle_mod.linear_int4g128(x, w.qweight, w.scale, w.minv, with_abs=True)
+    else:
+        w = synth.nvfp4_matrix(rng, N, K)
+        y = q4.q4_linear_nvfp4(P.bf16_dev(x), *P.nvfp4_dev(w))
+        yo, ao = oracle_mod.linear_nvfp4(x, w.codes, w.scale, w.global_scale, with_abs=True)
+    P.check(y, yo, ao, f"{layout} chunks near 2^+-120, M={M}")

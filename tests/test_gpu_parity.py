@@ -254,3 +254,43 @@ def test_nvfp4_batched_sweep(q4, oracle_mod, shape_index, M):
     y = q4.q4_linear_nvfp4(P.bf16_dev(x), *P.nvfp4_dev(w))
     yo, ao = oracle_mod.linear_nvfp4(x, w.codes, w.scale, w.global_scale, with_abs=True)
     P.check(y, yo, ao, f"nvfp4 batched M={M} shape {shape_index}")
+
+
+# ------------------------------------------- k-step counts that are not powers of two
+@pytest.mark.parametrize("K", [3072, 6144, 12288])
+@pytest.mark.parametrize("M", [1, 3, 4])
+def test_k_not_a_power_of_two_ksteps(q4, oracle_mod, M, K):
+    """K = 3072 and 6144 (3 and 6 k-steps of 1024 columns) run the whole-row
+    kernel with its k-steps padded to 4 and 8 (the padded ones read nothing);
+    K = 12288 (12 k-steps) runs the split-K kernel.  Both layouts, 1-4 tokens."""
+    _int4_case(q4, oracle_mod, M, 1000, K, seed=5)
+    _nvfp4_case(q4, oracle_mod, M, 1000, K, seed=5)
+
+
+# ------------------------------------------ one-token staged kernel (K % 2048 == 0)
+@pytest.mark.parametrize("N,K", [(1, 2048), (17, 4096), (151, 2048), (152, 8192), (153, 2048),
+                                 (1000, 16384), (4099, 2048), (16384, 4096)])
+def test_one_token_staged_kernel_shapes(q4, oracle_mod, N, K):
+    """One token with K a multiple of 2048 runs the bulk-copy staged kernel: rows
+    fewer than, equal to and just above the SM count, rows per CTA that leave the
+    last stage partly empty, one to eight 2048-column units per row (partials of
+    a row summed by the last of its warps)."""
+    _int4_case(q4, oracle_mod, 1, N, K, seed=6)
+    _nvfp4_case(q4, oracle_mod, 1, N, K, seed=6)
+
+
+def test_one_token_unaligned_scales_take_the_whole_row_kernel(q4, oracle_mod):
+    """Scale arrays that are only 2-byte aligned cannot be bulk-copied: the call
+    falls back to the whole-row kernel with the same result (within tolerance)."""
+    rng = synth.rng_for(107)
+    N, K = 640, 2048
+    w = synth.int4_matrix(rng, N, K)
+    x = synth.activations(rng, 1, K)
+    q, s, m = P.int4_dev(w)
+    s2 = torch.empty(s.numel() + 1, dtype=torch.float16, device="cuda")[1:].view(s.shape)
+    m2 = torch.empty(m.numel() + 1, dtype=torch.float16, device="cuda")[1:].view(m.shape)
+    s2.copy_(s)
+    m2.copy_(m)
+    y = q4.q4_linear_int4g128(P.bf16_dev(x), q, s2, m2)
+    yo, ao = oracle_mod.linear_int4g128(x, w.qweight, w.scale, w.minv, with_abs=True)
+    P.check(y, yo, ao, "int4 one token, 2-byte aligned scales")
