@@ -275,22 +275,28 @@ def run_decode_step(args, device):
     """One decode step of the synthetic 28-layer int4 stack (hidden 2048, FFN
     8192): per layer q, k, v, gate, up read x; o reads v; down reads up; the
     next layer's x is down's output; then the restricted head (2049 rows).
-    Projections that share an input run as one call on their concatenated rows
-    (q|k|v: N = 6144; gate|up: N = 16384), 4 calls per layer + the head = 113
-    per step; --no-fuse runs the 7 separate calls per layer (197 per step).
+    Projections that share an input run as one call on their concatenated rows:
+    by default q|k|v|gate|up (N = 22528), then o and down read their inputs as
+    slices of that output, 3 calls per layer + the head = 85 per step;
+    --fusion pairs runs q|k|v (N = 6144) and gate|up (N = 16384) as two calls
+    (113 per step), --fusion none the 7 separate calls per layer (197 per step).
     Replayed from one CUDA graph; 1.007 GB of weights per step."""
     import torch
     from bit_weight_only_q4_gb300 import layout, q4, synth
     from bit_weight_only_q4_gb300 import upload as P
     c = synth.DECODE_STACK_28
     H, F = c["hidden"], c["ffn"]
-    fuse = not getattr(args, "no_fuse", False)
+    fusion = "none" if getattr(args, "no_fuse", False) else getattr(args, "fusion", "all")
+    fuse = fusion != "none"
     layers = []
     for layer in range(c["layers"]):
         m = {k: P.int4_dev(v) for k, v in synth.decode_stack_layer(layer).items()}
-        if fuse:
-            cat = lambda names: tuple(torch.cat([m[n][i] for n in names], 0).contiguous()
-                                      for i in range(3))
+        cat = lambda names: tuple(torch.cat([m[n][i] for n in names], 0).contiguous()
+                                  for i in range(3))
+        if fusion == "all":
+            layers.append({"f": cat(("q", "k", "v", "gate", "up")), "o": m["o"],
+                           "down": m["down"]})
+        elif fusion == "pairs":
             layers.append({"qkv": cat(("q", "k", "v")), "o": m["o"],
                            "gu": cat(("gate", "up")), "down": m["down"]})
         else:
@@ -298,13 +304,30 @@ def run_decode_step(args, device):
     head = P.bf16_dev(synth.decode_stack_head())
     x0 = P.bf16_dev(synth.decode_stack_input())
     logits = torch.empty((1, c["head_rows"]), dtype=torch.bfloat16, device=device)
-    shapes = [(3 * H, H), (H, H), (2 * F, H), (H, F)] if fuse else \
-        [(N, K) for _, N, K in synth.DECODE_LAYER_PROJS]
+    shapes = {"all": [(3 * H + 2 * F, H), (H, H), (H, F)],
+              "pairs": [(3 * H, H), (H, H), (2 * F, H), (H, F)],
+              "none": [(N, K) for _, N, K in synth.DECODE_LAYER_PROJS]}[fusion]
     ws_n = max(q4.workspace_bytes(q4.LAYOUT_INT4G128, 1, N, K) for N, K in shapes)
     ws = torch.zeros(ws_n, dtype=torch.uint8, device=device) if ws_n else None
     wbytes = sum(layout.weight_bytes("int4", N, K) for _, N, K in synth.DECODE_LAYER_PROJS) \
         * c["layers"] + 2 * c["head_rows"] * H
-    if fuse:
+    if fusion == "all":
+        y_f = torch.empty((1, 3 * H + 2 * F), dtype=torch.bfloat16, device=device)
+        y_o = torch.empty((1, H), dtype=torch.bfloat16, device=device)
+        y_down = torch.empty((1, H), dtype=torch.bfloat16, device=device)
+        v_view = y_f[:, 2 * H:3 * H]          # v's rows of the fused output
+        up_view = y_f[:, 3 * H + F:]          # up's rows
+
+        def step(_):
+            x = x0
+            for L in layers:
+                q4.q4_linear_int4g128(x, *L["f"], y=y_f, workspace=ws)
+                q4.q4_linear_int4g128(v_view, *L["o"], y=y_o, workspace=ws)
+                q4.q4_linear_int4g128(up_view, *L["down"], y=y_down, workspace=ws)
+                x = y_down
+            q4.audio_head_logits_restricted(x, head, 0, c["head_rows"], -1, logits=logits)
+        launches = 3 * c["layers"] + 1
+    elif fusion == "pairs":
         y_qkv = torch.empty((1, 3 * H), dtype=torch.bfloat16, device=device)
         y_o = torch.empty((1, H), dtype=torch.bfloat16, device=device)
         y_gu = torch.empty((1, 2 * F), dtype=torch.bfloat16, device=device)
@@ -345,7 +368,7 @@ def run_decode_step(args, device):
             "value": round(gbs, 1), "unit": "GB/s", "hbm_frac": round(gbs / peak, 4),
             "hbm_frac_nominal": round(gbs / HBM_NOMINAL_GBS, 4),
             "steps_per_s": round(1e3 / ms, 1), "launches_per_step": launches,
-            "fused_projections": fuse, "pdl": not args.no_pdl}
+            "fusion": fusion, "fused_projections": fuse, "pdl": not args.no_pdl}
 
 
 def run_batched(args, device):
@@ -785,7 +808,10 @@ def main(argv=None):
                          "measurement lines")
     ap.add_argument("--no-pdl", action="store_true")
     ap.add_argument("--no-fuse", action="store_true",
-                    help="decode_step: run q, k, v and gate, up as separate calls")
+                    help="decode_step: run q, k, v, gate, up as separate calls")
+    ap.add_argument("--fusion", choices=("all", "pairs", "none"), default="all",
+                    help="decode_step: q|k|v|gate|up as one call (all), q|k|v and "
+                         "gate|up (pairs), or separate calls (none)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--profile", action="store_true",

@@ -270,15 +270,6 @@ q4_status q4_linear_int4g128(const void *x, const uint8_t *qweight, const void *
         return tc_launch(W_INT4, x, qweight, scale, minv, nullptr, y, M, N, K, workspace,
                          workspace_bytes, static_cast<cudaStream_t>(stream),
                          (flags & Q4_FLAG_PDL) != 0);
-    if (M == 1) {
-        DeviceInfo dev;
-        if ((s = current_device(dev)) != Q4_OK)
-            return s;
-        StagePlan sp;
-        if (stage_plan(dev, W_INT4, M, N, K, x, qweight, scale, minv, y, sp))
-            return stage_launch(sp, x, qweight, scale, minv, nullptr, y, N, K,
-                                static_cast<cudaStream_t>(stream), (flags & Q4_FLAG_PDL) != 0);
-    }
     GemvParams p = {};
     p.x = static_cast<const uint16_t *>(x);
     p.w = qweight;
@@ -318,15 +309,6 @@ q4_status q4_linear_nvfp4(const void *x, const uint8_t *codes, const uint8_t *sc
         return tc_launch(W_NVFP4_A16, x, codes, scale_e4m3, nullptr, global_scale, y, M, N, K,
                          workspace, workspace_bytes, static_cast<cudaStream_t>(stream),
                          (flags & Q4_FLAG_PDL) != 0);
-    if (M == 1 && K % 32 == 0) {
-        DeviceInfo dev;
-        if ((s = current_device(dev)) != Q4_OK)
-            return s;
-        StagePlan sp;
-        if (stage_plan(dev, W_NVFP4_A16, M, N, K, x, codes, scale_e4m3, nullptr, y, sp))
-            return stage_launch(sp, x, codes, scale_e4m3, nullptr, global_scale, y, N, K,
-                                static_cast<cudaStream_t>(stream), (flags & Q4_FLAG_PDL) != 0);
-    }
     GemvParams p = {};
     p.x = static_cast<const uint16_t *>(x);
     p.w = codes;

@@ -130,7 +130,7 @@ __device__ __forceinline__ void rows_dot(const uint4 qv, uint32_t swr, uint32_t 
                 A[m] = fma2_f16(A[m], pb, xr[m][2 * jj + 1]);
             }
         }
-        const float sc = f16lo_to_f32(swr);
+        const float sc = f16lo_unpack_f32(swr);
 #pragma unroll
         for (int m = 0; m < MT; ++m)
             out[m] = fmaf(-1152.f, cd[m].y, A[m]) * cd[m].x * sc;
@@ -158,8 +158,8 @@ __device__ __forceinline__ void rows_dot(const uint4 qv, uint32_t swr, uint32_t 
                 A[m] = dp2a_hi_su(xr[m][4 * jj + 3], co, A[m]);
             }
         }
-        const float sc = f16lo_to_f32(swr);
-        const float mn = f16lo_to_f32(swm);
+        const float sc = f16lo_unpack_f32(swr);
+        const float mn = f16lo_unpack_f32(swm);
 #pragma unroll
         for (int m = 0; m < MT; ++m) {
             const float C = (float)A[m];
@@ -193,14 +193,14 @@ __device__ __forceinline__ void rows_dot(const uint4 qv, uint32_t swr, uint32_t 
                 }
             }
         }
-        const uint32_t s2 = e4m3x2_to_f16x2(swr);
-        const float sa = f16lo_to_f32(s2);
-        const float sb = f16hi_to_f32(s2);
+        float sa, sb;
+        f16x2_to_f32x2(e4m3x2lo_to_f16x2(swr), sa, sb);
 #pragma unroll
         for (int m = 0; m < MT; ++m) {
-            const float ta = f16lo_to_f32(Ha[m]) + f16hi_to_f32(Ha[m]);
-            const float tb = f16lo_to_f32(Hb[m]) + f16hi_to_f32(Hb[m]);
-            out[m] = fmaf(ta, sa, tb * sb) * cd[m].x;
+            float a0, a1, b0, b1;
+            f16x2_to_f32x2(Ha[m], a0, a1);
+            f16x2_to_f32x2(Hb[m], b0, b1);
+            out[m] = fmaf(a0 + a1, sa, (b0 + b1) * sb) * cd[m].x;
         }
     }
 }
@@ -387,7 +387,12 @@ q4_rows_kernel(GemvParams p)
     if constexpr (WK == W_NVFP4_A16)
         gsc = __ldg(p.gscale);
     pdl_launch_dependents();
-    pdl_wait();                                   // x comes from the previous kernel
+    // x comes from the previous kernel.  One warp waits for it; the others wait
+    // at the barrier, which issues nothing (all warps polling the dependency
+    // would take issue slots from the running call's CTA beside this one).
+    if (threadIdx.x < 32)
+        pdl_wait();
+    __syncthreads();
     stage_x<WK, MT, WK == W_INT4>(p, Kpad, xs, cf, (int)threadIdx.x, RK_THREADS);
     __syncthreads();
 

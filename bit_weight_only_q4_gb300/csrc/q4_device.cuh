@@ -203,6 +203,43 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_bytes)
     return r;
 }
 
+// The two fp16 halves of h2 as fp32: the pair is unpacked in place (no mask or
+// shift) and each half converted once.
+__device__ __forceinline__ void f16x2_to_f32x2(uint32_t h2, float &lo, float &hi)
+{
+    asm("{\n\t.reg .f16 l, h;\n\t"
+        "mov.b32 {l, h}, %2;\n\t"
+        "cvt.f32.f16 %0, l;\n\t"
+        "cvt.f32.f16 %1, h;\n\t}"
+        : "=f"(lo), "=f"(hi)
+        : "r"(h2));
+}
+
+// The low fp16 half of w as fp32 (unpacked in place).
+__device__ __forceinline__ float f16lo_unpack_f32(uint32_t w)
+{
+    float f;
+    asm("{\n\t.reg .f16 l, h;\n\t"
+        "mov.b32 {l, h}, %1;\n\t"
+        "cvt.f32.f16 %0, l;\n\t}"
+        : "=f"(f)
+        : "r"(w));
+    return f;
+}
+
+// Two float8_e4m3fn bytes in the low 16 bits of w -> f16x2 (exact), the 16-bit
+// operand taken by an in-place unpack.
+__device__ __forceinline__ uint32_t e4m3x2lo_to_f16x2(uint32_t w)
+{
+    uint32_t r;
+    asm("{\n\t.reg .b16 lo, hi;\n\t"
+        "mov.b32 {lo, hi}, %1;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, lo;\n\t}"
+        : "=r"(r)
+        : "r"(w));
+    return r;
+}
+
 __device__ __forceinline__ float f16lo_to_f32(uint32_t h2)
 {
     return __half2float(__ushort_as_half((unsigned short)(h2 & 0xffffu)));

@@ -82,20 +82,6 @@ bool rows_eligible(int kind, int K);
 q4_status rows_plan(const DeviceInfo &dev, int kind, int M, int N, int K, RowsPlan &plan);
 q4_status rows_launch(const RowsPlan &plan, GemvParams p, int M, cudaStream_t stream, bool pdl);
 
-// ---- one-token GEMV with bulk-copy weight stages (gemv_stage.cu)
-struct StagePlan {
-    int kind = 0, grid = 0, ns = 0, rows_max = 0;
-    size_t smem = 0;
-};
-// Whether the staged kernel serves this call (M == 1, K a multiple of 2048 with
-// K / 2048 in {1, 2, 4, 8}, 16-byte aligned pointers, fits half an SM), and how.
-bool stage_plan(const DeviceInfo &dev, int kind, int M, int N, int K, const void *x,
-                const void *codes, const void *scale, const void *minv, const void *y,
-                StagePlan &plan);
-q4_status stage_launch(const StagePlan &plan, const void *x, const uint8_t *codes,
-                       const void *scale, const void *minv, const float *gscale, void *y, int N,
-                       int K, cudaStream_t stream, bool pdl);
-
 // ---- tcgen05 tensor-core GEMM (tc_gemm.cu)
 bool tc_eligible(int kind, int M, int N, int K);
 size_t tc_workspace_bytes(int M, int N, int K, int sms);

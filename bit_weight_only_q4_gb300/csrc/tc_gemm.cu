@@ -667,64 +667,72 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
 }
 
 // x (bf16) -> prescaled fp16 once per call for large M, so that the GEMM's CTAs
-// do not each convert the same token tiles: one warp per token reads the row
-// twice (its maximum, then the conversion; the second read hits L2) and writes
-// 2^-e_m to xdn[m] for the GEMM's epilogue.
-__global__ void __launch_bounds__(256) q4_x_to_f16_kernel(const uint16_t *__restrict__ x,
-                                                          uint16_t *__restrict__ out,
-                                                          float *__restrict__ xdn, int M, int K)
+// do not each convert the same token tiles: one 256-thread block per token holds
+// the row in registers (up to XP_V 16-byte vectors per thread, K <= 16384; longer
+// rows are read a second time), reduces its maximum through shared memory, then
+// converts and writes the row and 2^-e_m to xdn[m] for the GEMM's epilogue.
+constexpr int XP_THREADS = 256;
+constexpr int XP_V = 8;
+
+__global__ void __launch_bounds__(XP_THREADS) q4_x_to_f16_kernel(const uint16_t *__restrict__ x,
+                                                                 uint16_t *__restrict__ out,
+                                                                 float *__restrict__ xdn, int M, int K)
 {
+    __shared__ uint32_t s_max[XP_THREADS / 32];
     pdl_launch_dependents();
     pdl_wait();
-    const int lane = threadIdx.x & 31;
+    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
     const int nvec = K / 8;
-    for (int m = blockIdx.x * 8 + (threadIdx.x >> 5); m < M; m += gridDim.x * 8) {
+    for (int m = blockIdx.x; m < M; m += gridDim.x) {
         const uint4 *row = reinterpret_cast<const uint4 *>(x + (int64_t)m * K);
+        uint4 v[XP_V];
         uint32_t mb = 0u;
-        int i = lane;
-        for (; i + 224 < nvec; i += 256) {          // eight loads in flight
-            uint4 v[8];
 #pragma unroll
-            for (int u = 0; u < 8; ++u)
-                v[u] = __ldcg(row + i + 32 * u);
-#pragma unroll
-            for (int u = 0; u < 8; ++u)
-                mb = bf16x8_absmax_bits(v[u], mb);
+        for (int u = 0; u < XP_V; ++u) {
+            const int i = t + u * XP_THREADS;
+            v[u] = i < nvec ? __ldcg(row + i) : make_uint4(0u, 0u, 0u, 0u);
         }
-        for (; i < nvec; i += 32)
+#pragma unroll
+        for (int u = 0; u < XP_V; ++u)
+            mb = bf16x8_absmax_bits(v[u], mb);
+        for (int i = t + XP_V * XP_THREADS; i < nvec; i += XP_THREADS)
             mb = bf16x8_absmax_bits(__ldcg(row + i), mb);
 #pragma unroll
         for (int o = 16; o >= 1; o >>= 1) {
-            const uint32_t t = __shfl_xor_sync(0xffffffffu, mb, o);
-            mb = t > mb ? t : mb;
+            const uint32_t u2 = __shfl_xor_sync(0xffffffffu, mb, o);
+            mb = u2 > mb ? u2 : mb;
         }
+        if (lane == 0)
+            s_max[warp] = mb;
+        __syncthreads();
+        mb = 0u;
+#pragma unroll
+        for (int w = 0; w < XP_THREADS / 32; ++w)
+            mb = s_max[w] > mb ? s_max[w] : mb;
+        __syncthreads();                        // s_max is rewritten for the next row
         const int e = x_prescale_exponent(mb);
         const float up = pow2f_tc(e);
-        uint4 *dst = reinterpret_cast<uint4 *>(out + (int64_t)m * K);
-        auto conv = [up](uint4 t) {
-            const uint32_t w[4] = {t.x, t.y, t.z, t.w};
+        auto conv = [up](uint4 q) {
+            const uint32_t w4[4] = {q.x, q.y, q.z, q.w};
             uint32_t o[4];
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                __half2 h = __floats2half2_rn(bf16_bits_to_f32(w[j] & 0xffffu) * up,
-                                              bf16_bits_to_f32(w[j] >> 16) * up);
+                __half2 h = __floats2half2_rn(bf16_bits_to_f32(w4[j] & 0xffffu) * up,
+                                              bf16_bits_to_f32(w4[j] >> 16) * up);
                 o[j] = *reinterpret_cast<uint32_t *>(&h);
             }
             return make_uint4(o[0], o[1], o[2], o[3]);
         };
-        i = lane;
-        for (; i + 224 < nvec; i += 256) {
-            uint4 v[8];
+        uint4 *dst = reinterpret_cast<uint4 *>(out + (int64_t)m * K);
 #pragma unroll
-            for (int u = 0; u < 8; ++u)
-                v[u] = __ldcg(row + i + 32 * u);
-#pragma unroll
-            for (int u = 0; u < 8; ++u)
-                dst[i + 32 * u] = conv(v[u]);
+        for (int u = 0; u < XP_V; ++u) {
+            const int i = t + u * XP_THREADS;
+            if (i < nvec)
+                dst[i] = conv(v[u]);
         }
-        for (; i < nvec; i += 32)
+        for (int i = t + XP_V * XP_THREADS; i < nvec; i += XP_THREADS)
             dst[i] = conv(__ldcg(row + i));
-        if (lane == 0)
+        if (t == 0)
             xdn[m] = pow2f_tc(-e);
     }
 }
@@ -905,12 +913,12 @@ q4_status tc_launch(int kind, const void *x, const uint8_t *codes, const void *s
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     if (xf16 > 0) {
-        int64_t blocks = ((int64_t)M + 7) / 8;                // one warp per token
+        int64_t blocks = M;                                   // one block per token
         if (blocks > (int64_t)dev.sms * 8)
             blocks = (int64_t)dev.sms * 8;
         cudaLaunchConfig_t pc = {};
         pc.gridDim = dim3((unsigned)blocks);
-        pc.blockDim = dim3(256);
+        pc.blockDim = dim3(XP_THREADS);
         pc.stream = stream;
         pc.attrs = pdl ? attr : nullptr;
         pc.numAttrs = pdl ? 1 : 0;
@@ -935,8 +943,9 @@ q4_status tc_launch(int kind, const void *x, const uint8_t *codes, const void *s
     const size_t x_stride = ((size_t)p.TN * 128 + 1023) / 1024 * 1024;
     const size_t budget = dev.smem_optin - 1024 /* alignment */ - 3072 /* static */ - 512;
     const int sc = p.TN <= 64 ? 2 : 1;
-    const int na = sc == 2 ? 2 : 3;
     const size_t aslot = (size_t)sc * 16384, lslot = (size_t)sc * (x_stride + 4096);
+    // four A slots when that still leaves four load slots (prefill), else two
+    const int na = (sc == 1 && budget >= 4 * aslot + 4 * lslot) ? 4 : (sc == 1 ? 3 : 2);
     const int sup_total = (p.chunks + sc - 1) / sc;
     const int sup_cta = (sup_total + p.KS - 1) / p.KS;
     int nl = budget > na * aslot ? (int)((budget - na * aslot) / lslot) : 0;

@@ -156,6 +156,31 @@ def _ws_args(ws):
     return ws.data_ptr(), ws.numel() * ws.element_size()
 
 
+# Workspaces the binding supplies when the caller passes none: one per (device,
+# stream, layout and shape), zero-filled once.  Calls of one shape on one stream
+# run in order (with programmatic dependent launch a kernel touches the
+# workspace only after the previous kernel has finished) and leave its counters
+# at zero, so they can share it; a different shape lays counters and partial
+# sums out differently and gets its own.  Reuse also keeps allocations, and
+# their fill kernels, out of captured CUDA graphs once a stream has made one
+# call of each shape.
+_ws_cache: dict = {}
+
+
+def _default_workspace(layout: int, M: int, N: int, K: int, device, stream) -> torch.Tensor | None:
+    n = workspace_bytes(layout, M, N, K)
+    if n == 0:
+        return None
+    key = (torch.device(device).index, _stream(stream), layout, M, N, K)
+    ws = _ws_cache.get(key)
+    if ws is None:
+        if len(_ws_cache) >= 64:        # many distinct shapes: start over (memory is
+            _ws_cache.clear()           # returned in stream order by the allocator)
+        ws = torch.zeros(n, dtype=torch.uint8, device=device)
+        _ws_cache[key] = ws
+    return ws
+
+
 def q4_linear_int4g128(x, qweight, scale, minv, y=None, workspace=None, stream=None):
     """y[M, N] (bf16) = x[M, K] (bf16) W^T, W in the int4-g128-minmax layout."""
     _cuda(x, "x", torch.bfloat16)
@@ -167,7 +192,7 @@ def q4_linear_int4g128(x, qweight, scale, minv, y=None, workspace=None, stream=N
     if y is None:
         y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
     if workspace is None:
-        workspace = alloc_workspace(LAYOUT_INT4G128, M, N, K, x.device)
+        workspace = _default_workspace(LAYOUT_INT4G128, M, N, K, x.device, stream)
     wp, wn = _ws_args(workspace)
     _check(load().q4_linear_int4g128(_ptr(x), _ptr(qweight), _ptr(scale), _ptr(minv), _ptr(y),
                                      M, N, K, wp, wn, _stream(stream)))
@@ -201,7 +226,7 @@ def q4_linear_nvfp4(x, codes, scale_e4m3, global_scale, y=None, workspace=None, 
     if y is None:
         y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
     if workspace is None:
-        workspace = alloc_workspace(LAYOUT_NVFP4, M, N, K, x.device)
+        workspace = _default_workspace(LAYOUT_NVFP4, M, N, K, x.device, stream)
     wp, wn = _ws_args(workspace)
     _check(load().q4_linear_nvfp4(_ptr(x), _ptr(codes), _ptr(scale_e4m3), _ptr(global_scale),
                                   _ptr(y), M, N, K, wp, wn, _stream(stream)))

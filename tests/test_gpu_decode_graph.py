@@ -55,36 +55,45 @@ def _cat(mats, names):
                             np.concatenate([mats[n].minv for n in names]))
 
 
-def test_decode_step_graph_with_pdl_matches_oracle(q4, oracle_mod):
-    """Four layers of the synthetic 28-layer int4 stack (fused q|k|v, o from the
-    v slice, fused gate|up, down from the up slice; the next layer reads down's
-    output) and the 2,049-row restricted head, 17 PDL-chained calls in one graph,
-    replayed twice; every call checked against the oracle on its own input."""
+@pytest.mark.parametrize("fusion", ["all", "pairs"])
+def test_decode_step_graph_with_pdl_matches_oracle(q4, oracle_mod, fusion):
+    """Four layers of the synthetic 28-layer int4 stack and the 2,049-row
+    restricted head in one graph of PDL-chained calls, replayed twice; every
+    call checked against the oracle on its own input.  fusion "all": q|k|v|gate|up
+    as one call, o and down reading the v and up slices of its output (13
+    calls); "pairs": q|k|v and gate|up as two calls (17 calls).  The next layer
+    reads down's output."""
     L = 4
-    H = 2048
+    H, F = 2048, 8192
+    names = [("q", "k", "v", "gate", "up")] if fusion == "all" else [("q", "k", "v"), ("gate", "up")]
     layers = []
     for layer in range(L):
         mats = synth.decode_stack_layer(layer)
-        qkv, gu = _cat(mats, ("q", "k", "v")), _cat(mats, ("gate", "up"))
-        layers.append({"qkv": qkv, "o": mats["o"], "gu": gu, "down": mats["down"]})
+        d = {"o": mats["o"], "down": mats["down"]}
+        for nm in names:
+            d["|".join(nm)] = _cat(mats, nm)
+        layers.append(d)
     dev = [{k: P.int4_dev(v) for k, v in l.items()} for l in layers]
     head = synth.decode_stack_head()
     head_d = P.bf16_dev(head)
     x0 = P.bf16_dev(synth.decode_stack_input())
-    out = [{"qkv": torch.empty((1, 3 * H), dtype=torch.bfloat16, device="cuda"),
-            "o": torch.empty((1, H), dtype=torch.bfloat16, device="cuda"),
-            "gu": torch.empty((1, 4 * H * 2), dtype=torch.bfloat16, device="cuda"),
-            "down": torch.empty((1, H), dtype=torch.bfloat16, device="cuda")}
-           for _ in range(L)]
+    width = {"q|k|v|gate|up": 3 * H + 2 * F, "q|k|v": 3 * H, "gate|up": 2 * F, "o": H, "down": H}
+    out = [{k: torch.empty((1, width[k]), dtype=torch.bfloat16, device="cuda") for k in l}
+           for l in layers]
+    # where o and down find their inputs: (output name, first column)
+    v_src = ("q|k|v|gate|up", 2 * H) if fusion == "all" else ("q|k|v", 2 * H)
+    up_src = ("q|k|v|gate|up", 3 * H + F) if fusion == "all" else ("gate|up", F)
     logits = torch.empty((1, 2049), dtype=torch.bfloat16, device="cuda")
 
     def step():
         x = x0
         for d, o in zip(dev, out):
-            q4.q4_linear_int4g128(x, *d["qkv"], y=o["qkv"])
-            q4.q4_linear_int4g128(o["qkv"][:, 2 * H:], *d["o"], y=o["o"])
-            q4.q4_linear_int4g128(x, *d["gu"], y=o["gu"])
-            q4.q4_linear_int4g128(o["gu"][:, 4 * H:], *d["down"], y=o["down"])
+            for nm in names:
+                key = "|".join(nm)
+                q4.q4_linear_int4g128(x, *d[key], y=o[key])
+                if key != "gate|up":
+                    q4.q4_linear_int4g128(o[v_src[0]][:, v_src[1]:v_src[1] + H], *d["o"], y=o["o"])
+            q4.q4_linear_int4g128(o[up_src[0]][:, up_src[1]:up_src[1] + F], *d["down"], y=o["down"])
             x = o["down"]
         q4.audio_head_logits_restricted(x, head_d, 0, 2049, -1, logits=logits)
 
@@ -114,11 +123,11 @@ def test_decode_step_graph_with_pdl_matches_oracle(q4, oracle_mod):
         def chk(name, inp, w):
             yo, ao = oracle_mod.linear_int4g128(inp, w.qweight, w.scale, w.minv, with_abs=True)
             y = torch.from_numpy(o[name].view(np.int16)).view(torch.bfloat16)
-            P.check(y, yo, ao, f"graph layer {li} {name}")
-        chk("qkv", x, lay["qkv"])
-        chk("o", np.ascontiguousarray(o["qkv"][:, 2 * H:]), lay["o"])
-        chk("gu", x, lay["gu"])
-        chk("down", np.ascontiguousarray(o["gu"][:, 4 * H:]), lay["down"])
+            P.check(y, yo, ao, f"graph ({fusion}) layer {li} {name}")
+        for nm in names:
+            chk("|".join(nm), x, lay["|".join(nm)])
+        chk("o", np.ascontiguousarray(o[v_src[0]][:, v_src[1]:v_src[1] + H]), lay["o"])
+        chk("down", np.ascontiguousarray(o[up_src[0]][:, up_src[1]:up_src[1] + F]), lay["down"])
         x = o["down"]
     yo, ao = oracle_mod.head_restricted(x, head, 0, 2049, -1, with_abs=True)
     P.check(torch.from_numpy(host[L].view(np.int16)).view(torch.bfloat16), yo, ao, "graph head")

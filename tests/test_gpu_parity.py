@@ -267,30 +267,12 @@ def test_k_not_a_power_of_two_ksteps(q4, oracle_mod, M, K):
     _nvfp4_case(q4, oracle_mod, M, 1000, K, seed=5)
 
 
-# ------------------------------------------ one-token staged kernel (K % 2048 == 0)
+# ------------------------------------------------------ one-token shapes
 @pytest.mark.parametrize("N,K", [(1, 2048), (17, 4096), (151, 2048), (152, 8192), (153, 2048),
                                  (1000, 16384), (4099, 2048), (16384, 4096)])
-def test_one_token_staged_kernel_shapes(q4, oracle_mod, N, K):
-    """One token with K a multiple of 2048 runs the bulk-copy staged kernel: rows
-    fewer than, equal to and just above the SM count, rows per CTA that leave the
-    last stage partly empty, one to eight 2048-column units per row (partials of
-    a row summed by the last of its warps)."""
+def test_one_token_shapes_around_the_sm_count(q4, oracle_mod, N, K):
+    """One token: rows fewer than, equal to and just above the SM count (one CTA
+    per SM), rows per CTA that leave warps without a row, one to sixteen
+    1024-column k-steps per row (16384: the split-K kernel)."""
     _int4_case(q4, oracle_mod, 1, N, K, seed=6)
     _nvfp4_case(q4, oracle_mod, 1, N, K, seed=6)
-
-
-def test_one_token_unaligned_scales_take_the_whole_row_kernel(q4, oracle_mod):
-    """Scale arrays that are only 2-byte aligned cannot be bulk-copied: the call
-    falls back to the whole-row kernel with the same result (within tolerance)."""
-    rng = synth.rng_for(107)
-    N, K = 640, 2048
-    w = synth.int4_matrix(rng, N, K)
-    x = synth.activations(rng, 1, K)
-    q, s, m = P.int4_dev(w)
-    s2 = torch.empty(s.numel() + 1, dtype=torch.float16, device="cuda")[1:].view(s.shape)
-    m2 = torch.empty(m.numel() + 1, dtype=torch.float16, device="cuda")[1:].view(m.shape)
-    s2.copy_(s)
-    m2.copy_(m)
-    y = q4.q4_linear_int4g128(P.bf16_dev(x), q, s2, m2)
-    yo, ao = oracle_mod.linear_int4g128(x, w.qweight, w.scale, w.minv, with_abs=True)
-    P.check(y, yo, ao, "int4 one token, 2-byte aligned scales")
