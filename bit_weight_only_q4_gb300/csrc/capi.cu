@@ -243,7 +243,9 @@ size_t q4_workspace_bytes(int layout, int M, int N, int K)
     } else {
         return 0;
     }
-    const size_t b = tc_workspace_bytes(M, N, K, sms);
+    // the tensor-core path (and its copy of x) only when the call can take it
+    const bool tc = M >= kTensorCoreMinM || (g_flags.load() & Q4_FLAG_FORCE_TENSOR_CORE);
+    const size_t b = tc ? tc_workspace_bytes(M, N, K, sms) : 0;
     return a > b ? a : b;
 }
 

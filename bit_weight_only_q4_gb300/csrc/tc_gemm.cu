@@ -60,8 +60,7 @@ struct TcParams {
     int tiles_m;               // ceil(M / TN)
     int KS;                    // split-K factor
     int chunks;                // K / 64
-    int nl;                    // load slots (codes and x of a super-chunk)
-    int na;                    // A slots (dequantised weights of a super-chunk)
+    int ns;                    // ring stages (super-chunks)
     int tmem_cols;             // power of two >= max(32, TN)
     int x_f16;                 // x already converted to prescaled fp16 (large M)
     const float *xdn;          // with x_f16: 2^-e_m per token [M]
@@ -329,19 +328,14 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
     unsigned char *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     __shared__ float s_xup[256], s_xdn[256];    // per-token 2^e_m and 2^-e_m (TN <= 256)
     const int TN = p.TN;
-    const int NL = p.nl;                        // load slots (codes + x of a stage)
-    const int NA = p.na;                        // A slots (dequantised weights of a stage)
+    const int NS = p.ns;
     const uint32_t x_bytes = (uint32_t)TN * 128;
     const uint32_t x_stride = (x_bytes + 1023) & ~1023u;
-    const uint32_t lslot_bytes = (uint32_t)SC * x_stride + TcStage<SC>::CODE;
-    // [A slots: NA x SC sub-tiles][load slots: NL x (SC x sub-tiles, codes)][barriers]
-    unsigned char *abase = smem;
-    unsigned char *lbase = smem + (size_t)NA * TcStage<SC>::A;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(lbase + (size_t)NL * lslot_bytes);
-    // bars: lfull[NL], lempty[NL], afull[NA], aempty[NA], done
-    uint64_t *lfull = bars, *lempty = bars + NL, *afull = bars + 2 * NL,
-             *aempty = bars + 2 * NL + NA, *done = bars + 2 * NL + 2 * NA;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(done + 1);
+    const uint32_t stage_bytes = TcStage<SC>::A + (uint32_t)SC * x_stride + TcStage<SC>::CODE;
+    // stage u: [A sub-tiles][x sub-tiles][codes]; barriers after the stages
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + (size_t)NS * stage_bytes);
+    // bars: full[NS], afull[NS], empty[NS], done
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 3 * NS + 1);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -361,15 +355,12 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
     const int c1 = (u1 * SC) < p.chunks ? u1 * SC : p.chunks;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < NL; ++i) {
-            mbar_init(smem_u32(&lfull[i]), 1);                 // TMA arrive + bytes
-            mbar_init(smem_u32(&lempty[i]), 1);                // MMA commit
+        for (int i = 0; i < NS; ++i) {
+            mbar_init(smem_u32(&bars[i]), 1);                  // TMA arrive + bytes
+            mbar_init(smem_u32(&bars[NS + i]), TC_WORKERS / G);   // the stage's worker group
+            mbar_init(smem_u32(&bars[2 * NS + i]), 1);         // MMA commit
         }
-        for (int i = 0; i < NA; ++i) {
-            mbar_init(smem_u32(&afull[i]), TC_WORKERS / G);    // the stage's worker group
-            mbar_init(smem_u32(&aempty[i]), 1);                // MMA commit
-        }
-        mbar_init(smem_u32(done), 1);                          // final commit
+        mbar_init(smem_u32(&bars[3 * NS]), 1);                 // final commit
         mbar_init_fence();
     }
     if (warp == 1) {
@@ -384,61 +375,46 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
-        // The codes of the first NL stages are requested before the dependency
-        // wait (weights do not depend on the previous kernel), their x sub-tiles
-        // right after it; later stages as the MMAs free load slots.
         pdl_launch_dependents();
         if (lane == 0) {
-            const int pre = nsup < NL ? nsup : NL;
-            for (int u = 0; u < pre; ++u) {
-                const int kc = c0 + u * SC;
-                const int nv = (c1 - kc) < SC ? (c1 - kc) : SC;
-                unsigned char *lst = lbase + (size_t)u * lslot_bytes;
-                mbar_arrive_expect_tx(smem_u32(&lfull[u]), TcStage<SC>::CODE + (uint32_t)nv * x_bytes);
-                tma_load_2d(smem_u32(lst + SC * x_stride), &wmap, kc * (TC_KC / 2), n0,
-                            smem_u32(&lfull[u]));
-            }
-            pdl_wait();                        // x comes from the previous kernel
-            for (int u = 0; u < pre; ++u) {
-                const int kc = c0 + u * SC;
-                const int nv = (c1 - kc) < SC ? (c1 - kc) : SC;
-                unsigned char *lst = lbase + (size_t)u * lslot_bytes;
-                for (int c = 0; c < nv; ++c)
-                    tma_load_2d(smem_u32(lst + c * x_stride), &xmap, (kc + c) * TC_KC, m0,
-                                smem_u32(&lfull[u]));
-            }
-            int issued = pre;
-            for (int u = pre; u < nsup; ++u) {
-                const int ls = u % NL;
-                if (!mbar_wait(smem_u32(&lempty[ls]), ((u / NL) - 1) & 1, p.err))
+            int issued = 0;
+            for (int u = 0; u < nsup; ++u) {
+                const int s = u % NS, use = u / NS;
+                if (use > 0 && !mbar_wait(smem_u32(&bars[2 * NS + s]), (use - 1) & 1, p.err))
                     break;
                 const int kc = c0 + u * SC;
                 const int nv = (c1 - kc) < SC ? (c1 - kc) : SC;
-                unsigned char *lst = lbase + (size_t)ls * lslot_bytes;
-                const uint32_t full = smem_u32(&lfull[ls]);
+                unsigned char *st = smem + (size_t)s * stage_bytes;
+                const uint32_t full = smem_u32(&bars[s]);
                 mbar_arrive_expect_tx(full, TcStage<SC>::CODE + (uint32_t)nv * x_bytes);
-                tma_load_2d(smem_u32(lst + SC * x_stride), &wmap, kc * (TC_KC / 2), n0, full);
+                // codes of the super-chunk: 128 rows x SC * 32 bytes in one copy
+                tma_load_2d(smem_u32(st + TcStage<SC>::A + SC * x_stride), &wmap, kc * (TC_KC / 2),
+                            n0, full);
+                if (u == 0)
+                    pdl_wait();                // x comes from the previous kernel
                 for (int c = 0; c < nv; ++c)
-                    tma_load_2d(smem_u32(lst + c * x_stride), &xmap, (kc + c) * TC_KC, m0, full);
+                    tma_load_2d(smem_u32(st + TcStage<SC>::A + c * x_stride), &xmap, (kc + c) * TC_KC,
+                                m0, full);
                 issued = u + 1;
             }
             // drain: every issued copy has landed before the CTA can exit
-            for (int u = issued - NL > 0 ? issued - NL : 0; u < issued; ++u)
-                mbar_wait(smem_u32(&lfull[u % NL]), (u / NL) & 1, p.err);
+            for (int u = issued - NS > 0 ? issued - NS : 0; u < issued; ++u)
+                mbar_wait(smem_u32(&bars[u % NS]), (u / NS) & 1, p.err);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------- MMA issue
         if (lane == 0) {
             const uint32_t idesc = idesc_f16(TN);
             for (int u = 0; u < nsup; ++u) {
-                const int as = u % NA, ls = u % NL;
-                if (!mbar_wait(smem_u32(&afull[as]), (u / NA) & 1, p.err))
+                const int s = u % NS, use = u / NS;
+                if (!mbar_wait(smem_u32(&bars[NS + s]), use & 1, p.err))
                     break;
                 tc_fence_after();
                 const int kc = c0 + u * SC;
                 const int nv = (c1 - kc) < SC ? (c1 - kc) : SC;
-                const uint64_t ad = smem_desc_sw128(smem_u32(abase + (size_t)as * TcStage<SC>::A));
-                const uint64_t bd = smem_desc_sw128(smem_u32(lbase + (size_t)ls * lslot_bytes));
+                const uint32_t st = smem_u32(smem + (size_t)s * stage_bytes);
+                const uint64_t ad = smem_desc_sw128(st);
+                const uint64_t bd = smem_desc_sw128(st + TcStage<SC>::A);
                 const uint32_t alo = (uint32_t)ad, ahi = (uint32_t)(ad >> 32);
                 const uint32_t blo = (uint32_t)bd, bhi = (uint32_t)(bd >> 32);
 #pragma unroll
@@ -451,10 +427,9 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
                                   blo + (uint32_t)c * (x_stride >> 4) + 2u * kk, bhi, idesc,
                                   (u > 0 || c > 0 || kk > 0) ? 1u : 0u);
                 }
-                mma_commit(smem_u32(&aempty[as]));       // the A slot is free again
-                mma_commit(smem_u32(&lempty[ls]));       // and so is the load slot
+                mma_commit(smem_u32(&bars[2 * NS + s]));
             }
-            mma_commit(smem_u32(done));
+            mma_commit(smem_u32(&bars[3 * NS]));
         }
         // free the accumulator as soon as every worker has read it back
         __syncwarp();
@@ -558,15 +533,11 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
         asm volatile("bar.sync 2, %0;" ::"r"(TC_WORKERS * 32) : "memory");
         // one stage; false when a wait timed out
         auto stage = [&](int u, const uint32_t (&scs)[STEPS], const uint32_t (&mns)[STEPS]) -> bool {
-                const int ls = u % NL, as = u % NA;
+                const int st_i = u % NS, use = u / NS;
                 const int kc = c0 + u * SC;
                 const int nv = (c1 - kc) < SC ? (c1 - kc) : SC;
-                unsigned char *lst = lbase + (size_t)ls * lslot_bytes;   // [x sub-tiles][codes]
-                unsigned char *ast = abase + (size_t)as * TcStage<SC>::A;
-                if (!mbar_wait_warp(smem_u32(&lfull[ls]), (u / NL) & 1, p.err))
-                    return false;
-                // the A slot is free once the MMAs of stage u - NA have completed
-                if (u >= NA && !mbar_wait_warp(smem_u32(&aempty[as]), ((u / NA) - 1) & 1, p.err))
+                unsigned char *st = smem + (size_t)st_i * stage_bytes;
+                if (!mbar_wait_warp(smem_u32(&bars[st_i]), use & 1, p.err))
                     return false;
                 // x sub-tiles: bf16 -> prescaled fp16 in place (element-wise; a
                 // 16-byte vector v holds 8 columns of token v / 8, whatever the
@@ -581,7 +552,7 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
                         if (v < nv * per) {
                             const int sub = (v >= per) + (v >= 2 * per) + (v >= 3 * per);
                             const int vv = v - sub * per;
-                            uint4 *xv = reinterpret_cast<uint4 *>(lst + sub * x_stride) + vv;
+                            uint4 *xv = reinterpret_cast<uint4 *>(st + TcStage<SC>::A + sub * x_stride) + vv;
                             const float up = s_xup[vv >> 3];
                             const uint4 t = *xv;
                             const uint32_t e[4] = {t.x, t.y, t.z, t.w};
@@ -596,13 +567,13 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
                         }
                     }
                 }
-                const unsigned char *codes = lst + SC * x_stride;
+                const unsigned char *codes = st + TcStage<SC>::A + SC * x_stride;
     #pragma unroll
                 for (int k = 0; k < STEPS; ++k) {
                     const int rd = rowk[k];
                     const uint2 cw = *reinterpret_cast<const uint2 *>(codes + rd * (SC * 32) + cl * 8);
                     const uint32_t words[2] = {cw.x, cw.y};
-                    unsigned char *arow = ast + c * 16384 + rd * 128;
+                    unsigned char *arow = st + c * 16384 + rd * 128;
                     uint32_t sg = 0u;
                     if constexpr (LAYOUT == 1)
                         sg = f16x2_splat(e4m3x2_to_f16x2(scs[k] & 0xffu) & 0xffffu);
@@ -636,7 +607,7 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
                 fence_proxy_async();
                 __syncwarp();
                 if (lane == 0)
-                    mbar_arrive(smem_u32(&afull[as]));
+                    mbar_arrive(smem_u32(&bars[NS + st_i]));
                 if (warp == 2 && lane == 0)            return true;
         };
         bool alive = true;
@@ -656,7 +627,7 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
         }
 
         // ------------------------------------------------------------ epilogue
-        const bool ok = nsup > 0 && mbar_wait_warp(smem_u32(done), 0, p.err);
+        const bool ok = nsup > 0 && mbar_wait_warp(smem_u32(&bars[3 * NS]), 0, p.err);
         tc_fence_after();
         __shared__ unsigned last_flag;
         tc_epilogue<LAYOUT>(p, tmem_base, ok, w, lane, n0, m0, tile_n * p.tiles_m + tile_m, ks,
@@ -935,31 +906,27 @@ q4_status tc_launch(int kind, const void *x, const uint8_t *codes, const void *s
         p.x_f16 = 1;
         p.xdn = xdn;
     }
-    // A stage is SC chunks of 64 columns.  Its dequantised A tiles (16 KB per
-    // chunk) need only a few slots, NA; the load ring (codes 4 KB + x TN x 128 B
-    // per chunk) takes the rest of shared memory, up to all the stages of the
-    // CTA's K range, so that the copies of many stages are in flight at once
-    // (for batched decode, every stage's codes before the dependency wait).
+    // Stage = SC chunks (A sub-tiles, x sub-tiles, codes).  The largest SC that
+    // still leaves four stages in flight (three, two) amortises each hand-off
+    // over more weights without starving the copies.
     const size_t x_stride = ((size_t)p.TN * 128 + 1023) / 1024 * 1024;
-    const size_t budget = dev.smem_optin - 1024 /* alignment */ - 3072 /* static */ - 512;
-    const int sc = p.TN <= 64 ? 2 : 1;
-    const size_t aslot = (size_t)sc * 16384, lslot = (size_t)sc * (x_stride + 4096);
-    // four A slots when that still leaves four load slots (prefill), else two
-    const int na = (sc == 1 && budget >= 4 * aslot + 4 * lslot) ? 4 : (sc == 1 ? 3 : 2);
-    const int sup_total = (p.chunks + sc - 1) / sc;
-    const int sup_cta = (sup_total + p.KS - 1) / p.KS;
-    int nl = budget > na * aslot ? (int)((budget - na * aslot) / lslot) : 0;
-    if (nl > sup_cta)
-        nl = sup_cta;
-    if (nl > 16)
-        nl = 16;
-    if (nl < 2)
-        nl = 2;
-    const size_t smem = 1024 + (size_t)na * aslot + (size_t)nl * lslot + (2 * nl + 2 * na + 1) * 8 + 16;
-    if (smem > dev.smem_optin - 3072)
+    const size_t budget = dev.smem_optin - 1024 /* alignment */ - 3072 /* static */ - 256;
+    int sc = 1, ns = 0;
+    for (int need_ns = 4; need_ns >= 2 && ns == 0; --need_ns)
+        for (int cand = 4; cand >= 1; cand /= 2) {
+            const size_t stage = (size_t)cand * (16384 + x_stride + 4096);
+            const int fit = (int)(budget / stage);
+            if (fit >= need_ns) {
+                sc = cand;
+                ns = fit > 8 ? 8 : fit;
+                break;
+            }
+        }
+    if (ns < 2)
         return fail(Q4_ERR_SHAPE, "tensor-core tile does not fit in shared memory");
-    p.nl = nl;
-    p.na = na;
+    p.ns = ns;
+    const size_t stage = (size_t)sc * (16384 + x_stride + 4096);
+    const size_t smem = 1024 + (size_t)ns * stage + (3 * ns + 1) * 8 + 16;
 
     CUtensorMap xmap, wmap;
     {

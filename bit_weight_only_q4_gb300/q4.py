@@ -173,7 +173,7 @@ def _default_workspace(layout: int, M: int, N: int, K: int, device, stream) -> t
         return None
     key = (torch.device(device).index, _stream(stream), layout, M, N, K)
     ws = _ws_cache.get(key)
-    if ws is None:
+    if ws is None or ws.numel() < n:     # (a launch flag can change the size)
         if len(_ws_cache) >= 64:        # many distinct shapes: start over (memory is
             _ws_cache.clear()           # returned in stream order by the allocator)
         ws = torch.zeros(n, dtype=torch.uint8, device=device)

@@ -82,7 +82,10 @@ unsigned q4_get_launch_flags(void);
  * Bytes of device workspace that q4_linear_int4g128 (layout 0) or
  * q4_linear_nvfp4 (layout 1) needs for an [M,N,K] call on the current device:
  * split-K partial sums and arrival counters of whichever kernel the call may use
- * (also when a Q4_FLAG_FORCE_* flag selects it).
+ * under the current launch flags, and above 64 tokens the per-token prescaled
+ * fp16 copy of x and its scales that the tensor-core path reads (the
+ * tensor-core part counts from M = 5 on, or for any M while
+ * Q4_FLAG_FORCE_TENSOR_CORE is set).
  * The workspace must be zero-filled once after allocation; every call leaves
  * its counters at zero again.  Calls that run concurrently must not share a
  * workspace.  Returns 0 for invalid sizes.

@@ -58,8 +58,13 @@ def test_launch_flags_roundtrip(lib):
 
 
 def test_workspace_bytes(lib):
-    # one 128-column k-range: no kernel splits K, no workspace
+    # one 128-column k-range: no CUDA-core kernel splits K, no workspace
     assert q4.workspace_bytes(0, 1, 2048, 128) == 0
+    # above 64 tokens the tensor-core path converts x once per call to a
+    # prescaled fp16 copy (M x K x 2 bytes) with one scale per token (M x 4),
+    # each rounded up to 256 bytes; up to 64 tokens it converts x in the GEMM
+    assert q4.workspace_bytes(0, 100, 2048, 128) == 100 * 128 * 2 + 512
+    assert q4.workspace_bytes(0, 48, 2048, 128) == 0
     # split-K needs counters and partial slots (the bound covers every kernel a
     # call may pick, including the tensor-core path forced by a flag)
     a = q4.workspace_bytes(0, 1, 2048, 2048)
