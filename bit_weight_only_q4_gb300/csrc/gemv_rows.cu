@@ -40,17 +40,20 @@
 
 namespace q4 {
 
-// Ring bytes of a CTA of NW warps holding NB batches of RB rows per thread.
-__host__ __device__ constexpr size_t rows_ring_bytes(int NW, int NB, int RB)
+// Ring bytes of a CTA of NW warps holding NB batches of RB rows per thread,
+// each row W 16-byte slices.
+__host__ __device__ constexpr size_t rows_ring_bytes(int NW, int NB, int RB, int W)
 {
-    return (size_t)NB * RB * NW * 32 * 16;
+    return (size_t)NB * RB * W * NW * 32 * 16;
 }
 
-// One token (MT = 1): one 16-warp CTA per SM per call at 64 registers, so the
-// CTA of the next call fits beside it.  Several tokens: 8-warp CTAs, two per SM.
-template <int MT>
+// One token (MT = 1): one CTA per SM per call on half of the SM's registers, so
+// the CTA of the next call fits beside it -- 16 warps at 64 registers with one
+// 32-column slice per lane (W = 1), or 8 warps at 128 registers with two (W = 2).
+// Several tokens: 8-warp CTAs, two per SM.
+template <int MT, int W>
 struct RowsShape {
-    static constexpr int NW = MT == 1 ? 16 : 8;
+    static constexpr int NW = (MT == 1 && W == 1) ? 16 : 8;
     static constexpr int MIN_CTAS = 2;
 };
 
@@ -168,8 +171,8 @@ __device__ __forceinline__ void rows_dot(const uint4 qv, uint32_t swr, uint32_t 
     } else {
         // NVFP4: each 16-column group (two words) is summed in fp16 -- eight exact
         // products (E2M1 x prescaled x, at most 10 significant bits) per half, one
-        // rounding per add, magnitude below 2^16 by the prescale -- then the two
-        // halves go to fp32 and meet the group scale.  Packed fp16 FMAs take one
+        // rounding per add, magnitude below 2^16 by the prescale -- then each half
+        // meets the group scale in an fp32 accumulator.  Packed fp16 FMAs take one
         // instruction per two weights where fp32 accumulation of fp16 products
         // takes two per weight.
         uint32_t Ha[MT], Hb[MT];
@@ -193,15 +196,12 @@ __device__ __forceinline__ void rows_dot(const uint4 qv, uint32_t swr, uint32_t 
                 }
             }
         }
-        float sa, sb;
-        f16x2_to_f32x2(e4m3x2lo_to_f16x2(swr), sa, sb);
+        // the two e4m3 group scales are exact in fp16; half sums meet them in
+        // mixed-precision FMAs
+        const uint32_t s2 = e4m3x2lo_to_f16x2(swr);
 #pragma unroll
-        for (int m = 0; m < MT; ++m) {
-            float a0, a1, b0, b1;
-            f16x2_to_f32x2(Ha[m], a0, a1);
-            f16x2_to_f32x2(Hb[m], b0, b1);
-            out[m] = fmaf(a0 + a1, sa, (b0 + b1) * sb) * cd[m].x;
-        }
+        for (int m = 0; m < MT; ++m)
+            out[m] = f16_group_pair_f32(Ha[m], Hb[m], s2) * cd[m].x;
     }
 }
 
@@ -269,11 +269,15 @@ __device__ __forceinline__ uint32_t rows_min_global(const GemvParams &p, int64_t
 }
 
 // ------------------------------------------------------------ cp.async ring
-template <int WK, int MT, int RB, int S, int NB, int REG>
-__global__ void __launch_bounds__(RowsShape<MT>::NW * 32, RowsShape<MT>::MIN_CTAS)
+// A lane holds W slices of 32 columns (16 weight bytes) of each of its rows:
+// slice h of wide k-step ks is the lane's slice of 1024-column k-step W ks + h,
+// so the x image, the per-chunk data and the slice arithmetic are those of the
+// one-slice kernel, and every warp-wide request covers 512 contiguous bytes.
+template <int WK, int MT, int RB, int S, int NB, int REG, int W>
+__global__ void __launch_bounds__(RowsShape<MT, W>::NW * 32, RowsShape<MT, W>::MIN_CTAS)
 q4_rows_kernel(GemvParams p)
 {
-    constexpr int RK_WARPS = RowsShape<MT>::NW;
+    constexpr int RK_WARPS = RowsShape<MT, W>::NW;
     constexpr int RK_THREADS = RK_WARPS * 32;
     extern __shared__ __align__(16) unsigned char smem[];
     constexpr int KSTEP = Kind<WK>::KSTEP;
@@ -282,16 +286,24 @@ q4_rows_kernel(GemvParams p)
     constexpr int XV = (WK == W_BF16) ? 4 : ((WK == W_INT8) ? 8 : 16);   // x registers per token
     constexpr int G = RK_WARPS / S;
     constexpr int NSLOT = NB * RB;
-    constexpr int Kpad = S * KSTEP;
+    constexpr int Kpad = S * W * KSTEP;
+    // bytes between a lane's slices in a weight row, and in its scale row
+    constexpr int HB = 512;
+    constexpr int SB = (WK == W_INT4) ? (KSTEP / 128) * 2 : (WK == W_NVFP4_A16 ? KSTEP / 16 : 0);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int ks = warp % S;
     const int g = warp / S;
-    const int col0 = ks * KSTEP + lane * COLS;
-    const bool colok = col0 < p.K;
-    const uint32_t ring = smem_u32(smem) + threadIdx.x * 16;   // slot i at + i * 16 * threads
+    int col0[W];
+    bool colok[W];
+#pragma unroll
+    for (int h = 0; h < W; ++h) {
+        col0[h] = (W * ks + h) * KSTEP + lane * COLS;
+        colok[h] = col0[h] < p.K;
+    }
+    const uint32_t ring = smem_u32(smem) + threadIdx.x * 16;   // slice i at + i * 16 * threads
     const uint4 *ring_ld = reinterpret_cast<const uint4 *>(smem) + threadIdx.x;
-    constexpr size_t RING = rows_ring_bytes(RK_WARPS, NB, RB);
+    constexpr size_t RING = rows_ring_bytes(RK_WARPS, NB, RB, W);
     uint16_t *xs = reinterpret_cast<uint16_t *>(smem + RING);
     float *cf = reinterpret_cast<float *>(smem + RING + (size_t)MT * Kpad * 2);
     float *red = cf + (size_t)MT * (Kpad / 32) * CH;        // [row][ks][m] partials
@@ -300,8 +312,8 @@ q4_rows_kernel(GemvParams p)
     const int rows_cta = p.rows_q + (b < p.rows_r ? 1 : 0);
     const int my_rows = rows_cta > g ? (rows_cta - g + G - 1) / G : 0;   // rows g + G*j
     const int my_ring = my_rows > REG ? my_rows - REG : 0;    // rows j >= REG use the ring
-    const int64_t colbyte = (WK == W_BF16) ? (int64_t)col0 * 2
-                            : (WK == W_INT8) ? (int64_t)col0 : (int64_t)(col0 / 2);
+    const int64_t colbyte = (WK == W_BF16) ? (int64_t)col0[0] * 2
+                            : (WK == W_INT8) ? (int64_t)col0[0] : (int64_t)(col0[0] / 2);
 
     // Ring rows are requested strictly in order (jr = 0, 1, 2, ...).  The linear
     // layers map logical row n to physical row n, so their weight and scale
@@ -316,13 +328,13 @@ q4_rows_kernel(GemvParams p)
         wnext = p.w + prow * p.w_row_bytes + colbyte;
         wstep = (int64_t)G * p.w_row_bytes;
         if constexpr (WK == W_INT4) {
-            const int64_t gi = prow * (p.K >> 7) + (col0 >> 7);
+            const int64_t gi = prow * (p.K >> 7) + (col0[0] >> 7);
             snext = reinterpret_cast<const uint8_t *>(static_cast<const uint16_t *>(p.scale) + gi);
             mdiff = reinterpret_cast<const uint8_t *>(p.minv) -
                     reinterpret_cast<const uint8_t *>(p.scale);
             sstep = (int64_t)G * (p.K >> 7) * 2;
         } else if constexpr (WK == W_NVFP4_A16) {
-            snext = static_cast<const uint8_t *>(p.scale) + prow * (p.K >> 4) + (col0 >> 4);
+            snext = static_cast<const uint8_t *>(p.scale) + prow * (p.K >> 4) + (col0[0] >> 4);
             sstep = (int64_t)G * (p.K >> 4);
         } else {
             snext = reinterpret_cast<const uint8_t *>(static_cast<const uint16_t *>(p.scale) + prow);
@@ -333,49 +345,69 @@ q4_rows_kernel(GemvParams p)
     // Request ring row jr (row j = REG + jr of this warp) into ring slot `slot`
     // (one commit group per call, empty past the last row, so wait_group counts
     // stay uniform).
-    uint32_t sw[NSLOT], swm[NSLOT];
+    uint32_t sw[NSLOT][W], swm[NSLOT][W];
     auto issue = [&](int jr, int slot) {
-        uint32_t sv = 0u, mv = 0u;
+        uint32_t sv[W], mv[W];
+#pragma unroll
+        for (int h = 0; h < W; ++h) {
+            sv[h] = 0u;
+            mv[h] = 0u;
+        }
         if (jr < my_ring) {
-            const uint8_t *src = p.w;
-            if (colok) {
-                if constexpr (kStep) {
-                    src = wnext;
-                    sv = ld_nc_u16(snext);
-                    if constexpr (WK == W_INT4)
-                        mv = ld_nc_u16(snext + mdiff);
-                } else {
-                    const int64_t prow = rows_phys(p, n0 + g + G * (REG + jr));
-                    src = p.w + prow * p.w_row_bytes + colbyte;
-                    sv = rows_scale_global<WK>(p, prow, col0);
-                    mv = rows_min_global<WK>(p, prow, col0);
+#pragma unroll
+            for (int h = 0; h < W; ++h) {
+                const uint8_t *src = p.w;
+                if (colok[h]) {
+                    if constexpr (kStep) {
+                        src = wnext + h * HB;
+                        sv[h] = ld_nc_u16(snext + h * SB);
+                        if constexpr (WK == W_INT4)
+                            mv[h] = ld_nc_u16(snext + h * SB + mdiff);
+                    } else {
+                        const int64_t prow = rows_phys(p, n0 + g + G * (REG + jr));
+                        src = p.w + prow * p.w_row_bytes + colbyte + h * HB;
+                        sv[h] = rows_scale_global<WK>(p, prow, col0[h]);
+                        mv[h] = rows_min_global<WK>(p, prow, col0[h]);
+                    }
                 }
+                cp_async_16(ring + (uint32_t)(slot * W + h) * (RK_THREADS * 16), src,
+                            colok[h] ? 16u : 0u);
             }
-            cp_async_16(ring + (uint32_t)slot * (RK_THREADS * 16), src, colok ? 16u : 0u);
             if constexpr (kStep) {
                 wnext += wstep;
                 snext += sstep;
             }
         }
-        sw[slot] = sv;
-        swm[slot] = mv;
+#pragma unroll
+        for (int h = 0; h < W; ++h) {
+            sw[slot][h] = sv[h];
+            swm[slot][h] = mv[h];
+        }
         cp_async_commit();
     };
 
     // the first REG rows of the warp: 128-bit loads straight into registers
     constexpr int NREG = REG > 0 ? REG : 1;
-    uint4 q[NREG];
-    uint32_t sq[NREG], sqm[NREG];
+    uint4 q[NREG][W];
+    uint32_t sq[NREG][W], sqm[NREG][W];
 #pragma unroll
     for (int r = 0; r < NREG; ++r) {
-        q[r] = make_uint4(0u, 0u, 0u, 0u);
-        sq[r] = 0u;
-        sqm[r] = 0u;
-        if (r < REG && r < my_rows && colok) {
+#pragma unroll
+        for (int h = 0; h < W; ++h) {
+            q[r][h] = make_uint4(0u, 0u, 0u, 0u);
+            sq[r][h] = 0u;
+            sqm[r][h] = 0u;
+        }
+        if (r < REG && r < my_rows) {
             const int64_t prow = rows_phys(p, n0 + g + G * r);
-            q[r] = ld_stream_v4(p.w + prow * p.w_row_bytes + colbyte);
-            sq[r] = rows_scale_global<WK>(p, prow, col0);
-            sqm[r] = rows_min_global<WK>(p, prow, col0);
+#pragma unroll
+            for (int h = 0; h < W; ++h) {
+                if (colok[h]) {
+                    q[r][h] = ld_stream_v4(p.w + prow * p.w_row_bytes + colbyte + h * HB);
+                    sq[r][h] = rows_scale_global<WK>(p, prow, col0[h]);
+                    sqm[r][h] = rows_min_global<WK>(p, prow, col0[h]);
+                }
+            }
         }
     }
     if (REG > 0 && p.ring_defer_ns)
@@ -396,35 +428,55 @@ q4_rows_kernel(GemvParams p)
     stage_x<WK, MT, WK == W_INT4>(p, Kpad, xs, cf, (int)threadIdx.x, RK_THREADS);
     __syncthreads();
 
-    uint32_t xr[MT][XV];
-    float4 cd[MT];           // int4: (2^-p, X, -, -); NVFP4: (2^-p * g, ...)
-    rows_load_x<WK, MT, XV>(xs, cf, Kpad, ks, lane, col0, gsc, xr, cd);
+    uint32_t xr[W][MT][XV];
+    float4 cd[W][MT];        // int4: (2^-p, X, -, -); NVFP4: (2^-p * g, ...)
+#pragma unroll
+    for (int h = 0; h < W; ++h)
+        rows_load_x<WK, MT, XV>(xs, cf, Kpad, W * ks + h, lane, col0[h], gsc, xr[h], cd[h]);
+
+    // one row's partial: the slices' dot products, summed in slice order
+    auto row_dot = [&](const uint4 (&qv)[W], const uint32_t (&s0)[W], const uint32_t (&s1)[W],
+                       float *out) {
+        rows_dot<WK, MT, XV>(qv[0], s0[0], s1[0], xr[0], cd[0], out);
+#pragma unroll
+        for (int h = 1; h < W; ++h) {
+            float t[MT];
+            rows_dot<WK, MT, XV>(qv[h], s0[h], s1[h], xr[h], cd[h], t);
+#pragma unroll
+            for (int m = 0; m < MT; ++m)
+                out[m] += t[m];
+        }
+    };
 
     if constexpr (REG > 0) {
         static_assert(REG == RB, "the register batch is one row batch");
         float part[RB * MT];
 #pragma unroll
         for (int r = 0; r < RB; ++r)
-            rows_dot<WK, MT, XV>(q[r], sq[r], sqm[r], xr, cd, part + r * MT);
+            row_dot(q[r], sq[r], sqm[r], part + r * MT);
         rows_park<RB, MT, S>(part, lane, ks, g, G, my_rows, red);
     }
 
     for (int j0 = 0; j0 < my_ring; j0 += NSLOT) {
 #pragma unroll
-        for (int h = 0; h < NB; ++h) {
-            const int jb = j0 + h * RB;
+        for (int hb = 0; hb < NB; ++hb) {
+            const int jb = j0 + hb * RB;
             if (jb >= my_ring)
                 break;
             cp_async_wait<(NB - 1) * RB>();       // this batch's RB groups have landed
             float part[RB * MT];
 #pragma unroll
-            for (int r = 0; r < RB; ++r)
-                rows_dot<WK, MT, XV>(ring_ld[(h * RB + r) * RK_THREADS], sw[h * RB + r], swm[h * RB + r], xr, cd,
-                                     part + r * MT);
+            for (int r = 0; r < RB; ++r) {
+                uint4 qv[W];
+#pragma unroll
+                for (int h = 0; h < W; ++h)
+                    qv[h] = ring_ld[((hb * RB + r) * W + h) * RK_THREADS];
+                row_dot(qv, sw[hb * RB + r], swm[hb * RB + r], part + r * MT);
+            }
             // the slots' contents are in registers now: refill them NB * RB rows ahead
 #pragma unroll
             for (int r = 0; r < RB; ++r)
-                issue(jb + NSLOT + r, h * RB + r);
+                issue(jb + NSLOT + r, hb * RB + r);
             rows_park<RB, MT, S>(part, lane, ks, g + G * (REG + jb), G, my_ring - jb, red);
         }
     }
@@ -434,44 +486,56 @@ q4_rows_kernel(GemvParams p)
 }
 
 // ------------------------------------------------------------------ host side
-template <int WK, int MT, int RB, int NB>
+template <int WK, int MT, int RB, int NB, int W>
 static const void *rows_select_s(int S)
 {
     constexpr int REG = MT == 1 ? RB : 0;       // one token: first batch in registers
-    if (S == 1) return reinterpret_cast<const void *>(&q4_rows_kernel<WK, MT, RB, 1, NB, REG>);
-    if (S == 2) return reinterpret_cast<const void *>(&q4_rows_kernel<WK, MT, RB, 2, NB, REG>);
-    if (S == 4) return reinterpret_cast<const void *>(&q4_rows_kernel<WK, MT, RB, 4, NB, REG>);
-    if (S == 8) return reinterpret_cast<const void *>(&q4_rows_kernel<WK, MT, RB, 8, NB, REG>);
-    if constexpr (WK == W_INT8 && MT == 1) {    // K up to 8192 int8 columns: 16 k-steps
-        if (S == 16) return reinterpret_cast<const void *>(&q4_rows_kernel<WK, MT, RB, 16, NB, REG>);
+    if (S == 1) return reinterpret_cast<const void *>(&q4_rows_kernel<WK, MT, RB, 1, NB, REG, W>);
+    if constexpr (W == 1) {
+        if (S == 2) return reinterpret_cast<const void *>(&q4_rows_kernel<WK, MT, RB, 2, NB, REG, W>);
+        if (S == 4) return reinterpret_cast<const void *>(&q4_rows_kernel<WK, MT, RB, 4, NB, REG, W>);
+        if (S == 8) return reinterpret_cast<const void *>(&q4_rows_kernel<WK, MT, RB, 8, NB, REG, W>);
+        if constexpr (WK == W_INT8 && MT == 1) {    // K up to 8192 int8 columns: 16 k-steps
+            if (S == 16) return reinterpret_cast<const void *>(&q4_rows_kernel<WK, MT, RB, 16, NB, REG, W>);
+        }
     }
     return nullptr;
 }
 
-// (MT, RB, NB) variants: one token (1, 4, 2), two (2, 4, 2), four (4, 2, 2).
+// (MT, RB, NB, W) variants: one token (1, 4, 2, 1 or 2), two (2, 4, 2, 1), four
+// (4, 2, 2, 1).  Two slices per lane only for one token of the 4-bit kinds with
+// K <= 2048 (one wide k-step).
 template <int WK>
-static const void *rows_select_kind(int mt, int nb, int S)
+static const void *rows_select_kind(int mt, int w, int S)
 {
-    (void)nb;
-    if (mt == 1) return rows_select_s<WK, 1, 4, 2>(S);
-    if (mt == 2) return rows_select_s<WK, 2, 4, 2>(S);
-    if (mt == 4) return rows_select_s<WK, 4, 2, 2>(S);
+    if constexpr (WK == W_INT4 || WK == W_NVFP4_A16) {
+        if (mt == 1 && w == 2) return rows_select_s<WK, 1, 4, 2, 2>(S);
+    }
+    if (w != 1) return nullptr;
+    if (mt == 1) return rows_select_s<WK, 1, 4, 2, 1>(S);
+    if (mt == 2) return rows_select_s<WK, 2, 4, 2, 1>(S);
+    if (mt == 4) return rows_select_s<WK, 4, 2, 2, 1>(S);
     return nullptr;
 }
 
 static const void *rows_select(const RowsPlan &pl)
 {
-    if (pl.kind == W_INT4) return rows_select_kind<W_INT4>(pl.mt, pl.nb, pl.S);
-    if (pl.kind == W_NVFP4_A16) return rows_select_kind<W_NVFP4_A16>(pl.mt, pl.nb, pl.S);
-    if (pl.kind == W_BF16) return rows_select_kind<W_BF16>(pl.mt, pl.nb, pl.S);
-    if (pl.kind == W_INT8) return rows_select_kind<W_INT8>(pl.mt, pl.nb, pl.S);
+    if (pl.kind == W_INT4) return rows_select_kind<W_INT4>(pl.mt, pl.w, pl.S);
+    if (pl.kind == W_NVFP4_A16) return rows_select_kind<W_NVFP4_A16>(pl.mt, pl.w, pl.S);
+    if (pl.kind == W_BF16) return rows_select_kind<W_BF16>(pl.mt, pl.w, pl.S);
+    if (pl.kind == W_INT8) return rows_select_kind<W_INT8>(pl.mt, pl.w, pl.S);
     return nullptr;
 }
 
 static int rows_warps(const RowsPlan &pl)
 {
-    return pl.mt == 1 ? RowsShape<1>::NW : RowsShape<2>::NW;
+    if (pl.mt == 1)
+        return pl.w == 2 ? RowsShape<1, 2>::NW : RowsShape<1, 1>::NW;
+    return RowsShape<2, 1>::NW;
 }
+
+// Slices per lane of the one-token 4-bit kernels (1 or 2).
+constexpr int kOneTokenSlices = 2;
 
 static int rows_kstep(int kind)
 {
@@ -481,9 +545,9 @@ static int rows_kstep(int kind)
 // k-steps of a row: ceil(K / kstep) rounded up to a power of two, so that the
 // warps of a CTA split evenly into row groups (the k-steps past K read nothing
 // and add zeros).
-static int rows_ksteps(int kind, int K)
+static int rows_ksteps(int kind, int K, int w = 1)
 {
-    const int kstep = rows_kstep(kind);
+    const int kstep = rows_kstep(kind) * w;
     const int s = (K + kstep - 1) / kstep;
     int S = 1;
     while (S < s)
@@ -507,17 +571,24 @@ q4_status rows_plan(const DeviceInfo &dev, int kind, int M, int N, int K, RowsPl
 {
     plan = RowsPlan{};
     plan.kind = kind;
-    const int kstep = rows_kstep(kind);
     const int ch = (kind == W_INT4 || kind == W_INT8) ? 4 : (kind == W_BF16 ? 0 : 1);
-    plan.S = rows_ksteps(kind, K);
     // one launch per 1, 2 or 4 tokens; three tokens take the 4-token kernel once
     // (weights read once: 17.7 against 20.6 us per NVFP4 batched-decode step as
     // a 2-token plus a 1-token launch)
     plan.mt = M >= 3 ? 4 : (M >= 2 ? 2 : 1);
-    if (plan.S > 8)
+    if (rows_ksteps(kind, K) > 8)
         plan.mt = 1;                 // 16 k-steps need the 16-warp one-token CTA
+    // One token of a 4-bit kind with K <= 2048: two 32-column slices per lane,
+    // 8 warps (fewer instructions per weight byte: 2.94M against 3.66M for the
+    // NVFP4 16384 x 2048 GEMV; 4.68 against 4.75 us per chained call).  Longer
+    // rows keep 16 warps: with under seven rows per warp the call is bound by
+    // latency, not issue (int4 2048 x 8192: 4.13 against 3.92 us).
+    plan.w = (plan.mt == 1 && (kind == W_INT4 || kind == W_NVFP4_A16) &&
+              rows_ksteps(kind, K) <= 2) ? kOneTokenSlices : 1;
+    const int kstep = rows_kstep(kind) * plan.w;
+    plan.S = rows_ksteps(kind, K, plan.w);
     plan.rb = plan.mt == 4 ? 2 : 4;
-    const int nw = plan.mt == 1 ? RowsShape<1>::NW : RowsShape<2>::NW;
+    const int nw = rows_warps(plan);
     const int G = nw / plan.S;
     const size_t Kpad = (size_t)plan.S * kstep;
     // Grid: one 16-warp CTA per SM per call for one token, two 8-warp CTAs for
@@ -542,7 +613,7 @@ q4_status rows_plan(const DeviceInfo &dev, int kind, int M, int N, int K, RowsPl
     // Two row batches in flight per thread (measured: a deeper ring only delays
     // the first batches, since 16 warps' cp.async traffic per SM is throttled).
     plan.nb = 2;
-    plan.smem = rows_ring_bytes(nw, plan.nb, plan.rb) + rest;
+    plan.smem = rows_ring_bytes(nw, plan.nb, plan.rb, plan.w) + rest;
     if (plan.smem > dev.smem_optin)
         return fail(Q4_ERR_SHAPE, "K=%d too large for the whole-row kernels", K);
     const void *k = rows_select(plan);

@@ -122,6 +122,26 @@ __device__ __forceinline__ float fma2_f16(float acc, uint32_t a, uint32_t b)
     return acc;
 }
 
+// Two 16-column groups of fp16 half sums (a: the first group's even and odd
+// columns, b: the second's) against their fp16 scales s = (s_a, s_b), in fp32:
+// ((a.lo s_a + a.hi s_a) + b.lo s_b) + b.hi s_b, each product exact in fp32 and
+// one rounding per add.
+__device__ __forceinline__ float f16_group_pair_f32(uint32_t a, uint32_t b, uint32_t s)
+{
+    float acc;
+    asm("{\n\t.reg .b16 al, ah, bl, bh, sl, sh;\n\t"
+        "mov.b32 {al, ah}, %1;\n\t"
+        "mov.b32 {bl, bh}, %2;\n\t"
+        "mov.b32 {sl, sh}, %3;\n\t"
+        "fma.rn.f32.f16 %0, al, sl, 0f00000000;\n\t"
+        "fma.rn.f32.f16 %0, ah, sl, %0;\n\t"
+        "fma.rn.f32.f16 %0, bl, sh, %0;\n\t"
+        "fma.rn.f32.f16 %0, bh, sh, %0;\n\t}"
+        : "=f"(acc)
+        : "r"(a), "r"(b), "r"(s));
+    return acc;
+}
+
 // Packed fp16 add: a + b per half, one rounding each.
 __device__ __forceinline__ uint32_t hadd2_rn(uint32_t a, uint32_t b)
 {
