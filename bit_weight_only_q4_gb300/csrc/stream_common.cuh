@@ -90,123 +90,139 @@ __device__ void stage_x(const GemvParams &p, int Kpad, uint16_t *xs, float *cf, 
     const int blocks_per_row = Kpad / 8;
     const int total = MT * blocks_per_row;
     // total is a multiple of 4 and every 4 consecutive blocks form one 32-column
-    // chunk handled by 4 consecutive lanes of one warp.
-    for (int b0 = 0; b0 < total; b0 += nthreads) {
-        const int b = b0 + tid;
-        const bool active = b < total;
-        const int m = active ? b / blocks_per_row : 0;
-        const int k0 = active ? (b - m * blocks_per_row) * 8 : 0;
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (active && m < p.mcount && k0 < p.K)
-            v = *reinterpret_cast<const uint4 *>(p.x + (int64_t)(p.m0 + m) * p.K + k0);
-        if constexpr (WK == W_BF16) {
-            if (active)
-                *reinterpret_cast<uint4 *>(xs + (size_t)m * Kpad + k0) = v;
-        } else {
-            const uint32_t e[4] = {v.x, v.y, v.z, v.w};
-            float f[8];
+    // chunk handled by 4 consecutive lanes of one warp.  A thread requests up to
+    // XU blocks before converting any, so that long rows cost one round trip.
+    constexpr int XU = 2;
+    for (int b00 = 0; b00 < total; b00 += XU * nthreads) {
+        uint4 vv[XU];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                f[2 * i] = bf16_bits_to_f32(e[i] & 0xffffu);
-                f[2 * i + 1] = bf16_bits_to_f32(e[i] >> 16);
-            }
-            float amax = 0.f;
+        for (int u = 0; u < XU; ++u) {
+            const int b = b00 + u * nthreads + tid;
+            const int m = b < total ? b / blocks_per_row : 0;
+            const int k0 = b < total ? (b - m * blocks_per_row) * 8 : 0;
+            vv[u] = make_uint4(0u, 0u, 0u, 0u);
+            if (b < total && m < p.mcount && k0 < p.K)
+                vv[u] = *reinterpret_cast<const uint4 *>(p.x + (int64_t)(p.m0 + m) * p.K + k0);
+        }
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-                amax = fmaxf(amax, fabsf(f[i]));
-            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-            // exponent ex with amax = f * 2^ex, f in [0.5, 1)
-            int ex = 0;
-            if (amax > 0.f && !isinf(amax)) {
-                const int be = (int)((__float_as_uint(amax) >> 23) & 0xff);
-                if (be > 0)
-                    ex = be - 126;
-                else
-                    frexpf(amax, &ex);
-            }
-            // chunk maximum in [2^14, 2^15); NVFP4 in [2^9, 2^10) and int4 in
-            // [2^8, 2^9), so that a sum of eight products (|E2M1| <= 6,
-            // |c - 8| <= 8) stays below 2^16 when a kernel accumulates it in
-            // fp16; int16 staging in [2^14, 2^15)
-            int pw = (XI16 ? 15 : (WK == W_NVFP4_A16 ? 10 : (WK == W_INT4 ? 9 : 15))) - ex;
-            // |pw| <= 126 keeps 2^pw and 2^-pw normal fp32 numbers; the top of the
-            // bf16 range (amax < 2^128) needs pw >= 15 - 128 = -113, so no finite
-            // chunk is clamped at the top and every one lands in its target range
-            pw = pw > 126 ? 126 : (pw < -126 ? -126 : pw);
-            const float up = pow2f(pw);
-            if constexpr (XI16) {
-                // x * 2^p is exact in fp32 and below 2^15 in magnitude; rounding
-                // to the nearest integer is exact for values within 2^7 of the
-                // chunk maximum (BF16 has 8 significant bits)
-                int xi[8];
-                bool bad = false;
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    bad |= !(fabsf(f[i]) <= 3.402823466e38f);
-                    xi[i] = __float2int_rn(f[i] * up);
-                }
-                auto pack = [](int lo, int hi) {
-                    return ((uint32_t)lo & 0xffffu) | ((uint32_t)hi << 16);
-                };
+        for (int u = 0; u < XU; ++u) {
+            const int b0 = b00 + u * nthreads;
+            if (b0 >= total)          // uniform across the block
+                break;
+            const int b = b0 + tid;
+            const bool active = b < total;
+            const int m = active ? b / blocks_per_row : 0;
+            const int k0 = active ? (b - m * blocks_per_row) * 8 : 0;
+            const uint4 v = vv[u];
+            if constexpr (WK == W_BF16) {
                 if (active)
-                    reinterpret_cast<uint4 *>(xs + (size_t)m * Kpad)[xs_vec_index_kind<WK>(k0)] =
-                        make_uint4(pack(xi[0], xi[2]), pack(xi[4], xi[6]), pack(xi[1], xi[3]),
-                                   pack(xi[5], xi[7]));
-                float sx = (float)(((xi[0] + xi[1]) + (xi[2] + xi[3])) + ((xi[4] + xi[5]) + (xi[6] + xi[7])));
-                if (bad)
-                    sx = __int_as_float(0x7fc00000);
-                sx += __shfl_xor_sync(0xffffffffu, sx, 1);
-                sx += __shfl_xor_sync(0xffffffffu, sx, 2);
-                if (active && (k0 % 32) == 0)
-                    reinterpret_cast<float4 *>(cf)[(size_t)m * (Kpad / 32) + k0 / 32] =
-                        make_float4(pow2f(-pw), sx, 0.f, 0.f);
+                    *reinterpret_cast<uint4 *>(xs + (size_t)m * Kpad + k0) = v;
             } else {
-                float xq[8];
-                uint32_t h[4];
+                const uint32_t e[4] = {v.x, v.y, v.z, v.w};
+                float f[8];
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    __half2 hh;
-                    if constexpr (WK == W_INT4)   // pairs (x'[t], x'[t+4])
-                        hh = __floats2half2_rn(f[i] * up, f[i + 4] * up);
-                    else                          // natural order
-                        hh = __floats2half2_rn(f[2 * i] * up, f[2 * i + 1] * up);
-                    h[i] = *reinterpret_cast<uint32_t *>(&hh);
-                    xq[2 * i] = __low2float(hh);
-                    xq[2 * i + 1] = __high2float(hh);
+                    f[2 * i] = bf16_bits_to_f32(e[i] & 0xffffu);
+                    f[2 * i + 1] = bf16_bits_to_f32(e[i] >> 16);
                 }
-                if (active)
-                    reinterpret_cast<uint4 *>(xs + (size_t)m * Kpad)[xs_vec_index_kind<WK>(k0)] =
-                        make_uint4(h[0], h[1], h[2], h[3]);
-                if constexpr (WK == W_INT4) {
-                    // h[i] holds columns (i, i+4): even columns are i = 0, 2
-                    float s_even = (xq[0] + xq[1]) + (xq[4] + xq[5]);
-                    float s_odd = (xq[2] + xq[3]) + (xq[6] + xq[7]);
-                    s_even += __shfl_xor_sync(0xffffffffu, s_even, 1);
-                    s_even += __shfl_xor_sync(0xffffffffu, s_even, 2);
-                    s_odd += __shfl_xor_sync(0xffffffffu, s_odd, 1);
-                    s_odd += __shfl_xor_sync(0xffffffffu, s_odd, 2);
-                    if (active && (k0 % 32) == 0)
-                        reinterpret_cast<float4 *>(cf)[(size_t)m * (Kpad / 32) + k0 / 32] =
-                            make_float4(pow2f(-pw), s_even, s_odd, 0.f);
-                } else if constexpr (WK == W_INT8) {
-                    // sums of x' over the chunk's first and last 16 columns (the two
-                    // lanes of the chunk): blocks t = 0, 1 and t = 2, 3
-                    float sh = 0.f;
+                float amax = 0.f;
 #pragma unroll
-                    for (int i = 0; i < 8; ++i)
-                        sh += xq[i];
-                    sh += __shfl_xor_sync(0xffffffffu, sh, 1);
-                    const float other = __shfl_xor_sync(0xffffffffu, sh, 2);
+                for (int i = 0; i < 8; ++i)
+                    amax = fmaxf(amax, fabsf(f[i]));
+                amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+                amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+                // exponent ex with amax = f * 2^ex, f in [0.5, 1)
+                int ex = 0;
+                if (amax > 0.f && !isinf(amax)) {
+                    const int be = (int)((__float_as_uint(amax) >> 23) & 0xff);
+                    if (be > 0)
+                        ex = be - 126;
+                    else
+                        frexpf(amax, &ex);
+                }
+                // chunk maximum in [2^14, 2^15); NVFP4 in [2^9, 2^10) and int4 in
+                // [2^8, 2^9), so that a sum of eight products (|E2M1| <= 6,
+                // |c - 8| <= 8) stays below 2^16 when a kernel accumulates it in
+                // fp16; int16 staging in [2^14, 2^15)
+                int pw = (XI16 ? 15 : (WK == W_NVFP4_A16 ? 10 : (WK == W_INT4 ? 9 : 15))) - ex;
+                // |pw| <= 126 keeps 2^pw and 2^-pw normal fp32 numbers; the top of the
+                // bf16 range (amax < 2^128) needs pw >= 15 - 128 = -113, so no finite
+                // chunk is clamped at the top and every one lands in its target range
+                pw = pw > 126 ? 126 : (pw < -126 ? -126 : pw);
+                const float up = pow2f(pw);
+                if constexpr (XI16) {
+                    // x * 2^p is exact in fp32 and below 2^15 in magnitude; rounding
+                    // to the nearest integer is exact for values within 2^7 of the
+                    // chunk maximum (BF16 has 8 significant bits)
+                    int xi[8];
+                    bool bad = false;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        bad |= !(fabsf(f[i]) <= 3.402823466e38f);
+                        xi[i] = __float2int_rn(f[i] * up);
+                    }
+                    auto pack = [](int lo, int hi) {
+                        return ((uint32_t)lo & 0xffffu) | ((uint32_t)hi << 16);
+                    };
+                    if (active)
+                        reinterpret_cast<uint4 *>(xs + (size_t)m * Kpad)[xs_vec_index_kind<WK>(k0)] =
+                            make_uint4(pack(xi[0], xi[2]), pack(xi[4], xi[6]), pack(xi[1], xi[3]),
+                                       pack(xi[5], xi[7]));
+                    float sx = (float)(((xi[0] + xi[1]) + (xi[2] + xi[3])) + ((xi[4] + xi[5]) + (xi[6] + xi[7])));
+                    if (bad)
+                        sx = __int_as_float(0x7fc00000);
+                    sx += __shfl_xor_sync(0xffffffffu, sx, 1);
+                    sx += __shfl_xor_sync(0xffffffffu, sx, 2);
                     if (active && (k0 % 32) == 0)
                         reinterpret_cast<float4 *>(cf)[(size_t)m * (Kpad / 32) + k0 / 32] =
-                            make_float4(pow2f(-pw), sh, other, 0.f);
+                            make_float4(pow2f(-pw), sx, 0.f, 0.f);
                 } else {
-                    if (active && (k0 % 32) == 0)
-                        cf[(size_t)m * (Kpad / 32) + k0 / 32] = pow2f(-pw);
+                    float xq[8];
+                    uint32_t h[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        __half2 hh;
+                        if constexpr (WK == W_INT4)   // pairs (x'[t], x'[t+4])
+                            hh = __floats2half2_rn(f[i] * up, f[i + 4] * up);
+                        else                          // natural order
+                            hh = __floats2half2_rn(f[2 * i] * up, f[2 * i + 1] * up);
+                        h[i] = *reinterpret_cast<uint32_t *>(&hh);
+                        xq[2 * i] = __low2float(hh);
+                        xq[2 * i + 1] = __high2float(hh);
+                    }
+                    if (active)
+                        reinterpret_cast<uint4 *>(xs + (size_t)m * Kpad)[xs_vec_index_kind<WK>(k0)] =
+                            make_uint4(h[0], h[1], h[2], h[3]);
+                    if constexpr (WK == W_INT4) {
+                        // h[i] holds columns (i, i+4): even columns are i = 0, 2
+                        float s_even = (xq[0] + xq[1]) + (xq[4] + xq[5]);
+                        float s_odd = (xq[2] + xq[3]) + (xq[6] + xq[7]);
+                        s_even += __shfl_xor_sync(0xffffffffu, s_even, 1);
+                        s_even += __shfl_xor_sync(0xffffffffu, s_even, 2);
+                        s_odd += __shfl_xor_sync(0xffffffffu, s_odd, 1);
+                        s_odd += __shfl_xor_sync(0xffffffffu, s_odd, 2);
+                        if (active && (k0 % 32) == 0)
+                            reinterpret_cast<float4 *>(cf)[(size_t)m * (Kpad / 32) + k0 / 32] =
+                                make_float4(pow2f(-pw), s_even, s_odd, 0.f);
+                    } else if constexpr (WK == W_INT8) {
+                        // sums of x' over the chunk's first and last 16 columns (the two
+                        // lanes of the chunk): blocks t = 0, 1 and t = 2, 3
+                        float sh = 0.f;
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            sh += xq[i];
+                        sh += __shfl_xor_sync(0xffffffffu, sh, 1);
+                        const float other = __shfl_xor_sync(0xffffffffu, sh, 2);
+                        if (active && (k0 % 32) == 0)
+                            reinterpret_cast<float4 *>(cf)[(size_t)m * (Kpad / 32) + k0 / 32] =
+                                make_float4(pow2f(-pw), sh, other, 0.f);
+                    } else {
+                        if (active && (k0 % 32) == 0)
+                            cf[(size_t)m * (Kpad / 32) + k0 / 32] = pow2f(-pw);
+                    }
                 }
+                (void)CH;
             }
-            (void)CH;
         }
     }
 }
