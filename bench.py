@@ -49,7 +49,7 @@ CALLS_PER_STEP = 8192
 # valid only for the kernel sources it was taken on (see _kernel_sha).
 TRAFFIC = {
     # workload key: (bytes per launch, _kernel_sha() when captured)
-    "nvfp4_gemv": (18909696, "626568acef56ef9115b723634b4612cfd8ace1802f241bbb525766e307460d18"),
+    "nvfp4_gemv": (18919424, "34632184ce813853f5483414916b20f00ab253a92824d57c69dd201d3dcded0a"),
 }
 
 
