@@ -521,8 +521,12 @@ def run_extra(args, local):
 def run_profile(args, local):
     """Plain launches for an ncu capture: W warm-up calls, then K calls, no graphs
     and no timing (a number printed under a profiler is never a bench value).
-    GEMV workloads rotate their weight ring; prefill runs the int4 K=2048 ->
-    N=8192 GEMM at M=2048; batched runs the NVFP4 K=8192 -> N=2048 GEMM at M=48."""
+    GEMV workloads rotate their weight ring; prefill alternates the int4 and the
+    NVFP4 K=2048 -> N=8192 GEMM at M=2048 (select one with ncu's kernel filter:
+    template argument 0 is int4, 1 NVFP4); batched runs the NVFP4 K=8192 ->
+    N=2048 GEMM at M=48; decode_step runs the step's distinct calls (fused
+    q|k|v|gate|up 22528 x 2048, o 2048 x 2048, down 2048 x 8192, then the
+    restricted head) over eight layers' weights (289 MB, beyond L2) in turn."""
     import torch
     from bit_weight_only_q4_gb300 import build as libbuild
     from bit_weight_only_q4_gb300 import q4, synth
@@ -538,9 +542,39 @@ def run_profile(args, local):
     elif args.workload == "prefill":
         x, w = synth.prefill("int4", 0)
         xd, wd = P.bf16_dev(x), P.int4_dev(w)
+        _, wn = synth.prefill("nvfp4", 0)
+        wnd = P.nvfp4_dev(wn)
         ws = q4.alloc_workspace(q4.LAYOUT_INT4G128, x.shape[0], w.N, w.K, device)
-        call = lambda i: q4.q4_linear_int4g128(xd, *wd, workspace=ws)
-        desc = "prefill int4 M=2048 K=2048 N=8192"
+        call = lambda i: (q4.q4_linear_int4g128(xd, *wd, workspace=ws) if i % 2 == 0
+                          else q4.q4_linear_nvfp4(xd, *wnd, workspace=ws))
+        desc = "prefill M=2048 K=2048 N=8192, int4 and nvfp4 in turn"
+    elif args.workload == "decode_step":
+        c = synth.DECODE_STACK_28
+        H, F = c["hidden"], c["ffn"]
+        nl = 8
+        layers = []
+        for layer in range(nl):
+            m = {k: P.int4_dev(v) for k, v in synth.decode_stack_layer(layer).items()}
+            f = tuple(torch.cat([m[n][j] for n in ("q", "k", "v", "gate", "up")], 0).contiguous()
+                      for j in range(3))
+            layers.append((f, m["o"], m["down"]))
+        head = P.bf16_dev(synth.decode_stack_head())
+        x0 = P.bf16_dev(synth.decode_stack_input())
+        y_f = torch.empty((1, 3 * H + 2 * F), dtype=torch.bfloat16, device=device)
+        y_o = torch.empty((1, H), dtype=torch.bfloat16, device=device)
+        y_d = torch.empty((1, H), dtype=torch.bfloat16, device=device)
+        logits = torch.empty((1, c["head_rows"]), dtype=torch.bfloat16, device=device)
+        ws_n = max(q4.workspace_bytes(q4.LAYOUT_INT4G128, 1, N, K)
+                   for N, K in ((3 * H + 2 * F, H), (H, H), (H, F)))
+        ws = torch.zeros(ws_n, dtype=torch.uint8, device=device) if ws_n else None
+
+        def call(i):
+            f, o, d = layers[i % nl]
+            q4.q4_linear_int4g128(x0, *f, y=y_f, workspace=ws)
+            q4.q4_linear_int4g128(y_f[:, 2 * H:3 * H], *o, y=y_o, workspace=ws)
+            q4.q4_linear_int4g128(y_f[:, 3 * H + F:], *d, y=y_d, workspace=ws)
+            q4.audio_head_logits_restricted(y_d, head, 0, c["head_rows"], -1, logits=logits)
+        desc = "decode-step calls: int4 22528x2048, 2048x2048, 2048x8192, head 2049x2048"
     elif args.workload == "batched":
         x, w = synth.nvfp4_batched(1, 48)
         xd, wd = P.bf16_dev(x), P.nvfp4_dev(w)

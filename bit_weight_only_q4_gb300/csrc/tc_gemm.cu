@@ -120,6 +120,30 @@ __device__ __forceinline__ void mma_f16_2(uint32_t tmem_d, uint32_t a_lo, uint32
                  : "memory");
 }
 
+// The same MMA with the A operand in tensor memory (row i of A in lane i, its K
+// values packed two per 32-bit column, K = 16 in eight columns).
+__device__ __forceinline__ void mma_f16_tmem_a(uint32_t tmem_d, uint32_t tmem_a, uint32_t b_lo,
+                                               uint32_t b_hi, uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile("{\n\t.reg .b64 bd;\n\t.reg .pred p;\n\t"
+                 "setp.ne.u32 p, %5, 0;\n\t"
+                 "mov.b64 bd, {%2, %3};\n\t"
+                 "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], bd, %4, p;\n\t}"
+                 ::"r"(tmem_d), "r"(tmem_a), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate)
+                 : "memory");
+}
+
+// A warp writes 16 consecutive 32-bit columns of its 32 TMEM lanes.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16])
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+                 "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};"
+                 ::"r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]),
+                   "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]),
+                   "r"(v[13]), "r"(v[14]), "r"(v[15])
+                 : "memory");
+}
+
 __device__ __forceinline__ void mma_commit(uint32_t bar)
 {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
@@ -200,6 +224,34 @@ __device__ __forceinline__ uint32_t f16x2_splat(uint32_t h16)
     return (h16 & 0xffffu) | (h16 << 16);
 }
 
+// One packed code word (8 consecutive columns of a row, low nibble = even column)
+// -> 4 f16 pairs of weights in column order.  int4: w = c * s + min (s2, m2 the
+// splatted fp16 scale and min; one rounding); NVFP4: w = E2M1 * e4m3 scale (sg
+// splatted; exact in fp16, the global scale is applied in the epilogue).
+template <int LAYOUT>
+__device__ __forceinline__ void tc_dequant_word(uint32_t word, uint32_t s2, uint32_t m2,
+                                                uint32_t (&o)[4])
+{
+    if constexpr (LAYOUT == 0) {
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+            // byte b -> (1024 + c_lo, 1024 + 16 c_hi) -> (c_lo, c_hi)
+            const uint32_t t = prmt(word, 0u, (uint32_t)(b | (4 << 4) | (b << 8) | (4 << 12)));
+            uint32_t v2;
+            asm("lop3.b32 %0, %1, 0x00F0000F, 0x64006400, 0xEA;" : "=r"(v2) : "r"(t));
+            v2 = hfma2(v2, 0x2C003C00u, 0xD400E400u);   // * (1, 1/16) + (-1024, -64)
+            o[b] = hfma2(v2, s2, m2);                   // c * s + min, one rounding
+        }
+    } else {
+        (void)m2;
+        uint32_t h[4];
+        e2m1x8_to_f16x2x4(word, h);
+#pragma unroll
+        for (int b = 0; b < 4; ++b)
+            o[b] = hmul2(h[b], s2);                     // exact in fp16
+    }
+}
+
 // Epilogue of both tensor-core kernels, run by the 16 worker warps (w = 0..15)
 // once the final MMA commit has been seen (ok): read the accumulator back from
 // TMEM (warp w reads lane quadrant (w + 2) % 4, a quarter of its columns),
@@ -208,7 +260,7 @@ __device__ __forceinline__ uint32_t f16x2_splat(uint32_t h16)
 template <int LAYOUT>
 __device__ __forceinline__ void tc_epilogue(const TcParams &p, uint32_t tmem_base, bool ok, int w,
                                             int lane, int n0, int m0, int tile, int ks,
-                                            const float *xdn, unsigned *last_flag)
+                                            const float *xdn, unsigned *last_flag, bool free_tmem)
 {
     const int TN = p.TN;
     const int quad = (w + 2) & 3;            // TMEM lane quadrant of this warp
@@ -225,7 +277,7 @@ __device__ __forceinline__ void tc_epilogue(const TcParams &p, uint32_t tmem_bas
         uint32_t v[16];
         if (cb < TN)
             tmem_ld16(tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)cb, v);
-        if (it == ncb - 1) {
+        if (free_tmem && it == ncb - 1) {
             // last TMEM read done: let warp 1 free the accumulator now
             tc_fence_before();
             asm volatile("bar.arrive 3, %0;" ::"r"((TC_WORKERS + 1) * 32) : "memory");
@@ -319,11 +371,27 @@ struct TcStage {
     static constexpr uint32_t CODE = SC * 4096u;        // 128 rows x SC * 32 bytes
 };
 
-template <int LAYOUT, int SC, int G>   // LAYOUT 0 int4-g128, 1 NVFP4; G worker groups
+// ATM (x converted by the pre-pass, one chunk per stage): the dequantised A
+// sub-tile goes to tensor memory instead of shared memory.  A stage then holds
+// only the x sub-tile and the codes, so more stages fit, the A tile costs no
+// shared-memory bandwidth, and an MMA reading A from TMEM is shorter (138
+// against 171 cycles at N = 256, measured alone).  TMEM: accumulator in columns
+// 0 .. 255, the A sub-tile of ring stage s in columns 256 + 32 s .. + 31.
+// RT = 2 (prefill tiles of 256 tokens): a CTA owns two 128-row weight tiles and
+// issues both tiles' MMAs against each x sub-tile it loads, into two TMEM
+// accumulators (columns 0 .. 255 and 256 .. 511), so each token tile is read from
+// L2 half as often; the stage then holds both A sub-tiles and a 256-row code box.
+template <int LAYOUT, int SC, int G, bool ATM, int RT>   // LAYOUT 0 int4-g128, 1 NVFP4; G worker groups
 __global__ void __launch_bounds__(TC_THREADS, 1)
 q4_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap wmap,
              TcParams p)
 {
+    static_assert(!ATM || SC == 1, "A in tensor memory takes one chunk per stage");
+    static_assert(RT == 1 || (RT == 2 && SC == 1 && !ATM), "two row tiles: one chunk per stage, A in shared memory");
+    constexpr uint32_t A_BYTES = (uint32_t)RT * TcStage<SC>::A;
+    constexpr uint32_t CODE_BYTES = (uint32_t)RT * TcStage<SC>::CODE;
+    constexpr uint32_t OFF_X = ATM ? 0u : A_BYTES;          // x sub-tiles in a stage
+    constexpr uint32_t TMEM_A = 256;                         // first A column (ATM)
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     __shared__ float s_xup[256], s_xdn[256];    // per-token 2^e_m and 2^-e_m (TN <= 256)
@@ -331,7 +399,7 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
     const int NS = p.ns;
     const uint32_t x_bytes = (uint32_t)TN * 128;
     const uint32_t x_stride = (x_bytes + 1023) & ~1023u;
-    const uint32_t stage_bytes = TcStage<SC>::A + (uint32_t)SC * x_stride + TcStage<SC>::CODE;
+    const uint32_t stage_bytes = OFF_X + (uint32_t)SC * x_stride + CODE_BYTES;
     // stage u: [A sub-tiles][x sub-tiles][codes]; barriers after the stages
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + (size_t)NS * stage_bytes);
     // bars: full[NS], afull[NS], empty[NS], done
@@ -344,7 +412,7 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
     const int rem = blockIdx.x - tile_n * tiles_mk;
     const int tile_m = rem / p.KS;
     const int ks = rem - tile_m * p.KS;
-    const int n0 = tile_n * TC_ROWS;
+    const int n0 = tile_n * TC_ROWS * RT;
     const int m0 = tile_m * TN;
     // split-K on super-chunk boundaries
     const int sup_total = (p.chunks + SC - 1) / SC;
@@ -386,14 +454,14 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
                 const int nv = (c1 - kc) < SC ? (c1 - kc) : SC;
                 unsigned char *st = smem + (size_t)s * stage_bytes;
                 const uint32_t full = smem_u32(&bars[s]);
-                mbar_arrive_expect_tx(full, TcStage<SC>::CODE + (uint32_t)nv * x_bytes);
-                // codes of the super-chunk: 128 rows x SC * 32 bytes in one copy
-                tma_load_2d(smem_u32(st + TcStage<SC>::A + SC * x_stride), &wmap, kc * (TC_KC / 2),
+                mbar_arrive_expect_tx(full, CODE_BYTES + (uint32_t)nv * x_bytes);
+                // codes of the super-chunk: 128 RT rows x SC * 32 bytes in one copy
+                tma_load_2d(smem_u32(st + OFF_X + SC * x_stride), &wmap, kc * (TC_KC / 2),
                             n0, full);
                 if (u == 0)
                     pdl_wait();                // x comes from the previous kernel
                 for (int c = 0; c < nv; ++c)
-                    tma_load_2d(smem_u32(st + TcStage<SC>::A + c * x_stride), &xmap, (kc + c) * TC_KC,
+                    tma_load_2d(smem_u32(st + OFF_X + c * x_stride), &xmap, (kc + c) * TC_KC,
                                 m0, full);
                 issued = u + 1;
             }
@@ -414,18 +482,31 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
                 const int nv = (c1 - kc) < SC ? (c1 - kc) : SC;
                 const uint32_t st = smem_u32(smem + (size_t)s * stage_bytes);
                 const uint64_t ad = smem_desc_sw128(st);
-                const uint64_t bd = smem_desc_sw128(st + TcStage<SC>::A);
+                const uint64_t bd = smem_desc_sw128(st + OFF_X);
                 const uint32_t alo = (uint32_t)ad, ahi = (uint32_t)(ad >> 32);
                 const uint32_t blo = (uint32_t)bd, bhi = (uint32_t)(bd >> 32);
-#pragma unroll
-                for (int c = 0; c < SC; ++c) {
-                    if (c >= nv)
-                        break;
+                if constexpr (ATM) {
+                    (void)alo;
+                    (void)ahi;
+                    const uint32_t a = tmem_base + TMEM_A + 32u * (uint32_t)s;
 #pragma unroll
                     for (int kk = 0; kk < TC_KC / 16; ++kk)
-                        mma_f16_2(tmem_base, alo + (uint32_t)c * 1024u + 2u * kk, ahi,
-                                  blo + (uint32_t)c * (x_stride >> 4) + 2u * kk, bhi, idesc,
-                                  (u > 0 || c > 0 || kk > 0) ? 1u : 0u);
+                        mma_f16_tmem_a(tmem_base, a + 8u * kk, blo + 2u * kk, bhi, idesc,
+                                       (u > 0 || kk > 0) ? 1u : 0u);
+                } else {
+#pragma unroll
+                    for (int c = 0; c < SC; ++c) {
+                        if (c >= nv)
+                            break;
+#pragma unroll
+                        for (int kk = 0; kk < TC_KC / 16; ++kk)
+#pragma unroll
+                            for (int rt = 0; rt < RT; ++rt)     // row tile rt: A at + 16 KB rt
+                                mma_f16_2(tmem_base + 256u * (uint32_t)rt,
+                                          alo + (uint32_t)(c * RT + rt) * 1024u + 2u * kk, ahi,
+                                          blo + (uint32_t)c * (x_stride >> 4) + 2u * kk, bhi, idesc,
+                                          (u > 0 || c > 0 || kk > 0) ? 1u : 0u);
+                    }
                 }
                 mma_commit(smem_u32(&bars[2 * NS + s]));
             }
@@ -439,100 +520,188 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
                      ::"r"(tmem_base), "r"(p.tmem_cols) : "memory");
     } else {
         // ------------------------------------------------------------- workers
-        // G groups of WG = 16 / G warps take the stages in turn (group gi the
-        // stages gi, gi + G, ...), so G stages are dequantised at once.
-        // Dequant mapping inside a group: a warp reads 256 contiguous code bytes
-        // per step (no bank conflicts): L = 4 SC lanes per code row, 32 / L rows per
-        // step, STEPS = SC * G steps.  In step k a lane takes 16 weights: row
-        // (128 / WG) wg + (32 / L) k + lane / L, chunk c = (lane % L) / 4, columns
-        // 16 (lane % 4) .. + 15 of that chunk.
-        constexpr int WG = TC_WORKERS / G;
-        constexpr int L = 4 * SC;
-        constexpr int RPS = 32 / L;
-        constexpr int STEPS = SC * G;
-        constexpr int SA = 4;                    // stages of scales loaded ahead
         const int w = warp - 2;                  // 0..15
-        const int gi = w / WG;                   // worker group
-        const int wg = w % WG;                   // warp within the group
-        const int wt = wg * 32 + lane;           // thread within the group
-        const int cl = lane % L;
-        const int c = cl >> 2;
-        const int qd = cl & 3;
-        int rowk[STEPS];
-        bool rok[STEPS];
-#pragma unroll
-        for (int k = 0; k < STEPS; ++k) {
-            rowk[k] = (128 / WG) * wg + RPS * k + lane / L;
-            rok[k] = n0 + rowk[k] < p.N;
-        }
-        // Group scales (int4: fp16 scale and min, loaded apart and combined only
-        // where used; NVFP4: the e4m3 byte) run SA stages ahead in SA register
-        // sets, each refilled right after its stage: no register moves, so no
-        // wait on a load still in flight.
-        auto load_scale = [&](int u, int k, const void *base) -> uint32_t {
-            const int kc = c0 + u * SC + c;
-            if (u >= nsup || !rok[k] || kc >= c1)
-                return 0u;
-            const int64_t n = n0 + rowk[k];
-            if constexpr (LAYOUT == 0)
-                return ld_nc_u16(static_cast<const uint16_t *>(base) + n * (p.K / 128) + (kc * TC_KC) / 128);
-            else
-                return ld_nc_u8(static_cast<const uint8_t *>(base) + n * (p.K / 16) + kc * 4 + qd);
-        };
-        uint32_t scq[SA][STEPS], mnq[SA][STEPS];
-#pragma unroll
-        for (int j = 0; j < SA; ++j)
-#pragma unroll
-            for (int k = 0; k < STEPS; ++k) {
-                scq[j][k] = load_scale(gi + j * G, k, p.scale);
-                mnq[j][k] = LAYOUT == 0 ? load_scale(gi + j * G, k, p.minv) : 0u;
-            }
-        // Per-token prescale of x (see x_prescale_exponent): tiles converted here
-        // take 2^e_m from the largest |x| of token m over this CTA's K range (one
-        // warp per token reads that range from global memory while the first
-        // stage's copies are in flight); x converted by the pre-pass brings its
-        // 2^-e_m along.  The epilogue multiplies token m's sums by 2^-e_m.
-        pdl_wait();                              // x comes from the previous kernel
-        if (!p.x_f16) {
-            // eight consecutive threads per token (TN <= 64 here), four 16-byte
-            // loads in flight each (the scale registers above are live), then a
-            // max over the eight
-            const int nvec = (c1 - c0) * (TC_KC / 8);
-            const int t = (w * 32 + lane) >> 3;
-            uint32_t mb = 0u;
-            if (t < TN && m0 + t < p.M) {
-                const uint4 *row = reinterpret_cast<const uint4 *>(
-                    p.x + (int64_t)(m0 + t) * p.K + (int64_t)c0 * TC_KC);
-                int j = lane & 7;
-                for (; j + 24 < nvec; j += 32) {
-                    uint4 v[4];
-#pragma unroll
-                    for (int u = 0; u < 4; ++u)
-                        v[u] = __ldcg(row + j + 8 * u);
-#pragma unroll
-                    for (int u = 0; u < 4; ++u)
-                        mb = bf16x8_absmax_bits(v[u], mb);
+        if constexpr (ATM) {
+            // G groups of WG = 16 / G warps take the stages in turn.  A warp may
+            // write only TMEM lane quadrant warp % 4, so it owns rows 32 (warp % 4) +
+            // lane; the WG / 4 warps of a group in one quadrant split the chunk's 64
+            // columns (h = 0, 1: columns 32 h .. + 31).  A thread reads its row's 16
+            // code bytes, dequantises 32 weights and writes them as 16 packed columns
+            // of its lane.
+            static_assert(TC_WORKERS / G == 8, "two warps per quadrant and group");
+            constexpr int SA = 4;                    // stages of scales loaded ahead
+            const int gi = w / 8;
+            const int h = (w % 8) / 4;
+            const int quad = warp & 3;
+            const int row = quad * 32 + lane;
+            const int64_t n = n0 + row;
+            const bool rok = n < p.N;
+            const uint32_t t_lane = (uint32_t)(quad * 32) << 16;
+            // int4: scale | min << 16 of the row's group; NVFP4: the e4m3 scales of
+            // the thread's two 16-column groups (low byte first)
+            auto load_scale = [&](int u) -> uint32_t {
+                if (u >= nsup || !rok)
+                    return 0u;
+                const int kc = c0 + u;
+                if constexpr (LAYOUT == 0) {
+                    const int64_t g2 = n * (p.K / 128) + kc / 2;
+                    return ld_nc_u16(static_cast<const uint16_t *>(p.scale) + g2) |
+                           (ld_nc_u16(p.minv + g2) << 16);
+                } else {
+                    return ld_nc_u16(static_cast<const uint8_t *>(p.scale) + n * (p.K / 16) + kc * 4 + 2 * h);
                 }
-                for (; j < nvec; j += 8)
-                    mb = bf16x8_absmax_bits(__ldcg(row + j), mb);
-            }
+            };
+            uint32_t scq[SA];
 #pragma unroll
-            for (int o = 4; o >= 1; o >>= 1) {
-                const uint32_t u2 = __shfl_xor_sync(0xffffffffu, mb, o);
-                mb = u2 > mb ? u2 : mb;
-            }
-            if ((lane & 7) == 0 && t < TN) {
-                const int e = x_prescale_exponent(mb);
-                s_xup[t] = pow2f_tc(e);
-                s_xdn[t] = pow2f_tc(-e);
-            }
-        } else {
+            for (int j = 0; j < SA; ++j)
+                scq[j] = load_scale(gi + j * G);
+            pdl_wait();                              // x comes from the previous kernel
             for (int t = w * 32 + lane; t < TN; t += TC_WORKERS * 32)
                 s_xdn[t] = m0 + t < p.M ? p.xdn[m0 + t] : 1.f;
-        }
-        asm volatile("bar.sync 2, %0;" ::"r"(TC_WORKERS * 32) : "memory");
-        // one stage; false when a wait timed out
-        auto stage = [&](int u, const uint32_t (&scs)[STEPS], const uint32_t (&mns)[STEPS]) -> bool {
+            asm volatile("bar.sync 2, %0;" ::"r"(TC_WORKERS * 32) : "memory");
+            auto stage = [&](int u, uint32_t sc) -> bool {
+                const int st_i = u % NS, use = u / NS;
+                const unsigned char *st = smem + (size_t)st_i * stage_bytes;
+                if (!mbar_wait_warp(smem_u32(&bars[st_i]), use & 1, p.err))
+                    return false;
+                // The slot's previous A was read by MMAs whose commit the producer
+                // waited for before requesting this use's copies.
+                tc_fence_after();
+                const uint4 cw = *reinterpret_cast<const uint4 *>(st + x_stride + row * 32 + h * 16);
+                const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
+                uint32_t v[16];
+                uint32_t s2, m2 = 0u;
+                if constexpr (LAYOUT == 0) {
+                    s2 = f16x2_splat(sc & 0xffffu);
+                    m2 = f16x2_splat(sc >> 16);
+                } else {
+                    s2 = f16x2_splat(e4m3x2_to_f16x2(sc & 0xffu) & 0xffffu);
+                }
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    if constexpr (LAYOUT == 1) {
+                        if (j == 2)
+                            s2 = f16x2_splat(e4m3x2_to_f16x2((sc >> 8) & 0xffu) & 0xffffu);
+                    }
+                    uint32_t o[4];
+                    tc_dequant_word<LAYOUT>(words[j], s2, m2, o);
+#pragma unroll
+                    for (int b = 0; b < 4; ++b)
+                        v[4 * j + b] = o[b];
+                }
+                tmem_st16(tmem_base + t_lane + TMEM_A + 32u * (uint32_t)st_i + 16u * (uint32_t)h, v);
+                asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(smem_u32(&bars[NS + st_i]));
+                return true;
+            };
+            bool alive = true;
+            for (int u0 = gi; u0 < nsup && alive; u0 += SA * G) {
+#pragma unroll
+                for (int j = 0; j < SA; ++j) {
+                    const int u = u0 + j * G;
+                    if (alive && u < nsup)
+                        alive = stage(u, scq[j]);
+                    scq[j] = load_scale(u + SA * G);
+                }
+            }
+        } else {
+            // G groups of WG = 16 / G warps take the stages in turn (group gi the
+            // stages gi, gi + G, ...), so G stages are dequantised at once.
+            // Dequant mapping inside a group: a warp reads 256 contiguous code bytes
+            // per step (no bank conflicts): L = 4 SC lanes per code row, 32 / L rows per
+            // step, STEPS = SC * G * RT steps.  In step k a lane takes 16 weights: row
+            // (128 RT / WG) wg + (32 / L) k + lane / L, chunk c = (lane % L) / 4,
+            // columns 16 (lane % 4) .. + 15 of that chunk (rows 128 .. 255 are the
+            // second row tile, whose A sub-tile follows the first's).
+            constexpr int WG = TC_WORKERS / G;
+            constexpr int L = 4 * SC;
+            constexpr int RPS = 32 / L;
+            constexpr int STEPS = SC * G * RT;
+            constexpr int SA = 4;                    // stages of scales loaded ahead
+            const int gi = w / WG;                   // worker group
+            const int wg = w % WG;                   // warp within the group
+            const int wt = wg * 32 + lane;           // thread within the group
+            const int cl = lane % L;
+            const int c = cl >> 2;
+            const int qd = cl & 3;
+            int rowk[STEPS];
+            bool rok[STEPS];
+#pragma unroll
+            for (int k = 0; k < STEPS; ++k) {
+                rowk[k] = (128 * RT / WG) * wg + RPS * k + lane / L;
+                rok[k] = n0 + rowk[k] < p.N;
+            }
+            // Group scales (int4: fp16 scale and min, loaded apart and combined only
+            // where used; NVFP4: the e4m3 byte) run SA stages ahead in SA register
+            // sets, each refilled right after its stage: no register moves, so no
+            // wait on a load still in flight.
+            auto load_scale = [&](int u, int k, const void *base) -> uint32_t {
+                const int kc = c0 + u * SC + c;
+                if (u >= nsup || !rok[k] || kc >= c1)
+                    return 0u;
+                const int64_t n = n0 + rowk[k];
+                if constexpr (LAYOUT == 0)
+                    return ld_nc_u16(static_cast<const uint16_t *>(base) + n * (p.K / 128) + (kc * TC_KC) / 128);
+                else
+                    return ld_nc_u8(static_cast<const uint8_t *>(base) + n * (p.K / 16) + kc * 4 + qd);
+            };
+            uint32_t scq[SA][STEPS], mnq[SA][STEPS];
+#pragma unroll
+            for (int j = 0; j < SA; ++j)
+#pragma unroll
+                for (int k = 0; k < STEPS; ++k) {
+                    scq[j][k] = load_scale(gi + j * G, k, p.scale);
+                    mnq[j][k] = LAYOUT == 0 ? load_scale(gi + j * G, k, p.minv) : 0u;
+                }
+            // Per-token prescale of x (see x_prescale_exponent): tiles converted here
+            // take 2^e_m from the largest |x| of token m over this CTA's K range (one
+            // warp per token reads that range from global memory while the first
+            // stage's copies are in flight); x converted by the pre-pass brings its
+            // 2^-e_m along.  The epilogue multiplies token m's sums by 2^-e_m.
+            pdl_wait();                              // x comes from the previous kernel
+            if (!p.x_f16) {
+                // eight consecutive threads per token (TN <= 64 here), four 16-byte
+                // loads in flight each (the scale registers above are live), then a
+                // max over the eight
+                const int nvec = (c1 - c0) * (TC_KC / 8);
+                const int t = (w * 32 + lane) >> 3;
+                uint32_t mb = 0u;
+                if (t < TN && m0 + t < p.M) {
+                    const uint4 *row = reinterpret_cast<const uint4 *>(
+                        p.x + (int64_t)(m0 + t) * p.K + (int64_t)c0 * TC_KC);
+                    int j = lane & 7;
+                    for (; j + 24 < nvec; j += 32) {
+                        uint4 v[4];
+#pragma unroll
+                        for (int u = 0; u < 4; ++u)
+                            v[u] = __ldcg(row + j + 8 * u);
+#pragma unroll
+                        for (int u = 0; u < 4; ++u)
+                            mb = bf16x8_absmax_bits(v[u], mb);
+                    }
+                    for (; j < nvec; j += 8)
+                        mb = bf16x8_absmax_bits(__ldcg(row + j), mb);
+                }
+#pragma unroll
+                for (int o = 4; o >= 1; o >>= 1) {
+                    const uint32_t u2 = __shfl_xor_sync(0xffffffffu, mb, o);
+                    mb = u2 > mb ? u2 : mb;
+                }
+                if ((lane & 7) == 0 && t < TN) {
+                    const int e = x_prescale_exponent(mb);
+                    s_xup[t] = pow2f_tc(e);
+                    s_xdn[t] = pow2f_tc(-e);
+                }
+            } else {
+                for (int t = w * 32 + lane; t < TN; t += TC_WORKERS * 32)
+                    s_xdn[t] = m0 + t < p.M ? p.xdn[m0 + t] : 1.f;
+            }
+            asm volatile("bar.sync 2, %0;" ::"r"(TC_WORKERS * 32) : "memory");
+            // one stage; false when a wait timed out
+            auto stage = [&](int u, const uint32_t (&scs)[STEPS], const uint32_t (&mns)[STEPS]) -> bool {
                 const int st_i = u % NS, use = u / NS;
                 const int kc = c0 + u * SC;
                 const int nv = (c1 - kc) < SC ? (c1 - kc) : SC;
@@ -546,18 +715,18 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
                 // the loop is unrolled and interleaves with the code loads below.
                 if (!p.x_f16) {
                     const int per = TN * 8;                  // vectors per sub-tile
-    #pragma unroll
+#pragma unroll
                     for (int j = 0; j < SC * G; ++j) {
                         const int v = wt + j * WG * 32;
                         if (v < nv * per) {
                             const int sub = (v >= per) + (v >= 2 * per) + (v >= 3 * per);
                             const int vv = v - sub * per;
-                            uint4 *xv = reinterpret_cast<uint4 *>(st + TcStage<SC>::A + sub * x_stride) + vv;
+                            uint4 *xv = reinterpret_cast<uint4 *>(st + OFF_X + sub * x_stride) + vv;
                             const float up = s_xup[vv >> 3];
                             const uint4 t = *xv;
                             const uint32_t e[4] = {t.x, t.y, t.z, t.w};
                             uint32_t o[4];
-    #pragma unroll
+#pragma unroll
                             for (int q = 0; q < 4; ++q) {
                                 __half2 h = __floats2half2_rn(bf16_bits_to_f32(e[q] & 0xffffu) * up,
                                                               bf16_bits_to_f32(e[q] >> 16) * up);
@@ -567,8 +736,8 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
                         }
                     }
                 }
-                const unsigned char *codes = st + TcStage<SC>::A + SC * x_stride;
-    #pragma unroll
+                const unsigned char *codes = st + OFF_X + SC * x_stride;
+#pragma unroll
                 for (int k = 0; k < STEPS; ++k) {
                     const int rd = rowk[k];
                     const uint2 cw = *reinterpret_cast<const uint2 *>(codes + rd * (SC * 32) + cl * 8);
@@ -577,13 +746,13 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
                     uint32_t sg = 0u;
                     if constexpr (LAYOUT == 1)
                         sg = f16x2_splat(e4m3x2_to_f16x2(scs[k] & 0xffu) & 0xffffu);
-    #pragma unroll
+#pragma unroll
                     for (int j = 0; j < 2; ++j) {           // 8 K columns per 16-byte chunk
                         uint32_t o[4];
                         if constexpr (LAYOUT == 0) {
                             const uint32_t s2 = f16x2_splat(scs[k]);
                             const uint32_t m2 = f16x2_splat(mns[k]);
-    #pragma unroll
+#pragma unroll
                             for (int b = 0; b < 4; ++b) {
                                 // byte b -> (1024 + c_lo, 1024 + 16 c_hi) -> (c_lo, c_hi)
                                 const uint32_t t = prmt(words[j], 0u, (uint32_t)(b | (4 << 4) | (b << 8) | (4 << 12)));
@@ -595,7 +764,7 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
                         } else {
                             uint32_t h[4];
                             e2m1x8_to_f16x2x4(words[j], h);
-    #pragma unroll
+#pragma unroll
                             for (int b = 0; b < 4; ++b)
                                 o[b] = hmul2(h[b], sg);                    // exact in fp16
                         }
@@ -608,20 +777,21 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
                 __syncwarp();
                 if (lane == 0)
                     mbar_arrive(smem_u32(&bars[NS + st_i]));
-                if (warp == 2 && lane == 0)            return true;
-        };
-        bool alive = true;
-        for (int u0 = gi; u0 < nsup && alive; u0 += SA * G) {
+                return true;
+            };
+            bool alive = true;
+            for (int u0 = gi; u0 < nsup && alive; u0 += SA * G) {
 #pragma unroll
-            for (int j = 0; j < SA; ++j) {
-                const int u = u0 + j * G;
-                if (alive && u < nsup)
-                    alive = stage(u, scq[j], mnq[j]);
+                for (int j = 0; j < SA; ++j) {
+                    const int u = u0 + j * G;
+                    if (alive && u < nsup)
+                        alive = stage(u, scq[j], mnq[j]);
 #pragma unroll
-                for (int k = 0; k < STEPS; ++k) {
-                    scq[j][k] = load_scale(u + SA * G, k, p.scale);
-                    if constexpr (LAYOUT == 0)
-                        mnq[j][k] = load_scale(u + SA * G, k, p.minv);
+                    for (int k = 0; k < STEPS; ++k) {
+                        scq[j][k] = load_scale(u + SA * G, k, p.scale);
+                        if constexpr (LAYOUT == 0)
+                            mnq[j][k] = load_scale(u + SA * G, k, p.minv);
+                    }
                 }
             }
         }
@@ -630,8 +800,11 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
         const bool ok = nsup > 0 && mbar_wait_warp(smem_u32(&bars[3 * NS]), 0, p.err);
         tc_fence_after();
         __shared__ unsigned last_flag;
-        tc_epilogue<LAYOUT>(p, tmem_base, ok, w, lane, n0, m0, tile_n * p.tiles_m + tile_m, ks,
-                            s_xdn, &last_flag);
+#pragma unroll
+        for (int rt = 0; rt < RT; ++rt)
+            tc_epilogue<LAYOUT>(p, tmem_base + 256u * (uint32_t)rt, ok, w, lane, n0 + TC_ROWS * rt, m0,
+                                (tile_n * RT + rt) * p.tiles_m + tile_m, ks, s_xdn, &last_flag,
+                                rt == RT - 1);
     }
 
     __syncthreads();
@@ -738,11 +911,43 @@ bool tc_eligible(int kind, int M, int N, int K)
     return kind == W_INT4 || kind == W_NVFP4_A16;
 }
 
-static int tc_tn(int M)
+// x is converted inside the GEMM for tiles of up to 64 tokens (at most SC
+// vectors per thread), by a separate pass for more.
+static bool tc_preconvert(int M) { return M > 64; }
+
+// Tiles of pre-converted x keep their dequantised A sub-tiles in tensor memory,
+// except full 256-token tiles, whose CTAs own two weight-row tiles (two
+// accumulators fill the tensor memory).
+constexpr bool kTcTmemA = true;
+constexpr bool kTcTwoRowTiles = true;
+
+// CTA tile: TN tokens (MMA N) x RT weight-row tiles of 128.  Each x sub-tile a
+// CTA loads feeds RT tiles' MMAs, so for prefill (x converted by the pre-pass,
+// tiles of 256 tokens) the CTA takes two row tiles where that still gives over
+// half a wave of CTAs without split-K.  Measured at M = 2048: 2048 -> 8192 72
+// against 94 us with one row tile; 8192 -> 2048 (64 CTAs of two row tiles) 95 with
+// two-way split-K and 105 with 128-token tiles, against 77-79 with one row tile.
+// Otherwise one row tile and TN = M rounded up to 16 (at most 256).
+struct TcShape {
+    int TN, RT;
+};
+
+static TcShape tc_shape(int M, int N, int sms)
 {
-    if (M > 256)
-        return 256;
-    return (M + 15) / 16 * 16 < 16 ? 16 : (M + 15) / 16 * 16;
+    const int tn = M > 256 ? 256 : ((M + 15) / 16 * 16 < 16 ? 16 : (M + 15) / 16 * 16);
+    if (!kTcTwoRowTiles || !tc_preconvert(M) || M < 256)
+        return {tn, 1};
+    const int64_t pairs = (N + 2 * TC_ROWS - 1) / (2 * TC_ROWS);
+    if (pairs * ((M + 255) / 256) * 2 > sms)
+        return {256, 2};
+    return {tn, 1};
+}
+
+// Tiles of 128 weight rows x TN tokens (a CTA owns RT of them).
+static int64_t tc_tiles(int M, int N, int sms)
+{
+    const TcShape sh = tc_shape(M, N, sms);
+    return (int64_t)((N + TC_ROWS * sh.RT - 1) / (TC_ROWS * sh.RT)) * sh.RT * ((M + sh.TN - 1) / sh.TN);
 }
 
 // Split-K factor: as many CTAs as fit in one wave (one CTA per SM) when the tile
@@ -751,8 +956,7 @@ static int tc_tn(int M)
 // tail more than the extra CTAs shorten the main loop).
 static int tc_ks(const DeviceInfo &dev, int M, int N, int K)
 {
-    const int TN = tc_tn(M);
-    const int64_t tiles = (int64_t)((N + TC_ROWS - 1) / TC_ROWS) * ((M + TN - 1) / TN);
+    const int64_t tiles = tc_tiles(M, N, dev.sms) / tc_shape(M, N, dev.sms).RT;   // CTAs per K slice
     const int chunks = K / TC_KC;
     if (tiles * 2 > dev.sms)
         return 1;
@@ -763,10 +967,6 @@ static int tc_ks(const DeviceInfo &dev, int M, int N, int K)
         ks = 8;
     return ks < 1 ? 1 : ks;
 }
-
-// x is converted inside the GEMM for tiles of up to 64 tokens (at most SC
-// vectors per thread), by a separate pass for more.
-static bool tc_preconvert(int M) { return M > 64; }
 
 // [fp16 x, prescaled per token][per-token 2^-e_m, fp32]
 static size_t tc_xf16_data_bytes(int M, int K) { return ((size_t)M * K * 2 + 255) / 256 * 256; }
@@ -783,8 +983,8 @@ static size_t tc_split_bytes(int M, int N, int K, int sms)
     const int ks = tc_ks(d, M, N, K);
     if (ks == 1)
         return 0;
-    const int TN = tc_tn(M);
-    const size_t tiles = (size_t)((N + TC_ROWS - 1) / TC_ROWS) * ((M + TN - 1) / TN);
+    const int TN = tc_shape(M, N, sms).TN;
+    const size_t tiles = (size_t)tc_tiles(M, N, sms);
     return (tiles * 4 + 255) / 256 * 256 + tiles * ks * TN * TC_ROWS * 4;
 }
 
@@ -799,7 +999,8 @@ size_t tc_workspace_bytes(int M, int N, int K, int sms)
 
 static CUresult tc_encode_maps(EncodeTiledFn enc, CUtensorMap &xmap, CUtensorMap &wmap,
                                const void *xsrc, bool x_f16, const uint8_t *codes, int M, int N,
-                               int K, int TN, int code_box_bytes, bool code_swizzle)
+                               int K, int TN, int code_box_bytes, int code_box_rows,
+                               bool code_swizzle)
 {
     cuuint64_t xd[2] = {(cuuint64_t)K, (cuuint64_t)M};
     cuuint64_t xstr[1] = {(cuuint64_t)K * 2};
@@ -813,7 +1014,7 @@ static CUresult tc_encode_maps(EncodeTiledFn enc, CUtensorMap &xmap, CUtensorMap
         return r;
     cuuint64_t wd[2] = {(cuuint64_t)K / 2, (cuuint64_t)N};
     cuuint64_t wstr[1] = {(cuuint64_t)K / 2};
-    cuuint32_t wbox[2] = {(cuuint32_t)code_box_bytes, TC_ROWS};
+    cuuint32_t wbox[2] = {(cuuint32_t)code_box_bytes, (cuuint32_t)code_box_rows};
     return enc(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(codes), wd, wstr, wbox,
                estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                code_swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
@@ -821,20 +1022,20 @@ static CUresult tc_encode_maps(EncodeTiledFn enc, CUtensorMap &xmap, CUtensorMap
 }
 
 template <int LAYOUT>
-static const void *tc_select_layout(int sc, int groups)
+static const void *tc_select_layout(int sc, bool atm, int rt)
 {
-    if (groups == 2)
-        return sc == 4 ? reinterpret_cast<const void *>(&q4_tc_kernel<LAYOUT, 4, 2>)
-             : sc == 2 ? reinterpret_cast<const void *>(&q4_tc_kernel<LAYOUT, 2, 2>)
-                       : reinterpret_cast<const void *>(&q4_tc_kernel<LAYOUT, 1, 2>);
-    return sc == 4 ? reinterpret_cast<const void *>(&q4_tc_kernel<LAYOUT, 4, 1>)
-         : sc == 2 ? reinterpret_cast<const void *>(&q4_tc_kernel<LAYOUT, 2, 1>)
-                   : reinterpret_cast<const void *>(&q4_tc_kernel<LAYOUT, 1, 1>);
+    if (rt == 2)
+        return reinterpret_cast<const void *>(&q4_tc_kernel<LAYOUT, 1, 2, false, 2>);
+    if (atm)
+        return reinterpret_cast<const void *>(&q4_tc_kernel<LAYOUT, 1, 2, true, 1>);
+    return sc == 4 ? reinterpret_cast<const void *>(&q4_tc_kernel<LAYOUT, 4, 2, false, 1>)
+         : sc == 2 ? reinterpret_cast<const void *>(&q4_tc_kernel<LAYOUT, 2, 2, false, 1>)
+                   : reinterpret_cast<const void *>(&q4_tc_kernel<LAYOUT, 1, 2, false, 1>);
 }
 
-static const void *tc_select(int kind, int sc, int groups)
+static const void *tc_select(int kind, int sc, bool atm, int rt)
 {
-    return kind == W_INT4 ? tc_select_layout<0>(sc, groups) : tc_select_layout<1>(sc, groups);
+    return kind == W_INT4 ? tc_select_layout<0>(sc, atm, rt) : tc_select_layout<1>(sc, atm, rt);
 }
 
 q4_status tc_launch(int kind, const void *x, const uint8_t *codes, const void *scale,
@@ -859,7 +1060,8 @@ q4_status tc_launch(int kind, const void *x, const uint8_t *codes, const void *s
     p.M = M;
     p.N = N;
     p.K = K;
-    p.TN = tc_tn(M);
+    const TcShape shape = tc_shape(M, N, dev.sms);
+    p.TN = shape.TN;
     p.tiles_m = (M + p.TN - 1) / p.TN;
     p.KS = tc_ks(dev, M, N, K);
     p.chunks = K / TC_KC;
@@ -870,7 +1072,8 @@ q4_status tc_launch(int kind, const void *x, const uint8_t *codes, const void *s
     const size_t need = tc_workspace_bytes(M, N, K, dev.sms);
     if (need > ws_bytes)
         return fail(Q4_ERR_WORKSPACE, "tensor-core path needs %zu bytes of workspace", need);
-    const size_t tiles = (size_t)((N + TC_ROWS - 1) / TC_ROWS) * p.tiles_m;
+    const int rt = shape.RT;
+    const size_t tiles = (size_t)tc_tiles(M, N, dev.sms);     // 128-row tiles
     unsigned char *wsb = static_cast<unsigned char *>(ws);
     const size_t xf16 = tc_xf16_bytes(M, K);
     if (p.KS > 1) {
@@ -908,13 +1111,18 @@ q4_status tc_launch(int kind, const void *x, const uint8_t *codes, const void *s
     }
     // Stage = SC chunks (A sub-tiles, x sub-tiles, codes).  The largest SC that
     // still leaves four stages in flight (three, two) amortises each hand-off
-    // over more weights without starving the copies.
+    // over more weights without starving the copies.  With x converted by the
+    // pre-pass the A sub-tiles live in tensor memory instead (one chunk per
+    // stage; up to eight stages, whose A sub-tiles take TMEM columns 256 ..).
     const size_t x_stride = ((size_t)p.TN * 128 + 1023) / 1024 * 1024;
     const size_t budget = dev.smem_optin - 1024 /* alignment */ - 3072 /* static */ - 256;
+    const bool atm = p.x_f16 != 0 && kTcTmemA && rt == 1;
+    const size_t a_bytes = atm ? 0 : 16384 * (size_t)rt;
+    const size_t code_bytes = 4096 * (size_t)rt;
     int sc = 1, ns = 0;
     for (int need_ns = 4; need_ns >= 2 && ns == 0; --need_ns)
-        for (int cand = 4; cand >= 1; cand /= 2) {
-            const size_t stage = (size_t)cand * (16384 + x_stride + 4096);
+        for (int cand = (atm || rt == 2) ? 1 : 4; cand >= 1; cand /= 2) {
+            const size_t stage = (size_t)cand * (a_bytes + x_stride + code_bytes);
             const int fit = (int)(budget / stage);
             if (fit >= need_ns) {
                 sc = cand;
@@ -925,25 +1133,26 @@ q4_status tc_launch(int kind, const void *x, const uint8_t *codes, const void *s
     if (ns < 2)
         return fail(Q4_ERR_SHAPE, "tensor-core tile does not fit in shared memory");
     p.ns = ns;
-    const size_t stage = (size_t)sc * (16384 + x_stride + 4096);
+    if (atm || rt == 2)
+        p.tmem_cols = 512;
+    const size_t stage = (size_t)sc * (a_bytes + x_stride + code_bytes);
     const size_t smem = 1024 + (size_t)ns * stage + (3 * ns + 1) * 8 + 16;
 
     CUtensorMap xmap, wmap;
     {
         const CUresult r = tc_encode_maps(enc, xmap, wmap, xsrc, p.x_f16 != 0, codes, M, N, K, p.TN,
-                                          sc * TC_KC / 2, false);
+                                          sc * TC_KC / 2, TC_ROWS * rt, false);
         if (r != CUDA_SUCCESS)
             return fail(Q4_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
     }
     // two worker groups, two stages dequantised at once (measured: prefill
     // GEMMs 5-22% faster than one group of 16 warps; batched decode unchanged)
-    const int groups = 2;
-    const void *k = tc_select(kind, sc, groups);
+    const void *k = tc_select(kind, sc, atm, rt);
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess)
         return cuda_fail(e, "cudaFuncSetAttribute(tensor-core kernel)");
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(tiles * p.KS));
+    cfg.gridDim = dim3((unsigned)(tiles / rt * p.KS));
     cfg.blockDim = dim3(TC_THREADS);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;

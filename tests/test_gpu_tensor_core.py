@@ -53,10 +53,14 @@ def _mat(layout, rng, N, K):
 @pytest.mark.parametrize("M,N,K", [(16, 128, 128), (1, 128, 128), (5, 200, 256), (48, 1000, 640),
                                    (64, 384, 1024), (200, 130, 2048), (300, 256, 384),
                                    (17, 8192, 128), (48, 96, 8192), (8, 512, 2048),
-                                   (33, 2049, 8192), (64, 2048, 8192), (16, 16384, 2048)])
+                                   (33, 2049, 8192), (64, 2048, 8192), (16, 16384, 2048),
+                                   (300, 10000, 256), (2048, 2432, 128)])
 def test_forced_tensor_core_shapes(q4, oracle_mod, layout, M, N, K):
     """The tensor-core kernel on every shape (x converted in the kernel up to 64
-    tokens, by the pre-pass above)."""
+    tokens, by the pre-pass above; A sub-tiles in tensor memory from 65 to 255
+    tokens; CTAs of two 128-row tiles for 256-token tiles, here with a ragged last
+    token tile and a last row pair that ends inside its first tile or at its
+    second)."""
     if layout == "int4" and K % 128:
         pytest.skip("int4 needs K % 128")
     rng = synth.rng_for(300, M, N, K)
