@@ -62,6 +62,7 @@ struct TcParams {
     int chunks;                // K / 64
     int ns;                    // ring stages (super-chunks)
     int tmem_cols;             // power of two >= max(32, TN)
+    int tmem_a0;               // A in tensor memory: first column of the A sub-tiles
     int x_f16;                 // x already converted to prescaled fp16 (large M)
     const float *xdn;          // with x_f16: 2^-e_m per token [M]
 };
@@ -373,10 +374,12 @@ struct TcStage {
 
 // ATM (x converted by the pre-pass, one chunk per stage): the dequantised A
 // sub-tile goes to tensor memory instead of shared memory.  A stage then holds
-// only the x sub-tile and the codes, so more stages fit, the A tile costs no
-// shared-memory bandwidth, and an MMA reading A from TMEM is shorter (138
-// against 171 cycles at N = 256, measured alone).  TMEM: accumulator in columns
-// 0 .. 255, the A sub-tile of ring stage s in columns 256 + 32 s .. + 31.
+// only the x sub-tile and the codes, so more stages fit (more copies in flight),
+// the A tile costs no shared-memory bandwidth, and an MMA reading A from TMEM is
+// shorter at N = 256 (138 against 171 cycles, measured alone).  TMEM:
+// accumulator in columns 0 .. TN - 1, the A sub-tile of ring stage s in columns
+// a0 + 32 s .. + 31 (a0 = p.tmem_a0, TN rounded up to 32).
+//
 // RT = 2 (prefill tiles of 256 tokens): a CTA owns two 128-row weight tiles and
 // issues both tiles' MMAs against each x sub-tile it loads, into two TMEM
 // accumulators (columns 0 .. 255 and 256 .. 511), so each token tile is read from
@@ -391,7 +394,6 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
     constexpr uint32_t A_BYTES = (uint32_t)RT * TcStage<SC>::A;
     constexpr uint32_t CODE_BYTES = (uint32_t)RT * TcStage<SC>::CODE;
     constexpr uint32_t OFF_X = ATM ? 0u : A_BYTES;          // x sub-tiles in a stage
-    constexpr uint32_t TMEM_A = 256;                         // first A column (ATM)
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     __shared__ float s_xup[256], s_xdn[256];    // per-token 2^e_m and 2^-e_m (TN <= 256)
@@ -488,7 +490,7 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
                 if constexpr (ATM) {
                     (void)alo;
                     (void)ahi;
-                    const uint32_t a = tmem_base + TMEM_A + 32u * (uint32_t)s;
+                    const uint32_t a = tmem_base + (uint32_t)p.tmem_a0 + 32u * (uint32_t)s;
 #pragma unroll
                     for (int kk = 0; kk < TC_KC / 16; ++kk)
                         mma_f16_tmem_a(tmem_base, a + 8u * kk, blo + 2u * kk, bhi, idesc,
@@ -521,6 +523,52 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
     } else {
         // ------------------------------------------------------------- workers
         const int w = warp - 2;                  // 0..15
+        // Per-token prescale of x (see x_prescale_exponent): tiles converted here
+        // take 2^e_m from the largest |x| of token m over this CTA's K range (one
+        // warp per token reads that range from global memory while the first
+        // stage's copies are in flight); x converted by the pre-pass brings its
+        // 2^-e_m along.  The epilogue multiplies token m's sums by 2^-e_m.
+        auto prescale = [&]() {
+            pdl_wait();                              // x comes from the previous kernel
+            if (!p.x_f16) {
+                // eight consecutive threads per token (TN <= 64 here), four 16-byte
+                // loads in flight each (the scale registers above are live), then a
+                // max over the eight
+                const int nvec = (c1 - c0) * (TC_KC / 8);
+                const int t = (w * 32 + lane) >> 3;
+                uint32_t mb = 0u;
+                if (t < TN && m0 + t < p.M) {
+                    const uint4 *row = reinterpret_cast<const uint4 *>(
+                        p.x + (int64_t)(m0 + t) * p.K + (int64_t)c0 * TC_KC);
+                    int j = lane & 7;
+                    for (; j + 24 < nvec; j += 32) {
+                        uint4 v[4];
+#pragma unroll
+                        for (int u = 0; u < 4; ++u)
+                            v[u] = __ldcg(row + j + 8 * u);
+#pragma unroll
+                        for (int u = 0; u < 4; ++u)
+                            mb = bf16x8_absmax_bits(v[u], mb);
+                    }
+                    for (; j < nvec; j += 8)
+                        mb = bf16x8_absmax_bits(__ldcg(row + j), mb);
+                }
+#pragma unroll
+                for (int o = 4; o >= 1; o >>= 1) {
+                    const uint32_t u2 = __shfl_xor_sync(0xffffffffu, mb, o);
+                    mb = u2 > mb ? u2 : mb;
+                }
+                if ((lane & 7) == 0 && t < TN) {
+                    const int e = x_prescale_exponent(mb);
+                    s_xup[t] = pow2f_tc(e);
+                    s_xdn[t] = pow2f_tc(-e);
+                }
+            } else {
+                for (int t = w * 32 + lane; t < TN; t += TC_WORKERS * 32)
+                    s_xdn[t] = m0 + t < p.M ? p.xdn[m0 + t] : 1.f;
+            }
+            asm volatile("bar.sync 2, %0;" ::"r"(TC_WORKERS * 32) : "memory");
+        };
         if constexpr (ATM) {
             // G groups of WG = 16 / G warps take the stages in turn.  A warp may
             // write only TMEM lane quadrant warp % 4, so it owns rows 32 (warp % 4) +
@@ -555,10 +603,7 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
 #pragma unroll
             for (int j = 0; j < SA; ++j)
                 scq[j] = load_scale(gi + j * G);
-            pdl_wait();                              // x comes from the previous kernel
-            for (int t = w * 32 + lane; t < TN; t += TC_WORKERS * 32)
-                s_xdn[t] = m0 + t < p.M ? p.xdn[m0 + t] : 1.f;
-            asm volatile("bar.sync 2, %0;" ::"r"(TC_WORKERS * 32) : "memory");
+            prescale();
             auto stage = [&](int u, uint32_t sc) -> bool {
                 const int st_i = u % NS, use = u / NS;
                 const unsigned char *st = smem + (size_t)st_i * stage_bytes;
@@ -589,7 +634,8 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
                     for (int b = 0; b < 4; ++b)
                         v[4 * j + b] = o[b];
                 }
-                tmem_st16(tmem_base + t_lane + TMEM_A + 32u * (uint32_t)st_i + 16u * (uint32_t)h, v);
+                tmem_st16(tmem_base + t_lane + (uint32_t)p.tmem_a0 + 32u * (uint32_t)st_i + 16u * (uint32_t)h,
+                          v);
                 asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
                 tc_fence_before();
                 __syncwarp();
@@ -656,50 +702,7 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
                     scq[j][k] = load_scale(gi + j * G, k, p.scale);
                     mnq[j][k] = LAYOUT == 0 ? load_scale(gi + j * G, k, p.minv) : 0u;
                 }
-            // Per-token prescale of x (see x_prescale_exponent): tiles converted here
-            // take 2^e_m from the largest |x| of token m over this CTA's K range (one
-            // warp per token reads that range from global memory while the first
-            // stage's copies are in flight); x converted by the pre-pass brings its
-            // 2^-e_m along.  The epilogue multiplies token m's sums by 2^-e_m.
-            pdl_wait();                              // x comes from the previous kernel
-            if (!p.x_f16) {
-                // eight consecutive threads per token (TN <= 64 here), four 16-byte
-                // loads in flight each (the scale registers above are live), then a
-                // max over the eight
-                const int nvec = (c1 - c0) * (TC_KC / 8);
-                const int t = (w * 32 + lane) >> 3;
-                uint32_t mb = 0u;
-                if (t < TN && m0 + t < p.M) {
-                    const uint4 *row = reinterpret_cast<const uint4 *>(
-                        p.x + (int64_t)(m0 + t) * p.K + (int64_t)c0 * TC_KC);
-                    int j = lane & 7;
-                    for (; j + 24 < nvec; j += 32) {
-                        uint4 v[4];
-#pragma unroll
-                        for (int u = 0; u < 4; ++u)
-                            v[u] = __ldcg(row + j + 8 * u);
-#pragma unroll
-                        for (int u = 0; u < 4; ++u)
-                            mb = bf16x8_absmax_bits(v[u], mb);
-                    }
-                    for (; j < nvec; j += 8)
-                        mb = bf16x8_absmax_bits(__ldcg(row + j), mb);
-                }
-#pragma unroll
-                for (int o = 4; o >= 1; o >>= 1) {
-                    const uint32_t u2 = __shfl_xor_sync(0xffffffffu, mb, o);
-                    mb = u2 > mb ? u2 : mb;
-                }
-                if ((lane & 7) == 0 && t < TN) {
-                    const int e = x_prescale_exponent(mb);
-                    s_xup[t] = pow2f_tc(e);
-                    s_xdn[t] = pow2f_tc(-e);
-                }
-            } else {
-                for (int t = w * 32 + lane; t < TN; t += TC_WORKERS * 32)
-                    s_xdn[t] = m0 + t < p.M ? p.xdn[m0 + t] : 1.f;
-            }
-            asm volatile("bar.sync 2, %0;" ::"r"(TC_WORKERS * 32) : "memory");
+            prescale();
             // one stage; false when a wait timed out
             auto stage = [&](int u, const uint32_t (&scs)[STEPS], const uint32_t (&mns)[STEPS]) -> bool {
                 const int st_i = u % NS, use = u / NS;
@@ -1116,7 +1119,13 @@ q4_status tc_launch(int kind, const void *x, const uint8_t *codes, const void *s
     // stage; up to eight stages, whose A sub-tiles take TMEM columns 256 ..).
     const size_t x_stride = ((size_t)p.TN * 128 + 1023) / 1024 * 1024;
     const size_t budget = dev.smem_optin - 1024 /* alignment */ - 3072 /* static */ - 256;
-    const bool atm = p.x_f16 != 0 && kTcTmemA && rt == 1;
+    // (measured for batched decode, x converted in the kernel: M = 48 step 31.4
+    // against 27.9 us with A in shared memory, so only pre-converted tiles)
+    const bool atm = kTcTmemA && rt == 1 && p.x_f16 != 0;
+    // A in tensor memory: the A sub-tiles after the accumulator, one 32-column
+    // slot per stage
+    p.tmem_a0 = (p.TN + 31) / 32 * 32;
+    const int ns_cap = atm ? (512 - p.tmem_a0) / 32 : 8;
     const size_t a_bytes = atm ? 0 : 16384 * (size_t)rt;
     const size_t code_bytes = 4096 * (size_t)rt;
     int sc = 1, ns = 0;
@@ -1126,7 +1135,7 @@ q4_status tc_launch(int kind, const void *x, const uint8_t *codes, const void *s
             const int fit = (int)(budget / stage);
             if (fit >= need_ns) {
                 sc = cand;
-                ns = fit > 8 ? 8 : fit;
+                ns = fit > ns_cap ? ns_cap : fit;
                 break;
             }
         }
