@@ -253,12 +253,62 @@ __device__ __forceinline__ void tc_dequant_word(uint32_t word, uint32_t s2, uint
     }
 }
 
+// Split-K sum of one tile by its last-arriving CTA: y[m0 + c][n0 + 4q .. + 3] is
+// the sum over k of the KS partials (k < KS <= KSM), added in k order, so the
+// result does not depend on timing.  Work unit g4 = 32 c + q (four rows of one
+// token column); a thread takes 16 / KSM units per round and requests all their
+// partials (16-byte loads) before any add, so one round trip covers them.
+template <int KSM>
+__device__ __forceinline__ void tc_splitk_sum(const TcParams &p, const float4 *part, int n0, int m0,
+                                              int t0, int nthreads)
+{
+    constexpr int GU = 16 / KSM;
+    const int TN = p.TN, KS = p.KS;
+    const int total = TN * (TC_ROWS / 4);
+    const size_t kstride4 = (size_t)TN * TC_ROWS / 4;
+    for (int base = t0; base < total; base += GU * nthreads) {
+        float4 v[GU][KSM];
+#pragma unroll
+        for (int g = 0; g < GU; ++g) {
+            const int g4 = base + g * nthreads;
+#pragma unroll
+            for (int k = 0; k < KSM; ++k)
+                v[g][k] = (g4 < total && k < KS) ? __ldcg(part + k * kstride4 + g4)
+                                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int g = 0; g < GU; ++g) {
+            const int g4 = base + g * nthreads;
+            if (g4 >= total)
+                continue;
+            float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int k = 0; k < KSM; ++k)
+                if (k < KS) {
+                    sum.x += v[g][k].x; sum.y += v[g][k].y;
+                    sum.z += v[g][k].z; sum.w += v[g][k].w;
+                }
+            const int c = g4 / (TC_ROWS / 4), q = g4 % (TC_ROWS / 4);
+            const int m = m0 + c;
+            const int nb = n0 + 4 * q;
+            if (m < p.M) {
+                uint16_t *yr = p.y + (int64_t)m * p.N;
+                const float o[4] = {sum.x, sum.y, sum.z, sum.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    if (nb + i < p.N)
+                        yr[nb + i] = f32_to_bf16_bits(o[i]);
+            }
+        }
+    }
+}
+
 // Epilogue of both tensor-core kernels, run by the 16 worker warps (w = 0..15)
 // once the final MMA commit has been seen (ok): read the accumulator back from
 // TMEM (warp w reads lane quadrant (w + 2) % 4, a quarter of its columns),
 // release warp 1 to free TMEM after the last read, then store bf16 y -- or, under
 // split-K, fp32 partials that the last CTA of the tile to arrive sums in k order.
-template <int LAYOUT>
+template <int LAYOUT, bool SPLITK>
 __device__ __forceinline__ void tc_epilogue(const TcParams &p, uint32_t tmem_base, bool ok, int w,
                                             int lane, int n0, int m0, int tile, int ks,
                                             const float *xdn, unsigned *last_flag, bool free_tmem)
@@ -288,7 +338,7 @@ __device__ __forceinline__ void tc_epilogue(const TcParams &p, uint32_t tmem_bas
         // token m's sums times the global scale, then 2^-e_m (exact), undoing the
         // prescale of its x.  In this order an intermediate overflows only where
         // the result itself does (2^-e_m reaches 2^113 for the largest tokens).
-        if (p.KS == 1) {
+        if (!SPLITK || p.KS == 1) {
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
                 const int m = m0 + cb + j;
@@ -303,7 +353,7 @@ __device__ __forceinline__ void tc_epilogue(const TcParams &p, uint32_t tmem_bas
                 dst[(size_t)j * TC_ROWS] = (__uint_as_float(v[j]) * gsc) * xdn[cb + j];
         }
     }
-    if (p.KS > 1) {
+    if (SPLITK && p.KS > 1) {
         // split-K: the last CTA of this tile to arrive sums the partials (every
         // worker reaches both barriers, whatever happened before).  Every CTA
         // takes its ticket, also one whose wait timed out, so the counter always
@@ -321,39 +371,14 @@ __device__ __forceinline__ void tc_epilogue(const TcParams &p, uint32_t tmem_bas
         asm volatile("bar.sync 2, %0;" ::"r"(TC_WORKERS * 32) : "memory");
         if (*last_flag == 1u) {
             __threadfence();
-            // Each thread sums groups of four rows of one token column: all KS
-            // partials of a group are loaded (16 bytes each) before the adds,
-            // which run in k order, so the result does not depend on timing.
-            const size_t kstride4 = (size_t)TN * TC_ROWS / 4;
             const float4 *part = reinterpret_cast<const float4 *>(
                 p.ws + (size_t)tile * p.KS * TN * TC_ROWS);
-            for (int g4 = w * 32 + lane; g4 < TN * (TC_ROWS / 4); g4 += TC_WORKERS * 32) {
-                const int c = g4 / (TC_ROWS / 4), q = g4 % (TC_ROWS / 4);
-                float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
-                for (int k0 = 0; k0 < p.KS; k0 += 8) {
-                    float4 v[8];
-#pragma unroll
-                    for (int j = 0; j < 8; ++j)
-                        if (k0 + j < p.KS)
-                            v[j] = __ldcg(part + (k0 + j) * kstride4 + (size_t)c * (TC_ROWS / 4) + q);
-#pragma unroll
-                    for (int j = 0; j < 8; ++j)
-                        if (k0 + j < p.KS) {
-                            sum.x += v[j].x; sum.y += v[j].y;
-                            sum.z += v[j].z; sum.w += v[j].w;
-                        }
-                }
-                const int m = m0 + c;
-                const int nb = n0 + 4 * q;
-                if (m < p.M) {
-                    uint16_t *yr = p.y + (int64_t)m * p.N;
-                    const float o[4] = {sum.x, sum.y, sum.z, sum.w};
-#pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        if (nb + i < p.N)
-                            yr[nb + i] = f32_to_bf16_bits(o[i]);
-                }
-            }
+            if (p.KS <= 2)
+                tc_splitk_sum<2>(p, part, n0, m0, w * 32 + lane, TC_WORKERS * 32);
+            else if (p.KS <= 4)
+                tc_splitk_sum<4>(p, part, n0, m0, w * 32 + lane, TC_WORKERS * 32);
+            else
+                tc_splitk_sum<8>(p, part, n0, m0, w * 32 + lane, TC_WORKERS * 32);
         }
         if (*last_flag != 0u && w == 0 && lane == 0)
             p.tickets[tile] = 0u;
@@ -805,7 +830,7 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
         __shared__ unsigned last_flag;
 #pragma unroll
         for (int rt = 0; rt < RT; ++rt)
-            tc_epilogue<LAYOUT>(p, tmem_base + 256u * (uint32_t)rt, ok, w, lane, n0 + TC_ROWS * rt, m0,
+            tc_epilogue<LAYOUT, RT == 1>(p, tmem_base + 256u * (uint32_t)rt, ok, w, lane, n0 + TC_ROWS * rt, m0,
                                 (tile_n * RT + rt) * p.tiles_m + tile_m, ks, s_xdn, &last_flag,
                                 rt == RT - 1);
     }
@@ -1076,6 +1101,8 @@ q4_status tc_launch(int kind, const void *x, const uint8_t *codes, const void *s
     if (need > ws_bytes)
         return fail(Q4_ERR_WORKSPACE, "tensor-core path needs %zu bytes of workspace", need);
     const int rt = shape.RT;
+    if (rt == 2 && p.KS != 1)          // two-tile CTAs are only planned without split-K
+        return fail(Q4_ERR_SHAPE, "tensor-core plan: split-K with two row tiles");
     const size_t tiles = (size_t)tc_tiles(M, N, dev.sms);     // 128-row tiles
     unsigned char *wsb = static_cast<unsigned char *>(ws);
     const size_t xf16 = tc_xf16_bytes(M, K);
