@@ -205,17 +205,29 @@ __device__ __forceinline__ void rows_dot(const uint4 qv, uint32_t swr, uint32_t 
     }
 }
 
-// Sum RB x MT partials across the warp and park each row's total for k-step ks.
-template <int RB, int MT, int S>
-__device__ __forceinline__ void rows_park(float (&part)[RB * MT], int lane, int ks, int row0,
-                                          int G, int nvalid, float *red)
+// Sum RB x MT partials across the warp and park each row's total for k-step ks;
+// with DS (one k-step) the total is the row's result and goes to y as bf16.
+template <int RB, int MT, int S, bool DS>
+__device__ __forceinline__ void rows_park(const GemvParams &p, int n0, float (&part)[RB * MT],
+                                          int lane, int ks, int row0, int G, int nvalid,
+                                          float *red)
 {
     int idx = 0;
     const float tot = warp_sum_transpose<RB * MT>(part, lane, idx);
     const int r = idx / MT, m = idx - (idx / MT) * MT;
     if ((lane & (32 / (RB * MT) - 1)) == 0 && r < nvalid) {
         const int row = row0 + G * r;
-        red[((size_t)row * S + ks) * MT + m] = tot;
+        if constexpr (DS) {
+            static_assert(S == 1, "direct stores need one k-step");
+            (void)ks;
+            (void)red;
+            if (m < p.mcount)
+                p.y[(int64_t)(p.m0 + m) * p.ldy + n0 + row] = f32_to_bf16_bits(tot);
+        } else {
+            (void)p;
+            (void)n0;
+            red[((size_t)row * S + ks) * MT + m] = tot;
+        }
     }
 }
 
@@ -273,7 +285,7 @@ __device__ __forceinline__ uint32_t rows_min_global(const GemvParams &p, int64_t
 // slice h of wide k-step ks is the lane's slice of 1024-column k-step W ks + h,
 // so the x image, the per-chunk data and the slice arithmetic are those of the
 // one-slice kernel, and every warp-wide request covers 512 contiguous bytes.
-template <int WK, int MT, int RB, int S, int NB, int REG, int W>
+template <int WK, int MT, int RB, int S, int NB, int REG, int W, bool DS>
 __global__ void __launch_bounds__(RowsShape<MT, W>::NW * 32, RowsShape<MT, W>::MIN_CTAS)
 q4_rows_kernel(GemvParams p)
 {
@@ -454,7 +466,7 @@ q4_rows_kernel(GemvParams p)
 #pragma unroll
         for (int r = 0; r < RB; ++r)
             row_dot(q[r], sq[r], sqm[r], part + r * MT);
-        rows_park<RB, MT, S>(part, lane, ks, g, G, my_rows, red);
+        rows_park<RB, MT, S, DS>(p, n0, part, lane, ks, g, G, my_rows, red);
     }
 
     for (int j0 = 0; j0 < my_ring; j0 += NSLOT) {
@@ -477,26 +489,32 @@ q4_rows_kernel(GemvParams p)
 #pragma unroll
             for (int r = 0; r < RB; ++r)
                 issue(jb + NSLOT + r, hb * RB + r);
-            rows_park<RB, MT, S>(part, lane, ks, g + G * (REG + jb), G, my_ring - jb, red);
+            rows_park<RB, MT, S, DS>(p, n0, part, lane, ks, g + G * (REG + jb), G, my_ring - jb,
+                                     red);
         }
     }
     cp_async_wait<0>();                           // nothing left in flight at exit
-    __syncthreads();
-    rows_store<MT, S>(p, red, n0, rows_cta, RK_THREADS);
+    if constexpr (!DS) {
+        __syncthreads();
+        rows_store<MT, S>(p, red, n0, rows_cta, RK_THREADS);
+    }
 }
 
 // ------------------------------------------------------------------ host side
 template <int WK, int MT, int RB, int NB, int W>
-static const void *rows_select_s(int S)
+static const void *rows_select_s(int S, bool direct)
 {
     constexpr int REG = MT == 1 ? RB : 0;       // one token: first batch in registers
-    if (S == 1) return reinterpret_cast<const void *>(&q4_rows_kernel<WK, MT, RB, 1, NB, REG, W>);
+    if constexpr (W == 2) {
+        if (S == 1 && direct) return reinterpret_cast<const void *>(&q4_rows_kernel<WK, MT, RB, 1, NB, REG, W, true>);
+    }
+    if (S == 1) return reinterpret_cast<const void *>(&q4_rows_kernel<WK, MT, RB, 1, NB, REG, W, false>);
     if constexpr (W == 1) {
-        if (S == 2) return reinterpret_cast<const void *>(&q4_rows_kernel<WK, MT, RB, 2, NB, REG, W>);
-        if (S == 4) return reinterpret_cast<const void *>(&q4_rows_kernel<WK, MT, RB, 4, NB, REG, W>);
-        if (S == 8) return reinterpret_cast<const void *>(&q4_rows_kernel<WK, MT, RB, 8, NB, REG, W>);
+        if (S == 2) return reinterpret_cast<const void *>(&q4_rows_kernel<WK, MT, RB, 2, NB, REG, W, false>);
+        if (S == 4) return reinterpret_cast<const void *>(&q4_rows_kernel<WK, MT, RB, 4, NB, REG, W, false>);
+        if (S == 8) return reinterpret_cast<const void *>(&q4_rows_kernel<WK, MT, RB, 8, NB, REG, W, false>);
         if constexpr (WK == W_INT8 && MT == 1) {    // K up to 8192 int8 columns: 16 k-steps
-            if (S == 16) return reinterpret_cast<const void *>(&q4_rows_kernel<WK, MT, RB, 16, NB, REG, W>);
+            if (S == 16) return reinterpret_cast<const void *>(&q4_rows_kernel<WK, MT, RB, 16, NB, REG, W, false>);
         }
     }
     return nullptr;
@@ -506,24 +524,24 @@ static const void *rows_select_s(int S)
 // (4, 2, 2, 1).  Two slices per lane only for one token of the 4-bit kinds with
 // K <= 2048 (one wide k-step).
 template <int WK>
-static const void *rows_select_kind(int mt, int w, int S)
+static const void *rows_select_kind(int mt, int w, int S, bool direct)
 {
     if constexpr (WK == W_INT4 || WK == W_NVFP4_A16) {
-        if (mt == 1 && w == 2) return rows_select_s<WK, 1, 4, 2, 2>(S);
+        if (mt == 1 && w == 2) return rows_select_s<WK, 1, 4, 2, 2>(S, direct);
     }
     if (w != 1) return nullptr;
-    if (mt == 1) return rows_select_s<WK, 1, 4, 2, 1>(S);
-    if (mt == 2) return rows_select_s<WK, 2, 4, 2, 1>(S);
-    if (mt == 4) return rows_select_s<WK, 4, 2, 2, 1>(S);
+    if (mt == 1) return rows_select_s<WK, 1, 4, 2, 1>(S, false);
+    if (mt == 2) return rows_select_s<WK, 2, 4, 2, 1>(S, false);
+    if (mt == 4) return rows_select_s<WK, 4, 2, 2, 1>(S, false);
     return nullptr;
 }
 
 static const void *rows_select(const RowsPlan &pl)
 {
-    if (pl.kind == W_INT4) return rows_select_kind<W_INT4>(pl.mt, pl.w, pl.S);
-    if (pl.kind == W_NVFP4_A16) return rows_select_kind<W_NVFP4_A16>(pl.mt, pl.w, pl.S);
-    if (pl.kind == W_BF16) return rows_select_kind<W_BF16>(pl.mt, pl.w, pl.S);
-    if (pl.kind == W_INT8) return rows_select_kind<W_INT8>(pl.mt, pl.w, pl.S);
+    if (pl.kind == W_INT4) return rows_select_kind<W_INT4>(pl.mt, pl.w, pl.S, pl.direct);
+    if (pl.kind == W_NVFP4_A16) return rows_select_kind<W_NVFP4_A16>(pl.mt, pl.w, pl.S, pl.direct);
+    if (pl.kind == W_BF16) return rows_select_kind<W_BF16>(pl.mt, pl.w, pl.S, pl.direct);
+    if (pl.kind == W_INT8) return rows_select_kind<W_INT8>(pl.mt, pl.w, pl.S, pl.direct);
     return nullptr;
 }
 
@@ -613,6 +631,16 @@ q4_status rows_plan(const DeviceInfo &dev, int kind, int M, int N, int K, RowsPl
     // Two row batches in flight per thread (measured: a deeper ring only delays
     // the first batches, since 16 warps' cp.async traffic per SM is throttled).
     plan.nb = 2;
+    // Two-slice kernels whose warps own no more rows than they request before
+    // the dependency wait (4 register rows + an 8-row ring) store each row from
+    // the cross-lane reduction; longer row lists keep the final store pass,
+    // since their stores would meet their own later ring refills (NVFP4 16384 x
+    // 2048: 4.48 against 4.43 us per chained call with direct stores).
+    if (plan.w == 2 && plan.S == 1) {
+        const int64_t rows_cta = ((int64_t)N + grid - 1) / grid;
+        const int64_t per_warp = (rows_cta + (nw / plan.S) - 1) / (nw / plan.S);
+        plan.direct = per_warp <= (int64_t)plan.rb * (1 + plan.nb);
+    }
     plan.smem = rows_ring_bytes(nw, plan.nb, plan.rb, plan.w) + rest;
     if (plan.smem > dev.smem_optin)
         return fail(Q4_ERR_SHAPE, "K=%d too large for the whole-row kernels", K);

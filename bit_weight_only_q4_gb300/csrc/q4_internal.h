@@ -76,6 +76,7 @@ q4_status gemv_launch(const GemvPlan &plan, GemvParams p, int M, cudaStream_t st
 // ---- register-prefetch weight-streaming kernel (gemv_rows.cu)
 struct RowsPlan {
     int kind = 0, mt = 1, w = 1, rb = 4, nb = 2, S = 1, grid = 0;
+    bool direct = false;       // one-k-step rows stored from the cross-lane reduction
     size_t smem = 0;
 };
 bool rows_eligible(int kind, int K);

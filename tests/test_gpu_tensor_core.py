@@ -120,12 +120,15 @@ def _x_tokens_of_many_scales(rng, M, K):
 
 
 @pytest.mark.parametrize("layout", ["int4", "nvfp4"])
-@pytest.mark.parametrize("M,N,K", [(16, 1024, 2048), (48, 384, 8192), (2048, 256, 2048)])
+@pytest.mark.parametrize("M,N,K", [(16, 1024, 2048), (48, 384, 8192), (2048, 256, 2048),
+                                   (100, 512, 1024), (300, 10000, 128)])
 def test_activations_beyond_the_fp16_range(q4, oracle_mod, layout, M, N, K):
     """The MMA operand is fp16 (max 65504) while bf16 activations reach 3.4e38:
     every token is scaled by a power of two before the conversion and its sums
     scaled back, so tokens at any magnitude match the oracle (in-kernel
-    conversion up to 64 tokens, the pre-pass at 2048) and no error bit is set."""
+    conversion up to 64 tokens, the pre-pass above: with A in tensor memory at
+    100 and 2048 tokens, with two-row-tile CTAs at 300 tokens x 10000 rows) and no
+    error bit is set."""
     rng = synth.rng_for(304, M, N, K)
     w = _mat(layout, rng, N, K)
     x = _x_tokens_of_many_scales(rng, M, K)
