@@ -1,25 +1,31 @@
 // Weight-streaming kernels for sm_103a that own whole rows: the decode GEMV of
 // both 4-bit layouts for one to four tokens, and the restricted BF16 head.
 //
-// Same arithmetic as the other streaming kernels (stream_common.cuh: prescaled
-// fp16 x, shift-free E2M1 / fp16-magic int4 decode, fp32 accumulation by
-// mixed-precision FMAs).  Data movement is chosen for short, dependent calls:
+// Arithmetic: x staged per 32-column chunk with a power-of-two prescale
+// (stream_common.cuh); NVFP4 decoded by cvt.rn.f16x2.e2m1x2 and summed per half
+// group in packed fp16 FMAs, the half sums meeting the group scales in
+// mixed-precision FMAs; int4 summed exactly with dp2a on int16-staged x, scale
+// and min applied to the integer sums in fp32.  Data movement is chosen for
+// short, dependent calls:
 //
 //   * Each CTA owns a contiguous range of output rows with their full K.  Warp w
-//     owns one k-step ks = w % S (1024 4-bit or 256 bf16 columns) of the rows
-//     g, g + G, g + 2G, ... of its CTA (g = w / S, G = warps / S).  S is a
-//     template parameter, so the warp geometry costs no divisions.  No row is
-//     split between CTAs: no workspace, deterministic results.
+//     owns one k-step ks = w % S (W x 1024 4-bit or 256 bf16 columns, W = 1 or
+//     2 slices per lane) of the rows g, g + G, g + 2G, ... of its CTA (g = w / S,
+//     G = warps / S).  S is a template parameter, so the warp geometry costs no
+//     divisions.  No row is split between CTAs: no workspace, deterministic
+//     results.
 //   * Weights do not depend on the previous kernel, so they are requested
-//     before griddepcontrol.wait.  For one token a call runs one 16-warp CTA per
-//     SM on half of the SM's registers and shared memory, so the next call's CTA
-//     is resident beside it (programmatic dependent launch) and streams its
-//     weights while this call computes.
+//     before griddepcontrol.wait.  For one token a call runs one CTA per SM on
+//     half of the SM's registers and shared memory (16 warps with one slice per
+//     lane, or 8 warps with two for the 4-bit layouts at K <= 2048), so the next
+//     call's CTA is resident beside it (programmatic dependent launch) and
+//     streams its weights while this call computes.
 //   * After the wait the CTA stages x once in shared memory (prescaled fp16);
 //     every warp keeps its k-step's slice in registers, decodes and multiplies
 //     its rows, reduces each row across lanes (transposing butterfly) and parks
 //     the partial per k-step in shared memory.  A final pass sums each row's S
-//     partials in k order and stores bf16.
+//     partials in k order and stores bf16 (or, in the DS variant, with one
+//     k-step and few rows per warp, the reduction stores each row at once).
 //
 // Bringing the weights in: for one token the first RB rows of every warp come
 // straight into registers with 128-bit loads; every later row comes through a
