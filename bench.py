@@ -49,7 +49,7 @@ CALLS_PER_STEP = 8192
 # valid only for the kernel sources it was taken on (see _kernel_sha).
 TRAFFIC = {
     # workload key: (bytes per launch, _kernel_sha() when captured)
-    "nvfp4_gemv": (18919424, "34632184ce813853f5483414916b20f00ab253a92824d57c69dd201d3dcded0a"),
+    "nvfp4_gemv": (18919936, "03360da5c802ba8e7bcfcc5c71750e9d1255abd8631d054df1a48f5955185b73"),
 }
 
 
