@@ -232,20 +232,22 @@ size_t q4_workspace_bytes(int layout, int M, int N, int K)
         sms = 160;   // no device: size for a GB300-class part
     }
     size_t a = 0;
+    int kind = 0;
     if (layout == Q4_LAYOUT_INT4G128) {
         if (K % 128)
             return 0;
-        a = stream_ws_layout(W_INT4, M, N, K).total;
+        kind = W_INT4;
     } else if (layout == Q4_LAYOUT_NVFP4) {
         if (K % 16)
             return 0;
-        a = stream_ws_layout(W_NVFP4_A16, M, N, K).total;
+        kind = W_NVFP4_A16;
     } else {
         return 0;
     }
+    a = stream_ws_layout(kind, M, N, K).total;
     // the tensor-core path (and its copy of x) only when the call can take it
     const bool tc = M >= kTensorCoreMinM || (g_flags.load() & Q4_FLAG_FORCE_TENSOR_CORE);
-    const size_t b = tc ? tc_workspace_bytes(M, N, K, sms) : 0;
+    const size_t b = tc ? tc_workspace_bytes(kind, M, N, K, sms) : 0;
     return a > b ? a : b;
 }
 

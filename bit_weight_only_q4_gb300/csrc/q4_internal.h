@@ -85,7 +85,7 @@ q4_status rows_launch(const RowsPlan &plan, GemvParams p, int M, cudaStream_t st
 
 // ---- tcgen05 tensor-core GEMM (tc_gemm.cu)
 bool tc_eligible(int kind, int M, int N, int K);
-size_t tc_workspace_bytes(int M, int N, int K, int sms);
+size_t tc_workspace_bytes(int kind, int M, int N, int K, int sms);
 q4_status tc_launch(int kind, const void *x, const uint8_t *codes, const void *scale,
                     const void *minv, const float *gscale, void *y, int M, int N, int K,
                     void *ws, size_t ws_bytes, cudaStream_t stream, bool pdl);

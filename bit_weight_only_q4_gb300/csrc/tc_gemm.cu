@@ -97,10 +97,11 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr)
 
 // Instruction descriptor of tcgen05.mma kind::f16: fp16 A and B (K-major),
 // fp32 accumulator, M = 128, N = n.
-__device__ __forceinline__ uint32_t idesc_f16(int n)
+__device__ __forceinline__ uint32_t idesc_f16(int n, bool bf16 = false)
 {
+    const uint32_t ab = bf16 ? 1u : 0u;        // operand format: 0 f16, 1 bf16
     return (1u << 4)                    // D format: f32
-         | (0u << 7) | (0u << 10)       // A, B format: f16
+         | (ab << 7) | (ab << 10)       // A, B format
          | ((uint32_t)(n >> 3) << 17)   // N / 8
          | ((uint32_t)(TC_ROWS >> 4) << 24);   // M / 16
 }
@@ -189,6 +190,48 @@ __device__ __forceinline__ float pow2f_tc(int e)
     return __uint_as_float((uint32_t)(e + 127) << 23);
 }
 
+__device__ __forceinline__ uint32_t bmul2(uint32_t a, uint32_t b)
+{
+    uint32_t r;
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
+// An fp16 pair whose values have at most 7 significant bits and no bits below
+// the mantissa's third (every E2M1 value qualifies) -> the bf16 pair of the same
+// values times 2^-112: the exponent and mantissa fields move down by 3 bits (f16
+// bias 15, bf16 bias 127), the sign stays; zero stays zero.
+__device__ __forceinline__ uint32_t f16x2_to_bf16x2_scaled(uint32_t h)
+{
+    return ((h & 0x7fff7fffu) >> 3) | (h & 0x80008000u);
+}
+
+// NVFP4 with bf16 operands: the power of two 2^eg nearest below the global scale g
+// (clamped so that every E2M1 * e4m3 * 2^eg is a normal bf16 number and every
+// e4m3 * 2^(112 + eg) is finite in bf16) -- the weights are dequantised as
+// E2M1 * e4m3 * 2^eg, exactly, and the epilogue multiplies by g * 2^-eg.
+__device__ __forceinline__ int nvfp4_bf16_exponent(float g)
+{
+    const int eb = (int)((__float_as_uint(g) >> 23) & 0xffu);
+    if (eb == 0xff)
+        return 0;
+    const int e = eb - 127;
+    return e < -100 ? -100 : (e > 6 ? 6 : e);
+}
+
+// e4m3 scale byte -> bf16 pair (splatted) of scale * 2^(112 + eg), exact (4
+// significant bits, magnitude between 2^3 and 2^127).
+__device__ __forceinline__ uint32_t e4m3_to_bf16x2_scaled(uint32_t byte, float up)
+{
+    float lo, hi;
+    f16x2_to_f32x2(e4m3x2_to_f16x2(byte & 0xffu), lo, hi);
+    (void)hi;
+    const float s = lo * up;
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %1;" : "=r"(r) : "f"(s));
+    return r;
+}
+
 // Per-token power-of-two prescale of x for the fp16 MMA operand.  The MMA reads
 // x as fp16, whose range ends at 65504, while bf16 activations reach 3.4e38.  So
 // each token m is multiplied by 2^e_m before the conversion, with e_m chosen
@@ -228,8 +271,9 @@ __device__ __forceinline__ uint32_t f16x2_splat(uint32_t h16)
 // One packed code word (8 consecutive columns of a row, low nibble = even column)
 // -> 4 f16 pairs of weights in column order.  int4: w = c * s + min (s2, m2 the
 // splatted fp16 scale and min; one rounding); NVFP4: w = E2M1 * e4m3 scale (sg
-// splatted; exact in fp16, the global scale is applied in the epilogue).
-template <int LAYOUT>
+// splatted; exact in fp16, the global scale is applied in the epilogue), or with
+// XB the bf16 pairs of E2M1 * e4m3 * 2^eg (exact).
+template <int LAYOUT, bool XB>
 __device__ __forceinline__ void tc_dequant_word(uint32_t word, uint32_t s2, uint32_t m2,
                                                 uint32_t (&o)[4])
 {
@@ -243,6 +287,13 @@ __device__ __forceinline__ void tc_dequant_word(uint32_t word, uint32_t s2, uint
             v2 = hfma2(v2, 0x2C003C00u, 0xD400E400u);   // * (1, 1/16) + (-1024, -64)
             o[b] = hfma2(v2, s2, m2);                   // c * s + min, one rounding
         }
+    } else if constexpr (XB) {
+        (void)m2;
+        uint32_t h[4];
+        e2m1x8_to_f16x2x4(word, h);
+#pragma unroll
+        for (int b = 0; b < 4; ++b)                     // exact in bf16 (s2: see
+            o[b] = bmul2(f16x2_to_bf16x2_scaled(h[b]), s2);   // e4m3_to_bf16x2_scaled)
     } else {
         (void)m2;
         uint32_t h[4];
@@ -311,7 +362,8 @@ __device__ __forceinline__ void tc_splitk_sum(const TcParams &p, const float4 *p
 template <int LAYOUT, bool SPLITK>
 __device__ __forceinline__ void tc_epilogue(const TcParams &p, uint32_t tmem_base, bool ok, int w,
                                             int lane, int n0, int m0, int tile, int ks,
-                                            const float *xdn, unsigned *last_flag, bool free_tmem)
+                                            const float *xdn, unsigned *last_flag, bool free_tmem,
+                                            float gmul)
 {
     const int TN = p.TN;
     const int quad = (w + 2) & 3;            // TMEM lane quadrant of this warp
@@ -321,7 +373,7 @@ __device__ __forceinline__ void tc_epilogue(const TcParams &p, uint32_t tmem_bas
     const bool nok = n < p.N;
     float gsc = 1.f;
     if constexpr (LAYOUT == 1)
-        gsc = __ldg(p.gscale);
+        gsc = __ldg(p.gscale) * gmul;      // gmul: a power of two, exact
     const int ncb = (TN + 16 * TC_GROUPS - 1) / (16 * TC_GROUPS);   // same for every worker
     for (int it = 0; it < ncb; ++it) {
         const int cb = grp * 16 + it * 16 * TC_GROUPS;
@@ -409,13 +461,19 @@ struct TcStage {
 // issues both tiles' MMAs against each x sub-tile it loads, into two TMEM
 // accumulators (columns 0 .. 255 and 256 .. 511), so each token tile is read from
 // L2 half as often; the stage then holds both A sub-tiles and a 256-row code box.
-template <int LAYOUT, int SC, int G, bool ATM, int RT>   // LAYOUT 0 int4-g128, 1 NVFP4; G worker groups
+//
+// XB (NVFP4): the MMA takes bf16 operands.  x then goes to the tensor cores
+// exactly as the caller stored it (no scan, no conversion, no prescale), and the
+// weights are dequantised to bf16 as E2M1 * e4m3 * 2^eg, which is exact (at most
+// 6 significant bits; see nvfp4_bf16_exponent).
+template <int LAYOUT, int SC, int G, bool ATM, int RT, bool XB = false>   // LAYOUT 0 int4-g128, 1 NVFP4; G worker groups
 __global__ void __launch_bounds__(TC_THREADS, 1)
 q4_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap wmap,
              TcParams p)
 {
     static_assert(!ATM || SC == 1, "A in tensor memory takes one chunk per stage");
     static_assert(RT == 1 || (RT == 2 && SC == 1 && !ATM), "two row tiles: one chunk per stage, A in shared memory");
+    static_assert(!XB || LAYOUT == 1, "bf16 operands: NVFP4 only");
     constexpr uint32_t A_BYTES = (uint32_t)RT * TcStage<SC>::A;
     constexpr uint32_t CODE_BYTES = (uint32_t)RT * TcStage<SC>::CODE;
     constexpr uint32_t OFF_X = ATM ? 0u : A_BYTES;          // x sub-tiles in a stage
@@ -499,7 +557,7 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
     } else if (warp == 1) {
         // ------------------------------------------------------------- MMA issue
         if (lane == 0) {
-            const uint32_t idesc = idesc_f16(TN);
+            const uint32_t idesc = idesc_f16(TN, XB);
             for (int u = 0; u < nsup; ++u) {
                 const int s = u % NS, use = u / NS;
                 if (!mbar_wait(smem_u32(&bars[NS + s]), use & 1, p.err))
@@ -554,6 +612,13 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
         // stage's copies are in flight); x converted by the pre-pass brings its
         // 2^-e_m along.  The epilogue multiplies token m's sums by 2^-e_m.
         auto prescale = [&]() {
+            if constexpr (XB) {
+                // bf16 x goes to the MMA unscaled; the workers never read x
+                for (int t = w * 32 + lane; t < TN; t += TC_WORKERS * 32)
+                    s_xdn[t] = 1.f;
+                asm volatile("bar.sync 2, %0;" ::"r"(TC_WORKERS * 32) : "memory");
+                return;
+            }
             pdl_wait();                              // x comes from the previous kernel
             if (!p.x_f16) {
                 // eight consecutive threads per token (TN <= 64 here), four 16-byte
@@ -624,6 +689,9 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
                     return ld_nc_u16(static_cast<const uint8_t *>(p.scale) + n * (p.K / 16) + kc * 4 + 2 * h);
                 }
             };
+            float bf16_up = 1.f;               // XB: see e4m3_to_bf16x2_scaled
+            if constexpr (XB)
+                bf16_up = pow2f_tc(112 + nvfp4_bf16_exponent(__ldg(p.gscale)));
             uint32_t scq[SA];
 #pragma unroll
             for (int j = 0; j < SA; ++j)
@@ -644,6 +712,8 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
                 if constexpr (LAYOUT == 0) {
                     s2 = f16x2_splat(sc & 0xffffu);
                     m2 = f16x2_splat(sc >> 16);
+                } else if constexpr (XB) {
+                    s2 = e4m3_to_bf16x2_scaled(sc & 0xffu, bf16_up);
                 } else {
                     s2 = f16x2_splat(e4m3x2_to_f16x2(sc & 0xffu) & 0xffffu);
                 }
@@ -651,10 +721,11 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
                 for (int j = 0; j < 4; ++j) {
                     if constexpr (LAYOUT == 1) {
                         if (j == 2)
-                            s2 = f16x2_splat(e4m3x2_to_f16x2((sc >> 8) & 0xffu) & 0xffffu);
+                            s2 = XB ? e4m3_to_bf16x2_scaled((sc >> 8) & 0xffu, bf16_up)
+                                    : f16x2_splat(e4m3x2_to_f16x2((sc >> 8) & 0xffu) & 0xffffu);
                     }
                     uint32_t o[4];
-                    tc_dequant_word<LAYOUT>(words[j], s2, m2, o);
+                    tc_dequant_word<LAYOUT, XB>(words[j], s2, m2, o);
 #pragma unroll
                     for (int b = 0; b < 4; ++b)
                         v[4 * j + b] = o[b];
@@ -719,6 +790,10 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
                 else
                     return ld_nc_u8(static_cast<const uint8_t *>(base) + n * (p.K / 16) + kc * 4 + qd);
             };
+            // XB: e4m3 scales become bf16 scale * 2^(112 + eg) (see e4m3_to_bf16x2_scaled)
+            float bf16_up = 1.f;
+            if constexpr (XB)
+                bf16_up = pow2f_tc(112 + nvfp4_bf16_exponent(__ldg(p.gscale)));
             uint32_t scq[SA][STEPS], mnq[SA][STEPS];
 #pragma unroll
             for (int j = 0; j < SA; ++j)
@@ -741,7 +816,7 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
                 // swizzle).  Only tiles of at most 64 tokens are converted here
                 // (larger M arrive in fp16), so a thread has at most SC * G vectors:
                 // the loop is unrolled and interleaves with the code loads below.
-                if (!p.x_f16) {
+                if (!XB && !p.x_f16) {
                     const int per = TN * 8;                  // vectors per sub-tile
 #pragma unroll
                     for (int j = 0; j < SC * G; ++j) {
@@ -772,7 +847,9 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
                     const uint32_t words[2] = {cw.x, cw.y};
                     unsigned char *arow = st + c * 16384 + rd * 128;
                     uint32_t sg = 0u;
-                    if constexpr (LAYOUT == 1)
+                    if constexpr (XB)
+                        sg = e4m3_to_bf16x2_scaled(scs[k], bf16_up);
+                    else if constexpr (LAYOUT == 1)
                         sg = f16x2_splat(e4m3x2_to_f16x2(scs[k] & 0xffu) & 0xffffu);
 #pragma unroll
                     for (int j = 0; j < 2; ++j) {           // 8 K columns per 16-byte chunk
@@ -789,6 +866,12 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
                                 v2 = hfma2(v2, 0x2C003C00u, 0xD400E400u);   // * (1, 1/16) + (-1024, -64)
                                 o[b] = hfma2(v2, s2, m2);                   // c * s + min, one rounding
                             }
+                        } else if constexpr (XB) {
+                            uint32_t h[4];
+                            e2m1x8_to_f16x2x4(words[j], h);
+#pragma unroll
+                            for (int b = 0; b < 4; ++b)                    // exact in bf16
+                                o[b] = bmul2(f16x2_to_bf16x2_scaled(h[b]), sg);
                         } else {
                             uint32_t h[4];
                             e2m1x8_to_f16x2x4(words[j], h);
@@ -828,11 +911,14 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
         const bool ok = nsup > 0 && mbar_wait_warp(smem_u32(&bars[3 * NS]), 0, p.err);
         tc_fence_after();
         __shared__ unsigned last_flag;
+        float gmul = 1.f;
+        if constexpr (XB)
+            gmul = pow2f_tc(-nvfp4_bf16_exponent(__ldg(p.gscale)));
 #pragma unroll
         for (int rt = 0; rt < RT; ++rt)
             tc_epilogue<LAYOUT, RT == 1>(p, tmem_base + 256u * (uint32_t)rt, ok, w, lane, n0 + TC_ROWS * rt, m0,
                                 (tile_n * RT + rt) * p.tiles_m + tile_m, ks, s_xdn, &last_flag,
-                                rt == RT - 1);
+                                rt == RT - 1, gmul);
     }
 
     __syncthreads();
@@ -948,6 +1034,8 @@ static bool tc_preconvert(int M) { return M > 64; }
 // accumulators fill the tensor memory).
 constexpr bool kTcTmemA = true;
 constexpr bool kTcTwoRowTiles = true;
+// NVFP4 tiles whose x is not pre-converted take bf16 operands.
+constexpr bool kTcBf16Nvfp4 = true;
 
 // CTA tile: TN tokens (MMA N) x RT weight-row tiles of 128.  Each x sub-tile a
 // CTA loads feeds RT tiles' MMAs, so for prefill (x converted by the pre-pass,
@@ -999,9 +1087,14 @@ static int tc_ks(const DeviceInfo &dev, int M, int N, int K)
 // [fp16 x, prescaled per token][per-token 2^-e_m, fp32]
 static size_t tc_xf16_data_bytes(int M, int K) { return ((size_t)M * K * 2 + 255) / 256 * 256; }
 
-static size_t tc_xf16_bytes(int M, int K)
+// NVFP4 calls take bf16 operands (exact dequantised weights, x as stored): no
+// copy of x.
+static bool tc_bf16_operands(int kind) { return kTcBf16Nvfp4 && kind == W_NVFP4_A16; }
+
+static size_t tc_xf16_bytes(int kind, int M, int K)
 {
-    return tc_preconvert(M) ? tc_xf16_data_bytes(M, K) + ((size_t)M * 4 + 255) / 256 * 256 : 0;
+    return tc_preconvert(M) && !tc_bf16_operands(kind)
+               ? tc_xf16_data_bytes(M, K) + ((size_t)M * 4 + 255) / 256 * 256 : 0;
 }
 
 static size_t tc_split_bytes(int M, int N, int K, int sms)
@@ -1018,11 +1111,11 @@ static size_t tc_split_bytes(int M, int N, int K, int sms)
 
 // Workspace layout: [fp16 copy of x and its per-token scales (large M)][split-K
 // counters][partials].
-size_t tc_workspace_bytes(int M, int N, int K, int sms)
+size_t tc_workspace_bytes(int kind, int M, int N, int K, int sms)
 {
     if (K % TC_KC || M < 1 || N < 1)
         return 0;
-    return tc_xf16_bytes(M, K) + tc_split_bytes(M, N, K, sms);
+    return tc_xf16_bytes(kind, M, K) + tc_split_bytes(M, N, K, sms);
 }
 
 static CUresult tc_encode_maps(EncodeTiledFn enc, CUtensorMap &xmap, CUtensorMap &wmap,
@@ -1050,8 +1143,19 @@ static CUresult tc_encode_maps(EncodeTiledFn enc, CUtensorMap &xmap, CUtensorMap
 }
 
 template <int LAYOUT>
-static const void *tc_select_layout(int sc, bool atm, int rt)
+static const void *tc_select_layout(int sc, bool atm, int rt, bool xb)
 {
+    if constexpr (LAYOUT == 1) {
+        if (xb) {
+            if (rt == 2)
+                return reinterpret_cast<const void *>(&q4_tc_kernel<1, 1, 2, false, 2, true>);
+            if (atm)
+                return reinterpret_cast<const void *>(&q4_tc_kernel<1, 1, 2, true, 1, true>);
+            return sc == 4 ? reinterpret_cast<const void *>(&q4_tc_kernel<1, 4, 2, false, 1, true>)
+                 : sc == 2 ? reinterpret_cast<const void *>(&q4_tc_kernel<1, 2, 2, false, 1, true>)
+                           : reinterpret_cast<const void *>(&q4_tc_kernel<1, 1, 2, false, 1, true>);
+        }
+    }
     if (rt == 2)
         return reinterpret_cast<const void *>(&q4_tc_kernel<LAYOUT, 1, 2, false, 2>);
     if (atm)
@@ -1061,9 +1165,10 @@ static const void *tc_select_layout(int sc, bool atm, int rt)
                    : reinterpret_cast<const void *>(&q4_tc_kernel<LAYOUT, 1, 2, false, 1>);
 }
 
-static const void *tc_select(int kind, int sc, bool atm, int rt)
+static const void *tc_select(int kind, int sc, bool atm, int rt, bool xb)
 {
-    return kind == W_INT4 ? tc_select_layout<0>(sc, atm, rt) : tc_select_layout<1>(sc, atm, rt);
+    return kind == W_INT4 ? tc_select_layout<0>(sc, atm, rt, false)
+                          : tc_select_layout<1>(sc, atm, rt, xb);
 }
 
 q4_status tc_launch(int kind, const void *x, const uint8_t *codes, const void *scale,
@@ -1097,7 +1202,7 @@ q4_status tc_launch(int kind, const void *x, const uint8_t *codes, const void *s
     while (cols < p.TN)
         cols *= 2;
     p.tmem_cols = cols;
-    const size_t need = tc_workspace_bytes(M, N, K, dev.sms);
+    const size_t need = tc_workspace_bytes(kind, M, N, K, dev.sms);
     if (need > ws_bytes)
         return fail(Q4_ERR_WORKSPACE, "tensor-core path needs %zu bytes of workspace", need);
     const int rt = shape.RT;
@@ -1105,7 +1210,7 @@ q4_status tc_launch(int kind, const void *x, const uint8_t *codes, const void *s
         return fail(Q4_ERR_SHAPE, "tensor-core plan: split-K with two row tiles");
     const size_t tiles = (size_t)tc_tiles(M, N, dev.sms);     // 128-row tiles
     unsigned char *wsb = static_cast<unsigned char *>(ws);
-    const size_t xf16 = tc_xf16_bytes(M, K);
+    const size_t xf16 = tc_xf16_bytes(kind, M, K);
     if (p.KS > 1) {
         unsigned char *b = wsb + xf16;
         p.tickets = reinterpret_cast<unsigned *>(b);
@@ -1148,7 +1253,8 @@ q4_status tc_launch(int kind, const void *x, const uint8_t *codes, const void *s
     const size_t budget = dev.smem_optin - 1024 /* alignment */ - 3072 /* static */ - 256;
     // (measured for batched decode, x converted in the kernel: M = 48 step 31.4
     // against 27.9 us with A in shared memory, so only pre-converted tiles)
-    const bool atm = kTcTmemA && rt == 1 && p.x_f16 != 0;
+    const bool xb = tc_bf16_operands(kind);
+    const bool atm = kTcTmemA && rt == 1 && tc_preconvert(M);
     // A in tensor memory: the A sub-tiles after the accumulator, one 32-column
     // slot per stage
     p.tmem_a0 = (p.TN + 31) / 32 * 32;
@@ -1183,7 +1289,7 @@ q4_status tc_launch(int kind, const void *x, const uint8_t *codes, const void *s
     }
     // two worker groups, two stages dequantised at once (measured: prefill
     // GEMMs 5-22% faster than one group of 16 warps; batched decode unchanged)
-    const void *k = tc_select(kind, sc, atm, rt);
+    const void *k = tc_select(kind, sc, atm, rt, xb);
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess)
         return cuda_fail(e, "cudaFuncSetAttribute(tensor-core kernel)");

@@ -65,6 +65,10 @@ def test_workspace_bytes(lib):
     # each rounded up to 256 bytes; up to 64 tokens it converts x in the GEMM
     assert q4.workspace_bytes(0, 100, 2048, 128) == 100 * 128 * 2 + 512
     assert q4.workspace_bytes(0, 48, 2048, 128) == 0
+    # NVFP4 tensor-core calls take x as stored (bf16 operands): no copy of x
+    assert q4.workspace_bytes(1, 100, 2048, 128) == 0
+    assert q4.workspace_bytes(1, 2048, 8192, 2048) < 2048 * 2048 * 2 <= \
+        q4.workspace_bytes(0, 2048, 8192, 2048)
     # split-K needs counters and partial slots (the bound covers every kernel a
     # call may pick, including the tensor-core path forced by a flag)
     a = q4.workspace_bytes(0, 1, 2048, 2048)
