@@ -13,15 +13,18 @@
 //     tensor load with 128-byte swizzle) and the 128 rows x 32 bytes of packed
 //     codes (TMA tensor load) into a ring of shared-memory stages.
 //   * Sixteen worker warps in two groups of eight take the stages in turn and
-//     dequantise them into the A operand tiles (fp16, K-major, 128-byte
+//     dequantise them into the A operand tiles (16-bit, K-major, 128-byte
 //     swizzle): a thread takes 16 weights of one row per step, and a warp's code
-//     reads are 256 contiguous bytes (no bank conflicts).  They also convert the
-//     chunk's x tile in place from bf16 to fp16, each token scaled by a power of
-//     two that puts its largest |x| in [2^14, 2^15) (for large M a small kernel
-//     converts x once per call instead); the epilogue undoes the scale, so every
-//     bf16 activation is in range.  int4: w = fp16(c * s + m) (one fused
-//     multiply-add, single rounding); NVFP4: w = E2M1 * e4m3 in fp16, exact (the
-//     global scale is applied in the epilogue).
+//     reads are 256 contiguous bytes (no bank conflicts).
+//   * NVFP4: bf16 operands.  x goes to the MMA as stored, and the weights are
+//     E2M1 * e4m3 * 2^eg in bf16, exact (2^eg a power-of-two share of the global
+//     scale; the epilogue applies the rest).
+//   * int4: fp16 operands, w = fp16(c * s + m) (one fused multiply-add, single
+//     rounding).  The workers also convert the chunk's x tile in place from bf16
+//     to fp16, each token scaled by a power of two that puts its largest |x| in
+//     [2^14, 2^15) (for large M a small kernel converts x once per call
+//     instead); the epilogue undoes the scale, so every bf16 activation is in
+//     range.
 //   * Warp 1 allocates the TMEM accumulator (128 lanes x TN fp32 columns) and one
 //     thread issues tcgen05.mma (kind::f16, M=128, N=TN, K=16) four times per
 //     chunk, then tcgen05.commit frees the stage.

@@ -28,9 +28,11 @@
  * nearest even) from an fp32 row sum.  Below five tokens that sum is built from
  * exact int32 dot products (int4, x scaled to int16 per 32 columns) or from fp16
  * partial sums of at most eight products per half group (NVFP4); from five tokens
- * on, the tensor cores multiply fp16 operands (x scaled per token by a power of
- * two that keeps every bf16 value in the fp16 range, and the int4 weights rounded
- * once to fp16) into fp32 accumulators.
+ * on, the tensor cores multiply 16-bit operands into fp32 accumulators: for
+ * int4, fp16 (x scaled per token by a power of two that keeps every bf16 value in
+ * the fp16 range, and the weights rounded once to fp16); for NVFP4, bf16 (x as
+ * stored, and the weights E2M1 * e4m3, exact in bf16 after a power-of-two share of
+ * the global scale, the rest of which is applied to the accumulator).
  */
 #ifndef Q4_GB300_H
 #define Q4_GB300_H
@@ -82,8 +84,8 @@ unsigned q4_get_launch_flags(void);
  * Bytes of device workspace that q4_linear_int4g128 (layout 0) or
  * q4_linear_nvfp4 (layout 1) needs for an [M,N,K] call on the current device:
  * split-K partial sums and arrival counters of whichever kernel the call may use
- * under the current launch flags, and above 64 tokens the per-token prescaled
- * fp16 copy of x and its scales that the tensor-core path reads (the
+ * under the current launch flags, and for int4 above 64 tokens the per-token
+ * prescaled fp16 copy of x and its scales that the tensor-core path reads (the
  * tensor-core part counts from M = 5 on, or for any M while
  * Q4_FLAG_FORCE_TENSOR_CORE is set).
  * The workspace must be zero-filled once after allocation; every call leaves

@@ -56,8 +56,9 @@ def _mat(layout, rng, N, K):
                                    (33, 2049, 8192), (64, 2048, 8192), (16, 16384, 2048),
                                    (300, 10000, 256), (2048, 2432, 128)])
 def test_forced_tensor_core_shapes(q4, oracle_mod, layout, M, N, K):
-    """The tensor-core kernel on every shape (x converted in the kernel up to 64
-    tokens, by the pre-pass above; A sub-tiles in tensor memory from 65 to 255
+    """The tensor-core kernel on every shape (int4: x converted to fp16 in the
+    kernel up to 64 tokens, by the pre-pass above; NVFP4: bf16 operands, x as
+    stored; A sub-tiles in tensor memory from 65 to 255
     tokens; CTAs of two 128-row tiles for 256-token tiles, here with a ragged last
     token tile and a last row pair that ends inside its first tile or at its
     second)."""
@@ -123,12 +124,13 @@ def _x_tokens_of_many_scales(rng, M, K):
 @pytest.mark.parametrize("M,N,K", [(16, 1024, 2048), (48, 384, 8192), (2048, 256, 2048),
                                    (100, 512, 1024), (300, 10000, 128)])
 def test_activations_beyond_the_fp16_range(q4, oracle_mod, layout, M, N, K):
-    """The MMA operand is fp16 (max 65504) while bf16 activations reach 3.4e38:
-    every token is scaled by a power of two before the conversion and its sums
-    scaled back, so tokens at any magnitude match the oracle (in-kernel
-    conversion up to 64 tokens, the pre-pass above: with A in tensor memory at
-    100 and 2048 tokens, with two-row-tile CTAs at 300 tokens x 10000 rows) and no
-    error bit is set."""
+    """Tokens at magnitudes from 2^-60 to 2^120 match the oracle and set no error
+    bit.  int4: the MMA operand is fp16 (max 65504), so every token is scaled by
+    a power of two before the conversion and its sums scaled back (in-kernel
+    conversion up to 64 tokens, the pre-pass above).  NVFP4: bf16 operands take x
+    as stored, and the weights carry a power-of-two share of the global scale.
+    Both with A in tensor memory at 100 and 2048 tokens and with two-row-tile
+    CTAs at 300 tokens x 10000 rows."""
     rng = synth.rng_for(304, M, N, K)
     w = _mat(layout, rng, N, K)
     x = _x_tokens_of_many_scales(rng, M, K)
