@@ -140,3 +140,36 @@ def test_activations_beyond_the_fp16_range(q4, oracle_mod, layout, M, N, K):
     # the relative Frobenius bound is applied per token (tokens differ by 2^180)
     for m in range(M):
         P.check(y[m:m + 1], yo[m:m + 1], ao[m:m + 1], f"tc {layout} token {m} M={M}")
+
+
+@pytest.mark.parametrize("M,N,K", [(16, 384, 1024), (48, 2048, 8192), (100, 384, 1024),
+                                   (300, 10000, 128)])
+def test_nvfp4_global_scale_is_applied_exactly(q4, oracle_mod, M, N, K):
+    """NVFP4 on the tensor cores carries a power of two 2^eg of the global scale g
+    in its bf16 weights (eg clamped to [-100, 6]) and multiplies the accumulator by
+    g * 2^-eg.  Scaling g by a power of two therefore scales every output by the
+    same power exactly, wherever eg lands (inside the clamp, at either end of it),
+    as long as the outputs stay normal bf16 numbers; g = 0 gives zeros; and a
+    non-power-of-two g at either extreme matches the oracle.  Shapes: split-K
+    ring kernel, one row tile; A in tensor memory; two-row-tile CTAs."""
+    rng = synth.rng_for(305, M, N, K)
+    w = synth.nvfp4_matrix(rng, N, K, global_scale=1.0)
+    # |x| >= 2^-8, so that no product x * w * 2^eg falls below the fp32 normal range
+    xf = rng.standard_normal((M, K)).astype(np.float32)
+    xf = np.sign(xf) * np.maximum(np.abs(xf), np.float32(2.0 ** -8))
+    x = torch.from_numpy(xf).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    y1 = _run(q4, "nvfp4", x, w, q4.FLAG_FORCE_TENSOR_CORE).float()
+    for e in (-120, -100, -40, 6, 7, 40):
+        w.global_scale = np.float32(2.0 ** e)
+        yg = _run(q4, "nvfp4", x, w, q4.FLAG_FORCE_TENSOR_CORE)
+        want = (y1 * (2.0 ** e)).to(torch.bfloat16)
+        normal = (want.float().abs() >= 2.0 ** -126) | (y1 == 0)
+        assert normal.float().mean().item() > 0.99
+        assert torch.equal(yg.view(torch.int16)[normal], want.view(torch.int16)[normal]), e
+    w.global_scale = np.float32(0.0)
+    assert torch.count_nonzero(_run(q4, "nvfp4", x, w, q4.FLAG_FORCE_TENSOR_CORE)).item() == 0
+    for g in (3.1e-33, 1.7e3):
+        w.global_scale = np.float32(g)
+        y = _run(q4, "nvfp4", x, w, q4.FLAG_FORCE_TENSOR_CORE)
+        yo, ao = _oracle(oracle_mod, "nvfp4", x, w)
+        P.check(y.float() / g, yo / g, ao / g, f"tc nvfp4 g={g} M={M}")
