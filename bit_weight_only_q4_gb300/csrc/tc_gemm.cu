@@ -474,7 +474,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 q4_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap wmap,
              TcParams p)
 {
-    static_assert(!ATM || SC == 1, "A in tensor memory takes one chunk per stage");
+    static_assert(!ATM || SC <= 2, "A in tensor memory: one or two chunks per stage");
     static_assert(RT == 1 || (RT == 2 && SC == 1 && !ATM), "two row tiles: one chunk per stage, A in shared memory");
     static_assert(!XB || LAYOUT == 1, "bf16 operands: NVFP4 only");
     constexpr uint32_t A_BYTES = (uint32_t)RT * TcStage<SC>::A;
@@ -576,11 +576,18 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
                 if constexpr (ATM) {
                     (void)alo;
                     (void)ahi;
-                    const uint32_t a = tmem_base + (uint32_t)p.tmem_a0 + 32u * (uint32_t)s;
+                    // chunk c of stage s: A in columns a0 + 32 (SC s + c) .. + 31
+                    const uint32_t a = tmem_base + (uint32_t)p.tmem_a0 + 32u * (uint32_t)(SC * s);
 #pragma unroll
-                    for (int kk = 0; kk < TC_KC / 16; ++kk)
-                        mma_f16_tmem_a(tmem_base, a + 8u * kk, blo + 2u * kk, bhi, idesc,
-                                       (u > 0 || kk > 0) ? 1u : 0u);
+                    for (int c = 0; c < SC; ++c) {
+                        if (c >= nv)
+                            break;
+#pragma unroll
+                        for (int kk = 0; kk < TC_KC / 16; ++kk)
+                            mma_f16_tmem_a(tmem_base, a + 32u * (uint32_t)c + 8u * kk,
+                                           blo + (uint32_t)c * (x_stride >> 4) + 2u * kk, bhi, idesc,
+                                           (u > 0 || c > 0 || kk > 0) ? 1u : 0u);
+                    }
                 } else {
 #pragma unroll
                     for (int c = 0; c < SC; ++c) {
@@ -665,12 +672,14 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
         if constexpr (ATM) {
             // G groups of WG = 16 / G warps take the stages in turn.  A warp may
             // write only TMEM lane quadrant warp % 4, so it owns rows 32 (warp % 4) +
-            // lane; the WG / 4 warps of a group in one quadrant split the chunk's 64
-            // columns (h = 0, 1: columns 32 h .. + 31).  A thread reads its row's 16
-            // code bytes, dequantises 32 weights and writes them as 16 packed columns
-            // of its lane.
+            // lane; the WG / 4 warps of a group in one quadrant split the stage's
+            // 64 SC columns (h = 0, 1: CPT = 32 SC columns from CPT h, i.e. half a
+            // chunk for SC = 1 and chunk h for SC = 2).  A thread reads its row's
+            // 16 SC code bytes, dequantises CPT weights and writes them as 16 SC
+            // packed columns of its lane.
             static_assert(TC_WORKERS / G == 8, "two warps per quadrant and group");
             constexpr int SA = 4;                    // stages of scales loaded ahead
+            constexpr int CPT = 32 * SC;             // columns per thread and stage
             const int gi = w / 8;
             const int h = (w % 8) / 4;
             const int quad = warp & 3;
@@ -679,17 +688,21 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
             const bool rok = n < p.N;
             const uint32_t t_lane = (uint32_t)(quad * 32) << 16;
             // int4: scale | min << 16 of the row's group; NVFP4: the e4m3 scales of
-            // the thread's two 16-column groups (low byte first)
+            // the thread's 2 SC 16-column groups (low byte first)
             auto load_scale = [&](int u) -> uint32_t {
-                if (u >= nsup || !rok)
+                const int col = (c0 + u * SC) * TC_KC + CPT * h;   // first column
+                if (u >= nsup || !rok || col / TC_KC >= c1)
                     return 0u;
-                const int kc = c0 + u;
                 if constexpr (LAYOUT == 0) {
-                    const int64_t g2 = n * (p.K / 128) + kc / 2;
+                    const int64_t g2 = n * (p.K / 128) + col / 128;
                     return ld_nc_u16(static_cast<const uint16_t *>(p.scale) + g2) |
                            (ld_nc_u16(p.minv + g2) << 16);
                 } else {
-                    return ld_nc_u16(static_cast<const uint8_t *>(p.scale) + n * (p.K / 16) + kc * 4 + 2 * h);
+                    const uint8_t *sp = static_cast<const uint8_t *>(p.scale) + n * (p.K / 16) + col / 16;
+                    if constexpr (SC == 1)
+                        return ld_nc_u16(sp);
+                    else
+                        return ld_nc_u32(sp);
                 }
             };
             float bf16_up = 1.f;               // XB: see e4m3_to_bf16x2_scaled
@@ -708,33 +721,36 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
                 // The slot's previous A was read by MMAs whose commit the producer
                 // waited for before requesting this use's copies.
                 tc_fence_after();
-                const uint4 cw = *reinterpret_cast<const uint4 *>(st + x_stride + row * 32 + h * 16);
-                const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
-                uint32_t v[16];
-                uint32_t s2, m2 = 0u;
-                if constexpr (LAYOUT == 0) {
-                    s2 = f16x2_splat(sc & 0xffffu);
+                const unsigned char *crow = st + SC * x_stride + row * (32 * SC) + h * (16 * SC);
+                uint32_t m2 = 0u;
+                if constexpr (LAYOUT == 0)
                     m2 = f16x2_splat(sc >> 16);
-                } else if constexpr (XB) {
-                    s2 = e4m3_to_bf16x2_scaled(sc & 0xffu, bf16_up);
-                } else {
-                    s2 = f16x2_splat(e4m3x2_to_f16x2(sc & 0xffu) & 0xffffu);
-                }
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    if constexpr (LAYOUT == 1) {
-                        if (j == 2)
-                            s2 = XB ? e4m3_to_bf16x2_scaled((sc >> 8) & 0xffu, bf16_up)
-                                    : f16x2_splat(e4m3x2_to_f16x2((sc >> 8) & 0xffu) & 0xffffu);
+                for (int i = 0; i < SC; ++i) {         // 32 columns: 16 packed TMEM columns
+                    const uint4 cw = *reinterpret_cast<const uint4 *>(crow + 16 * i);
+                    const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
+                    uint32_t v[16];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        uint32_t s2;
+                        if constexpr (LAYOUT == 0) {
+                            s2 = f16x2_splat(sc & 0xffffu);
+                        } else {
+                            // 16-column group (2 i + j / 2) of the thread's columns
+                            const uint32_t b = (sc >> (8 * (2 * i + j / 2))) & 0xffu;
+                            s2 = XB ? e4m3_to_bf16x2_scaled(b, bf16_up)
+                                    : f16x2_splat(e4m3x2_to_f16x2(b) & 0xffffu);
+                        }
+                        uint32_t o[4];
+                        tc_dequant_word<LAYOUT, XB>(words[j], s2, m2, o);
+#pragma unroll
+                        for (int b = 0; b < 4; ++b)
+                            v[4 * j + b] = o[b];
                     }
-                    uint32_t o[4];
-                    tc_dequant_word<LAYOUT, XB>(words[j], s2, m2, o);
-#pragma unroll
-                    for (int b = 0; b < 4; ++b)
-                        v[4 * j + b] = o[b];
+                    tmem_st16(tmem_base + t_lane + (uint32_t)p.tmem_a0 + (uint32_t)(32 * SC) * (uint32_t)st_i +
+                                  (uint32_t)(16 * SC) * (uint32_t)h + 16u * (uint32_t)i,
+                              v);
                 }
-                tmem_st16(tmem_base + t_lane + (uint32_t)p.tmem_a0 + 32u * (uint32_t)st_i + 16u * (uint32_t)h,
-                          v);
                 asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
                 tc_fence_before();
                 __syncwarp();
@@ -1039,6 +1055,8 @@ constexpr bool kTcTmemA = true;
 constexpr bool kTcTwoRowTiles = true;
 // NVFP4 tiles whose x is not pre-converted take bf16 operands.
 constexpr bool kTcBf16Nvfp4 = true;
+// ... and their tiles of at most 64 tokens keep A in tensor memory as well.
+constexpr bool kTcTmemASkinny = true;
 
 // CTA tile: TN tokens (MMA N) x RT weight-row tiles of 128.  Each x sub-tile a
 // CTA loads feeds RT tiles' MMAs, so for prefill (x converted by the pre-pass,
@@ -1153,7 +1171,8 @@ static const void *tc_select_layout(int sc, bool atm, int rt, bool xb)
             if (rt == 2)
                 return reinterpret_cast<const void *>(&q4_tc_kernel<1, 1, 2, false, 2, true>);
             if (atm)
-                return reinterpret_cast<const void *>(&q4_tc_kernel<1, 1, 2, true, 1, true>);
+                return sc == 2 ? reinterpret_cast<const void *>(&q4_tc_kernel<1, 2, 2, true, 1, true>)
+                               : reinterpret_cast<const void *>(&q4_tc_kernel<1, 1, 2, true, 1, true>);
             return sc == 4 ? reinterpret_cast<const void *>(&q4_tc_kernel<1, 4, 2, false, 1, true>)
                  : sc == 2 ? reinterpret_cast<const void *>(&q4_tc_kernel<1, 2, 2, false, 1, true>)
                            : reinterpret_cast<const void *>(&q4_tc_kernel<1, 1, 2, false, 1, true>);
@@ -1257,19 +1276,22 @@ q4_status tc_launch(int kind, const void *x, const uint8_t *codes, const void *s
     // (measured for batched decode, x converted in the kernel: M = 48 step 31.4
     // against 27.9 us with A in shared memory, so only pre-converted tiles)
     const bool xb = tc_bf16_operands(kind);
-    const bool atm = kTcTmemA && rt == 1 && tc_preconvert(M);
-    // A in tensor memory: the A sub-tiles after the accumulator, one 32-column
-    // slot per stage
+    // skinny NVFP4 tiles keep A in tensor memory too, two chunks per stage
+    const bool atm_skinny = kTcTmemASkinny && xb && !tc_preconvert(M);
+    const bool atm = kTcTmemA && rt == 1 && (tc_preconvert(M) || atm_skinny);
+    // A in tensor memory: the A sub-tiles after the accumulator, SC 32-column
+    // slots per stage
     p.tmem_a0 = (p.TN + 31) / 32 * 32;
-    const int ns_cap = atm ? (512 - p.tmem_a0) / 32 : 8;
     const size_t a_bytes = atm ? 0 : 16384 * (size_t)rt;
     const size_t code_bytes = 4096 * (size_t)rt;
+    const int sc_max = atm_skinny ? 2 : ((atm || rt == 2) ? 1 : 4);
     int sc = 1, ns = 0;
     for (int need_ns = 4; need_ns >= 2 && ns == 0; --need_ns)
-        for (int cand = (atm || rt == 2) ? 1 : 4; cand >= 1; cand /= 2) {
+        for (int cand = sc_max; cand >= 1; cand /= 2) {
             const size_t stage = (size_t)cand * (a_bytes + x_stride + code_bytes);
             const int fit = (int)(budget / stage);
-            if (fit >= need_ns) {
+            const int ns_cap = atm ? (512 - p.tmem_a0) / (32 * cand) : 8;
+            if (fit >= need_ns && ns_cap >= need_ns) {
                 sc = cand;
                 ns = fit > ns_cap ? ns_cap : fit;
                 break;
