@@ -452,13 +452,14 @@ struct TcStage {
     static constexpr uint32_t CODE = SC * 4096u;        // 128 rows x SC * 32 bytes
 };
 
-// ATM (x converted by the pre-pass, one chunk per stage): the dequantised A
-// sub-tile goes to tensor memory instead of shared memory.  A stage then holds
-// only the x sub-tile and the codes, so more stages fit (more copies in flight),
-// the A tile costs no shared-memory bandwidth, and an MMA reading A from TMEM is
-// shorter at N = 256 (138 against 171 cycles, measured alone).  TMEM:
-// accumulator in columns 0 .. TN - 1, the A sub-tile of ring stage s in columns
-// a0 + 32 s .. + 31 (a0 = p.tmem_a0, TN rounded up to 32).
+// ATM (tiles of more than 64 tokens, one chunk per stage; NVFP4 tiles of at most
+// 64 tokens, two): the dequantised A sub-tiles go to tensor memory instead of
+// shared memory.  A stage then holds only the x sub-tiles and the codes, so more
+// stages fit (more copies in flight), the A tiles cost no shared-memory
+// bandwidth, and an MMA reading A from TMEM is shorter at N = 256 (138 against
+// 171 cycles, measured alone).  TMEM: accumulator in columns 0 .. TN - 1, chunk c
+// of ring stage s in columns a0 + 32 (SC s + c) .. + 31 (a0 = p.tmem_a0, TN
+// rounded up to 32).
 //
 // RT = 2 (prefill tiles of 256 tokens): a CTA owns two 128-row weight tiles and
 // issues both tiles' MMAs against each x sub-tile it loads, into two TMEM
