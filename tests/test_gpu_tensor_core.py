@@ -54,11 +54,14 @@ def _mat(layout, rng, N, K):
                                    (64, 384, 1024), (200, 130, 2048), (300, 256, 384),
                                    (17, 8192, 128), (48, 96, 8192), (8, 512, 2048),
                                    (33, 2049, 8192), (64, 2048, 8192), (16, 16384, 2048),
-                                   (300, 10000, 256), (2048, 2432, 128)])
+                                   (300, 10000, 256), (2048, 2432, 128), (7, 130, 64),
+                                   (48, 200, 192)])
 def test_forced_tensor_core_shapes(q4, oracle_mod, layout, M, N, K):
     """The tensor-core kernel on every shape (int4: x converted to fp16 in the
     kernel up to 64 tokens, by the pre-pass above; NVFP4: bf16 operands, x as
-    stored; A sub-tiles in tensor memory from 65 to 255
+    stored, and up to 64 tokens A in tensor memory with two chunks per stage,
+    here also with a last stage of one chunk (K = 64, 192); A sub-tiles in
+    tensor memory from 65 to 255
     tokens; CTAs of two 128-row tiles for 256-token tiles, here with a ragged last
     token tile and a last row pair that ends inside its first tile or at its
     second)."""
