@@ -68,13 +68,6 @@ __device__ __forceinline__ uint32_t ld_nc_u8(const void *p)
     return r;
 }
 
-__device__ __forceinline__ uint32_t ld_nc_u32(const void *p)   // p 4-byte aligned
-{
-    uint32_t r;
-    asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(r) : "l"(p));
-    return r;
-}
-
 // ---------------------------------------------- programmatic dependent launch
 // Wait until the grids this one depends on have completed and their writes are
 // visible (a no-op when the kernel was not launched with PDL).

@@ -193,6 +193,14 @@ __device__ __forceinline__ float pow2f_tc(int e)
     return __uint_as_float((uint32_t)(e + 127) << 23);
 }
 
+// 32-bit load through the non-coherent path (p 4-byte aligned)
+__device__ __forceinline__ uint32_t ld_nc_u32(const void *p)
+{
+    uint32_t r;
+    asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(r) : "l"(p));
+    return r;
+}
+
 __device__ __forceinline__ uint32_t bmul2(uint32_t a, uint32_t b)
 {
     uint32_t r;

@@ -79,3 +79,11 @@ def test_kernel_hash_covers_the_gemv_sources():
     for rel in bench.KERNEL_SOURCES:
         assert os.path.exists(os.path.join(ROOT, rel)), rel
     assert any(rel.endswith("gemv_rows.cu") for rel in bench.KERNEL_SOURCES)
+
+
+def test_recorded_traffic_matches_the_current_gemv_sources():
+    """The bench's DRAM-traffic figure for the headline GEMV was captured on the
+    kernel sources as they are now: a change to them needs a new ncu capture."""
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.traffic_for("nvfp4_gemv") is not None
