@@ -1190,7 +1190,8 @@ static const void *tc_select_layout(int sc, bool atm, int rt, bool xb)
     if (rt == 2)
         return reinterpret_cast<const void *>(&q4_tc_kernel<LAYOUT, 1, 2, false, 2>);
     if (atm)
-        return reinterpret_cast<const void *>(&q4_tc_kernel<LAYOUT, 1, 2, true, 1>);
+        return sc == 2 ? reinterpret_cast<const void *>(&q4_tc_kernel<LAYOUT, 2, 2, true, 1>)
+                       : reinterpret_cast<const void *>(&q4_tc_kernel<LAYOUT, 1, 2, true, 1>);
     return sc == 4 ? reinterpret_cast<const void *>(&q4_tc_kernel<LAYOUT, 4, 2, false, 1>)
          : sc == 2 ? reinterpret_cast<const void *>(&q4_tc_kernel<LAYOUT, 2, 2, false, 1>)
                    : reinterpret_cast<const void *>(&q4_tc_kernel<LAYOUT, 1, 2, false, 1>);
@@ -1277,15 +1278,17 @@ q4_status tc_launch(int kind, const void *x, const uint8_t *codes, const void *s
     }
     // Stage = SC chunks (A sub-tiles, x sub-tiles, codes).  The largest SC that
     // still leaves four stages in flight (three, two) amortises each hand-off
-    // over more weights without starving the copies.  With x converted by the
-    // pre-pass the A sub-tiles live in tensor memory instead (one chunk per
-    // stage; up to eight stages, whose A sub-tiles take TMEM columns 256 ..).
+    // over more weights without starving the copies.  One-row-tile CTAs of more
+    // than 64 tokens, and NVFP4 CTAs of at most 64, keep the A sub-tiles in
+    // tensor memory instead, with two chunks per stage where three stages fit
+    // (each hand-off costs about as much as a stage's MMAs at 256 tokens: at
+    // M = 2048, K = 8192 -> N = 2048, 59 / 49 us int4 / NVFP4 against 77 / 65
+    // with one chunk per stage and six stages).
     const size_t x_stride = ((size_t)p.TN * 128 + 1023) / 1024 * 1024;
     const size_t budget = dev.smem_optin - 1024 /* alignment */ - 3072 /* static */ - 256;
-    // (measured for batched decode, x converted in the kernel: M = 48 step 31.4
-    // against 27.9 us with A in shared memory, so only pre-converted tiles)
     const bool xb = tc_bf16_operands(kind);
-    // skinny NVFP4 tiles keep A in tensor memory too, two chunks per stage
+    // (A in tensor memory for int4 tiles of at most 64 tokens, whose x is
+    // converted in the kernel, was slower: M = 48 step 31.4 against 27.9 us)
     const bool atm_skinny = kTcTmemASkinny && xb && !tc_preconvert(M);
     const bool atm = kTcTmemA && rt == 1 && (tc_preconvert(M) || atm_skinny);
     // A in tensor memory: the A sub-tiles after the accumulator, SC 32-column
@@ -1293,9 +1296,9 @@ q4_status tc_launch(int kind, const void *x, const uint8_t *codes, const void *s
     p.tmem_a0 = (p.TN + 31) / 32 * 32;
     const size_t a_bytes = atm ? 0 : 16384 * (size_t)rt;
     const size_t code_bytes = 4096 * (size_t)rt;
-    const int sc_max = atm_skinny ? 2 : ((atm || rt == 2) ? 1 : 4);
+    const int sc_max = atm ? 2 : (rt == 2 ? 1 : 4);
     int sc = 1, ns = 0;
-    for (int need_ns = 4; need_ns >= 2 && ns == 0; --need_ns)
+    for (int need_ns = atm ? 3 : 4; need_ns >= 2 && ns == 0; --need_ns)
         for (int cand = sc_max; cand >= 1; cand /= 2) {
             const size_t stage = (size_t)cand * (a_bytes + x_stride + code_bytes);
             const int fit = (int)(budget / stage);
