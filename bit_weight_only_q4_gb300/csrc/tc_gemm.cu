@@ -1062,6 +1062,8 @@ static bool tc_preconvert(int M) { return M > 64; }
 // accumulators fill the tensor memory).
 constexpr bool kTcTmemA = true;
 constexpr bool kTcTwoRowTiles = true;
+// Token-tile width of long token ranges fitted to whole waves (tc_long_tn).
+constexpr bool kTcFitWaves = true;
 // NVFP4 tiles whose x is not pre-converted take bf16 operands.
 constexpr bool kTcBf16Nvfp4 = true;
 // ... and their tiles of at most 64 tokens keep A in tensor memory as well.
@@ -1078,15 +1080,38 @@ struct TcShape {
     int TN, RT;
 };
 
+// Long token ranges (M >= 1024) take the token-tile width from 256 down to 192
+// that needs the fewest waves of CTAs per token of a tile (each CTA's time grows
+// with its width): at M = 2048, 240-token tiles give 144 one-row-tile CTAs
+// (8192 -> 2048) where 256 give 128, or 288 two-row-tile CTAs (2048 -> 8192), two
+// full waves of 152 SMs, where 256 give 1.7.
+static int tc_long_tn(int M, int64_t row_units, int sms)
+{
+    if (!kTcFitWaves || M < 1024)
+        return 256;
+    int best = 256;
+    int64_t best_cost = -1;
+    for (int tn = 256; tn >= 192; tn -= 16) {
+        const int64_t ctas = row_units * ((M + tn - 1) / tn);
+        const int64_t cost = (ctas + sms - 1) / sms * tn;
+        if (best_cost < 0 || cost < best_cost) {
+            best_cost = cost;
+            best = tn;
+        }
+    }
+    return best;
+}
+
 static TcShape tc_shape(int M, int N, int sms)
 {
     const int tn = M > 256 ? 256 : ((M + 15) / 16 * 16 < 16 ? 16 : (M + 15) / 16 * 16);
+    const int64_t rows1 = (N + TC_ROWS - 1) / TC_ROWS;
     if (!kTcTwoRowTiles || !tc_preconvert(M) || M < 256)
-        return {tn, 1};
+        return {M > 256 ? tc_long_tn(M, rows1, sms) : tn, 1};
     const int64_t pairs = (N + 2 * TC_ROWS - 1) / (2 * TC_ROWS);
     if (pairs * ((M + 255) / 256) * 2 > sms)
-        return {256, 2};
-    return {tn, 1};
+        return {tc_long_tn(M, pairs, sms), 2};
+    return {tc_long_tn(M, rows1, sms), 1};
 }
 
 // Tiles of 128 weight rows x TN tokens (a CTA owns RT of them).
