@@ -521,9 +521,10 @@ def run_extra(args, local):
 def run_profile(args, local):
     """Plain launches for an ncu capture: W warm-up calls, then K calls, no graphs
     and no timing (a number printed under a profiler is never a bench value).
-    GEMV workloads rotate their weight ring; prefill alternates the int4 and the
-    NVFP4 K=2048 -> N=8192 GEMM at M=2048 (select one with ncu's kernel filter:
-    template argument 0 is int4, 1 NVFP4); batched runs the NVFP4 K=8192 ->
+    GEMV workloads rotate their weight ring; prefill cycles through the int4 and
+    the NVFP4 K=2048 -> N=8192 GEMM, then the int4 and the NVFP4 K=8192 -> N=2048
+    GEMM, at M=2048 (template argument 0 of the kernel is int4, 1 NVFP4; the int4
+    calls also launch the x pre-pass); batched runs the NVFP4 K=8192 ->
     N=2048 GEMM at M=48; decode_step runs the step's distinct calls (fused
     q|k|v|gate|up 22528 x 2048, o 2048 x 2048, down 2048 x 8192, then the
     restricted head) over eight layers' weights (289 MB, beyond L2) in turn."""
@@ -540,14 +541,20 @@ def run_profile(args, local):
         wl = Workload(args.workload, device)
         call, desc = wl.call, wl.desc
     elif args.workload == "prefill":
-        x, w = synth.prefill("int4", 0)
-        xd, wd = P.bf16_dev(x), P.int4_dev(w)
-        _, wn = synth.prefill("nvfp4", 0)
-        wnd = P.nvfp4_dev(wn)
-        ws = q4.alloc_workspace(q4.LAYOUT_INT4G128, x.shape[0], w.N, w.K, device)
-        call = lambda i: (q4.q4_linear_int4g128(xd, *wd, workspace=ws) if i % 2 == 0
-                          else q4.q4_linear_nvfp4(xd, *wnd, workspace=ws))
-        desc = "prefill M=2048 K=2048 N=8192, int4 and nvfp4 in turn"
+        gemms = []
+        for si in (0, 1):
+            x, w = synth.prefill("int4", si)
+            _, wn = synth.prefill("nvfp4", si)
+            xd = P.bf16_dev(x)
+            ws = q4.alloc_workspace(q4.LAYOUT_INT4G128, x.shape[0], w.N, w.K, device)
+            gemms.append((q4.q4_linear_int4g128, xd, P.int4_dev(w), ws))
+            gemms.append((q4.q4_linear_nvfp4, xd, P.nvfp4_dev(wn), ws))
+
+        def call(i):
+            f, xd, wd, ws = gemms[i % 4]
+            f(xd, *wd, workspace=ws)
+        desc = ("prefill M=2048: int4 and nvfp4 K=2048 N=8192, then int4 and nvfp4 "
+                "K=8192 N=2048, in turn")
     elif args.workload == "decode_step":
         c = synth.DECODE_STACK_28
         H, F = c["hidden"], c["ffn"]
