@@ -1053,29 +1053,21 @@ bool tc_eligible(int kind, int M, int N, int K)
     return kind == W_INT4 || kind == W_NVFP4_A16;
 }
 
-// x is converted inside the GEMM for tiles of up to 64 tokens (at most SC
-// vectors per thread), by a separate pass for more.
+// Tiles of more than 64 tokens: int4 x is converted by a separate pass (up to 64
+// tokens, inside the GEMM: at most SC vectors per thread), and the dequantised A
+// sub-tiles live in tensor memory, except in CTAs that own two weight-row tiles
+// (two accumulators fill the tensor memory).
 static bool tc_preconvert(int M) { return M > 64; }
 
-// Tiles of pre-converted x keep their dequantised A sub-tiles in tensor memory,
-// except full 256-token tiles, whose CTAs own two weight-row tiles (two
-// accumulators fill the tensor memory).
-constexpr bool kTcTmemA = true;
-constexpr bool kTcTwoRowTiles = true;
-// Token-tile width of long token ranges fitted to whole waves (tc_long_tn).
-constexpr bool kTcFitWaves = true;
-// NVFP4 tiles whose x is not pre-converted take bf16 operands.
-constexpr bool kTcBf16Nvfp4 = true;
-// ... and their tiles of at most 64 tokens keep A in tensor memory as well.
-constexpr bool kTcTmemASkinny = true;
-
 // CTA tile: TN tokens (MMA N) x RT weight-row tiles of 128.  Each x sub-tile a
-// CTA loads feeds RT tiles' MMAs, so for prefill (x converted by the pre-pass,
-// tiles of 256 tokens) the CTA takes two row tiles where that still gives over
-// half a wave of CTAs without split-K.  Measured at M = 2048: 2048 -> 8192 72
-// against 94 us with one row tile; 8192 -> 2048 (64 CTAs of two row tiles) 95 with
-// two-way split-K and 105 with 128-token tiles, against 77-79 with one row tile.
-// Otherwise one row tile and TN = M rounded up to 16 (at most 256).
+// CTA loads feeds RT tiles' MMAs, so for prefill (more than 256 tokens) the CTA
+// takes two row tiles where that still gives over half a wave of CTAs without
+// split-K.  Measured at M = 2048 (int4): 2048 -> 8192 72 against 94 us with one
+// row tile and A in shared memory, 70 against 77 with one row tile and A in
+// tensor memory; 8192 -> 2048 (64 CTAs of two row tiles) 95 with two-way split-K
+// and 105 with 128-token tiles, against 77-79 with one row tile (59 with
+// two-chunk tensor-memory stages).  Otherwise one row tile and TN = M rounded up
+// to 16 (at most 256); long token ranges then refit TN to whole waves.
 struct TcShape {
     int TN, RT;
 };
@@ -1087,7 +1079,7 @@ struct TcShape {
 // full waves of 152 SMs, where 256 give 1.7.
 static int tc_long_tn(int M, int64_t row_units, int sms)
 {
-    if (!kTcFitWaves || M < 1024)
+    if (M < 1024)
         return 256;
     int best = 256;
     int64_t best_cost = -1;
@@ -1106,7 +1098,7 @@ static TcShape tc_shape(int M, int N, int sms)
 {
     const int tn = M > 256 ? 256 : ((M + 15) / 16 * 16 < 16 ? 16 : (M + 15) / 16 * 16);
     const int64_t rows1 = (N + TC_ROWS - 1) / TC_ROWS;
-    if (!kTcTwoRowTiles || !tc_preconvert(M) || M < 256)
+    if (!tc_preconvert(M) || M < 256)
         return {M > 256 ? tc_long_tn(M, rows1, sms) : tn, 1};
     const int64_t pairs = (N + 2 * TC_ROWS - 1) / (2 * TC_ROWS);
     if (pairs * ((M + 255) / 256) * 2 > sms)
@@ -1144,7 +1136,7 @@ static size_t tc_xf16_data_bytes(int M, int K) { return ((size_t)M * K * 2 + 255
 
 // NVFP4 calls take bf16 operands (exact dequantised weights, x as stored): no
 // copy of x.
-static bool tc_bf16_operands(int kind) { return kTcBf16Nvfp4 && kind == W_NVFP4_A16; }
+static bool tc_bf16_operands(int kind) { return kind == W_NVFP4_A16; }
 
 static size_t tc_xf16_bytes(int kind, int M, int K)
 {
@@ -1314,8 +1306,8 @@ q4_status tc_launch(int kind, const void *x, const uint8_t *codes, const void *s
     const bool xb = tc_bf16_operands(kind);
     // (A in tensor memory for int4 tiles of at most 64 tokens, whose x is
     // converted in the kernel, was slower: M = 48 step 31.4 against 27.9 us)
-    const bool atm_skinny = kTcTmemASkinny && xb && !tc_preconvert(M);
-    const bool atm = kTcTmemA && rt == 1 && (tc_preconvert(M) || atm_skinny);
+    const bool atm_skinny = xb && !tc_preconvert(M);
+    const bool atm = rt == 1 && (tc_preconvert(M) || atm_skinny);
     // A in tensor memory: the A sub-tiles after the accumulator, SC 32-column
     // slots per stage
     p.tmem_a0 = (p.TN + 31) / 32 * 32;
