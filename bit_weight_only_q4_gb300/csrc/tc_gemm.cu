@@ -483,7 +483,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 q4_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap wmap,
              TcParams p)
 {
-    static_assert(!ATM || SC <= 2, "A in tensor memory: one or two chunks per stage");
+    static_assert(!ATM || SC <= 4, "A in tensor memory: one, two or four chunks per stage");
     static_assert(RT == 1 || (RT == 2 && SC == 1 && !ATM), "two row tiles: one chunk per stage, A in shared memory");
     static_assert(!XB || LAYOUT == 1, "bf16 operands: NVFP4 only");
     constexpr uint32_t A_BYTES = (uint32_t)RT * TcStage<SC>::A;
@@ -698,7 +698,7 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
             const uint32_t t_lane = (uint32_t)(quad * 32) << 16;
             // int4: scale | min << 16 of the row's group; NVFP4: the e4m3 scales of
             // the thread's 2 SC 16-column groups (low byte first)
-            auto load_scale = [&](int u) -> uint32_t {
+            auto load_scale = [&](int u) -> uint64_t {
                 const int col = (c0 + u * SC) * TC_KC + CPT * h;   // first column
                 if (u >= nsup || !rok || col / TC_KC >= c1)
                     return 0u;
@@ -710,19 +710,24 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
                     const uint8_t *sp = static_cast<const uint8_t *>(p.scale) + n * (p.K / 16) + col / 16;
                     if constexpr (SC == 1)
                         return ld_nc_u16(sp);
-                    else
+                    else if constexpr (SC == 2)
                         return ld_nc_u32(sp);
+                    else {                             // 4-byte aligned only
+                        const uint64_t lo = ld_nc_u32(sp);
+                        // the second chunk of the pair may lie past the row's end
+                        return (col / TC_KC + 1 < c1) ? lo | ((uint64_t)ld_nc_u32(sp + 4) << 32) : lo;
+                    }
                 }
             };
             float bf16_up = 1.f;               // XB: see e4m3_to_bf16x2_scaled
             if constexpr (XB)
                 bf16_up = pow2f_tc(112 + nvfp4_bf16_exponent(__ldg(p.gscale)));
-            uint32_t scq[SA];
+            uint64_t scq[SA];
 #pragma unroll
             for (int j = 0; j < SA; ++j)
                 scq[j] = load_scale(gi + j * G);
             prescale();
-            auto stage = [&](int u, uint32_t sc) -> bool {
+            auto stage = [&](int u, uint64_t sc) -> bool {
                 const int st_i = u % NS, use = u / NS;
                 const unsigned char *st = smem + (size_t)st_i * stage_bytes;
                 if (!mbar_wait_warp(smem_u32(&bars[st_i]), use & 1, p.err))
@@ -733,7 +738,7 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
                 const unsigned char *crow = st + SC * x_stride + row * (32 * SC) + h * (16 * SC);
                 uint32_t m2 = 0u;
                 if constexpr (LAYOUT == 0)
-                    m2 = f16x2_splat(sc >> 16);
+                    m2 = f16x2_splat((uint32_t)(sc >> 16) & 0xffffu);
 #pragma unroll
                 for (int i = 0; i < SC; ++i) {         // 32 columns: 16 packed TMEM columns
                     const uint4 cw = *reinterpret_cast<const uint4 *>(crow + 16 * i);
@@ -743,10 +748,10 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
                     for (int j = 0; j < 4; ++j) {
                         uint32_t s2;
                         if constexpr (LAYOUT == 0) {
-                            s2 = f16x2_splat(sc & 0xffffu);
+                            s2 = f16x2_splat((uint32_t)sc & 0xffffu);
                         } else {
                             // 16-column group (2 i + j / 2) of the thread's columns
-                            const uint32_t b = (sc >> (8 * (2 * i + j / 2))) & 0xffu;
+                            const uint32_t b = (uint32_t)(sc >> (8 * (2 * i + j / 2))) & 0xffu;
                             s2 = XB ? e4m3_to_bf16x2_scaled(b, bf16_up)
                                     : f16x2_splat(e4m3x2_to_f16x2(b) & 0xffffu);
                         }
@@ -1059,6 +1064,9 @@ bool tc_eligible(int kind, int M, int N, int K)
 // (two accumulators fill the tensor memory).
 static bool tc_preconvert(int M) { return M > 64; }
 
+// Chunks per stage of the NVFP4 tiles of at most 64 tokens (A in tensor memory).
+constexpr int kTcSkinnySc = 4;
+
 // CTA tile: TN tokens (MMA N) x RT weight-row tiles of 128.  Each x sub-tile a
 // CTA loads feeds RT tiles' MMAs, so for prefill (more than 256 tokens) the CTA
 // takes two row tiles where that still gives over half a wave of CTAs without
@@ -1197,7 +1205,8 @@ static const void *tc_select_layout(int sc, bool atm, int rt, bool xb)
             if (rt == 2)
                 return reinterpret_cast<const void *>(&q4_tc_kernel<1, 1, 2, false, 2, true>);
             if (atm)
-                return sc == 2 ? reinterpret_cast<const void *>(&q4_tc_kernel<1, 2, 2, true, 1, true>)
+                return sc == 4 ? reinterpret_cast<const void *>(&q4_tc_kernel<1, 4, 2, true, 1, true>)
+                     : sc == 2 ? reinterpret_cast<const void *>(&q4_tc_kernel<1, 2, 2, true, 1, true>)
                                : reinterpret_cast<const void *>(&q4_tc_kernel<1, 1, 2, true, 1, true>);
             return sc == 4 ? reinterpret_cast<const void *>(&q4_tc_kernel<1, 4, 2, false, 1, true>)
                  : sc == 2 ? reinterpret_cast<const void *>(&q4_tc_kernel<1, 2, 2, false, 1, true>)
@@ -1313,7 +1322,7 @@ q4_status tc_launch(int kind, const void *x, const uint8_t *codes, const void *s
     p.tmem_a0 = (p.TN + 31) / 32 * 32;
     const size_t a_bytes = atm ? 0 : 16384 * (size_t)rt;
     const size_t code_bytes = 4096 * (size_t)rt;
-    const int sc_max = atm ? 2 : (rt == 2 ? 1 : 4);
+    const int sc_max = atm ? (atm_skinny ? kTcSkinnySc : 2) : (rt == 2 ? 1 : 4);
     int sc = 1, ns = 0;
     for (int need_ns = atm ? 3 : 4; need_ns >= 2 && ns == 0; --need_ns)
         for (int cand = sc_max; cand >= 1; cand /= 2) {
